@@ -24,6 +24,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _SO = os.path.join(_HERE, "liboracle.so")
+_SO_F32 = os.path.join(_HERE, "liboracle_f32.so")
 _lock = threading.Lock()
 _lib = None
 
@@ -47,13 +48,29 @@ class OrcWeights(ctypes.Structure):
                 ("layers", ctypes.POINTER(OrcLayer))]
 
 
-def build(force: bool = False) -> str:
-    """Compile liboracle.so next to its source (gcc -O3, OpenMP, no fast-math)."""
-    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
-        tmp = _SO + ".%d.tmp" % os.getpid()
-        subprocess.check_call(["gcc", "-O3", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"])
-        os.replace(tmp, _SO)
-    return _SO
+def build(force: bool = False, fp32_accumulation: bool = False) -> str:
+    """Compile liboracle.so next to its source (gcc -O3, OpenMP, no fast-math).
+    fp32_accumulation builds liboracle_f32.so instead (see ORC_ACC_FLOAT in
+    oracle.c): a measuring stick for rounding sensitivity, not the oracle."""
+    so = _SO_F32 if fp32_accumulation else _SO
+    if force or not os.path.exists(so) or os.path.getmtime(so) < os.path.getmtime(_SRC):
+        tmp = so + ".%d.tmp" % os.getpid()
+        flags = ["-DORC_ACC_FLOAT"] if fp32_accumulation else []
+        subprocess.check_call(["gcc", "-O3", "-fopenmp", "-fPIC", "-shared"] + flags + [_SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, so)
+    return so
+
+
+_lib_f32 = None
+
+
+def lib_fp32_accumulation():
+    """The ORC_ACC_FLOAT build (GEMV partial sums rounded to float)."""
+    global _lib_f32
+    with _lock:
+        if _lib_f32 is None:
+            _lib_f32 = load(build(fp32_accumulation=True))
+    return _lib_f32
 
 
 def load(path: str):
@@ -83,6 +100,11 @@ def load(path: str):
     L.orc_decode_step.argtypes = [ctypes.POINTER(OrcConfig), ctypes.POINTER(OrcWeights),
                                   ctypes.c_int, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, vp, vp]
     L.orc_decode_step.restype = ctypes.c_int
+    L.orc_layer_forward.argtypes = [ctypes.POINTER(OrcConfig), ctypes.POINTER(OrcLayer), ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, vp, vp, vp, ctypes.c_int, ctypes.c_int, vp]
+    L.orc_layer_forward.restype = ctypes.c_int
+    L.orc_lm_head.argtypes = [ctypes.POINTER(OrcConfig), ctypes.POINTER(OrcWeights), vp, vp]
+    L.orc_lm_head.restype = None
     return L
 
 
@@ -186,7 +208,8 @@ class Oracle:
     The oracle owns a private copy of the KV cache (``kc``, ``vc``), so the
     caller's cache is never touched."""
 
-    def __init__(self, model, kc: np.ndarray, vc: np.ndarray):
+    def __init__(self, model, kc: np.ndarray, vc: np.ndarray, library=None):
+        self._L = library
         wl = model.wl
         self.model = model
         self.wl = wl
@@ -218,11 +241,35 @@ class Oracle:
         assert pos.size == B
         logits = np.empty((B, self.wl.vocab), dtype=np.float64)
         xt = np.empty((B, self.wl.n_layers + 1, self.wl.hidden), dtype=np.float64) if trace else None
-        rc = lib().orc_decode_step(ctypes.byref(self.cfg), ctypes.byref(self.w), B, _p(tok), _p(pos),
+        rc = (self._L or lib()).orc_decode_step(ctypes.byref(self.cfg), ctypes.byref(self.w), B, _p(tok), _p(pos),
                                    _p(self.kc), _p(self.vc), self.Bmax, self.Smax, _p(logits), _p(xt))
         if rc != 0:
             raise ValueError("oracle rejected the step arguments")
         return (logits, xt) if trace else logits
+
+
+def _layer(self, l: int, b: int, p: int, x: np.ndarray):
+    """Layer l of sequence b at position p from residual x (float64 [H]), against
+    this oracle's caches (slot p of layer l is written).  Returns (x_mid, x_out)."""
+    xo = np.array(x, dtype=np.float64, copy=True)
+    xm = np.empty_like(xo)
+    rc = (self._L or lib()).orc_layer_forward(ctypes.byref(self.cfg), ctypes.byref(self._layers[l]), l, b, p, _p(xo),
+                                 _p(self.kc), _p(self.vc), self.Bmax, self.Smax, _p(xm))
+    if rc != 0:
+        raise ValueError("oracle rejected the layer arguments")
+    return xm, xo
+
+
+def _lm_head(self, x: np.ndarray) -> np.ndarray:
+    """Final norm and LM head from residual x (float64 [H])."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(self.wl.vocab, dtype=np.float64)
+    (self._L or lib()).orc_lm_head(ctypes.byref(self.cfg), ctypes.byref(self.w), _p(x), _p(out))
+    return out
+
+
+Oracle.layer = _layer
+Oracle.lm_head = _lm_head
 
 
 def greedy(logits: np.ndarray):

@@ -44,6 +44,16 @@
 #include <omp.h>
 #endif
 
+/* GEMV accumulator.  The oracle accumulates in double.  Built with
+ * -DORC_ACC_FLOAT it rounds every partial sum to float instead: that build is
+ * not the oracle, it measures how far a plain fp32 implementation of the same
+ * definition lands from it (the model's own rounding sensitivity). */
+#ifdef ORC_ACC_FLOAT
+typedef float acc_t;
+#else
+typedef double acc_t;
+#endif
+
 /* ------------------------------------------------------------ bf16 */
 
 double orc_bf16_to_double(uint16_t b) {
@@ -101,7 +111,7 @@ void orc_gemv(int rows, int K, const void *W, int w_int8, const float *scales,
     for (int i = 0; i < K; ++i) hd[i] = orc_bf16_to_double(h[i]);
 #pragma omp parallel for schedule(static)
     for (int o = 0; o < rows; ++o) {
-        double acc = 0.0;
+        acc_t acc = 0;
         if (w_int8) {
             const int8_t *w = (const int8_t *)W + (size_t)o * K;
             for (int i = 0; i < K; ++i) acc += (double)w[i] * hd[i];
@@ -213,9 +223,79 @@ static void round_vec(int n, const double *y, uint16_t *out) {
 }
 
 /*
+ * Layer l of the decode step of sequence b at position p, applied in place to
+ * the residual x[H].  Writes K/V slot p of (l, b) into the caches (layout
+ * [L][Bmax][n_kv_heads][Smax][head_dim] bf16) before attending over slots
+ * 0..p.  If x_mid is not NULL it receives the residual after attention.
+ */
+int orc_layer_forward(const orc_config *c, const orc_layer *w, int l, int b, int p, double *x,
+                      uint16_t *kcache, uint16_t *vcache, int Bmax, int Smax, double *x_mid) {
+    const int H = c->hidden, nq = c->n_heads, nkv = c->n_kv_heads, d = c->head_dim;
+    const int I = c->intermediate;
+    if (nkv < 1 || nq % nkv != 0 || d % 2 != 0 || p < 0 || p >= Smax || b < 0 || b >= Bmax) return -1;
+    const int G = nq / nkv;
+    const int i8 = c->weight_int8;
+    double *y = malloc(sizeof(double) * (H > I ? H : I));
+    double *q = malloc(sizeof(double) * nq * d), *k = malloc(sizeof(double) * nkv * d);
+    double *v = malloc(sizeof(double) * nkv * d), *o = malloc(sizeof(double) * nq * d);
+    double *gt = malloc(sizeof(double) * I), *up = malloc(sizeof(double) * I);
+    uint16_t *hb = malloc(sizeof(uint16_t) * (H > I ? H : I));
+    uint16_t *ob = malloc(sizeof(uint16_t) * nq * d);
+
+    orc_rmsnorm(H, x, w->attn_norm, c->rms_eps, y);
+    round_vec(H, y, hb);
+    orc_gemv(nq * d, H, w->wq, i8, w->sq, hb, q);
+    orc_gemv(nkv * d, H, w->wk, i8, w->sk, hb, k);
+    orc_gemv(nkv * d, H, w->wv, i8, w->sv, hb, v);
+    for (int j = 0; j < nq; ++j) orc_rope(d, p, c->rope_theta, q + (size_t)j * d);
+    for (int g = 0; g < nkv; ++g) orc_rope(d, p, c->rope_theta, k + (size_t)g * d);
+
+    for (int g = 0; g < nkv; ++g) {
+        size_t row = (((size_t)l * Bmax + b) * nkv + g) * (size_t)Smax;
+        for (int i = 0; i < d; ++i) {
+            kcache[(row + p) * d + i] = orc_double_to_bf16(k[(size_t)g * d + i]);
+            vcache[(row + p) * d + i] = orc_double_to_bf16(v[(size_t)g * d + i]);
+        }
+    }
+#pragma omp parallel for schedule(static)
+    for (int j = 0; j < nq; ++j) {
+        int g = j / G;
+        size_t row = (((size_t)l * Bmax + b) * nkv + g) * (size_t)Smax;
+        orc_attention(p + 1, d, q + (size_t)j * d, kcache + row * d, vcache + row * d, NULL,
+                      o + (size_t)j * d);
+    }
+    round_vec(nq * d, o, ob);
+    orc_gemv(H, nq * d, w->wo, i8, w->so, ob, y);
+    for (int i = 0; i < H; ++i) x[i] += y[i];
+    if (x_mid) memcpy(x_mid, x, sizeof(double) * H);
+
+    orc_rmsnorm(H, x, w->mlp_norm, c->rms_eps, y);
+    round_vec(H, y, hb);
+    orc_gemv(I, H, w->wg, i8, w->sg, hb, gt);
+    orc_gemv(I, H, w->wu, i8, w->su, hb, up);
+    for (int i = 0; i < I; ++i) hb[i] = orc_double_to_bf16(orc_silu(gt[i]) * up[i]);
+    orc_gemv(H, I, w->wd, i8, w->sd, hb, y);
+    for (int i = 0; i < H; ++i) x[i] += y[i];
+
+    free(y); free(q); free(k); free(v); free(o); free(gt); free(up); free(hb); free(ob);
+    return 0;
+}
+
+/* Final RMSNorm and LM head: logits[V] = W_lm bf16(rmsnorm(x) * g_final). */
+void orc_lm_head(const orc_config *c, const orc_weights *wt, const double *x, double *logits) {
+    const int H = c->hidden;
+    double *y = malloc(sizeof(double) * H);
+    uint16_t *hb = malloc(sizeof(uint16_t) * H);
+    orc_rmsnorm(H, x, wt->final_norm, c->rms_eps, y);
+    round_vec(H, y, hb);
+    orc_gemv(c->vocab, H, wt->lm_head, c->lm_head_int8, wt->s_lm, hb, logits);
+    free(y);
+    free(hb);
+}
+
+/*
  * One decode step for B sequences.  Sequence b decodes tokens[b] at
- * positions[b], reading and writing its own rows of the caches
- * kcache/vcache, laid out [L][Bmax][n_kv_heads][Smax][head_dim] bf16.
+ * positions[b], reading and writing its own rows of the caches.
  * logits: [B][vocab] doubles.  x_trace, if not NULL, receives the residual
  * stream [B][L+1][H] at the input of every layer and after the last one.
  * Returns 0, or -1 on bad arguments.
@@ -223,74 +303,23 @@ static void round_vec(int n, const double *y, uint16_t *out) {
 int orc_decode_step(const orc_config *c, const orc_weights *wt, int B, const int32_t *tokens,
                     const int32_t *positions, uint16_t *kcache, uint16_t *vcache, int Bmax, int Smax,
                     double *logits, double *x_trace) {
-    const int L = c->n_layers, H = c->hidden, nq = c->n_heads, nkv = c->n_kv_heads, d = c->head_dim;
-    const int I = c->intermediate, V = c->vocab;
-    if (B < 1 || B > Bmax || nkv < 1 || nq % nkv != 0 || d % 2 != 0) return -1;
-    const int G = nq / nkv;
-    const int i8 = c->weight_int8;
-
-    double *x = malloc(sizeof(double) * H), *y = malloc(sizeof(double) * (H > I ? H : I));
-    double *q = malloc(sizeof(double) * nq * d), *k = malloc(sizeof(double) * nkv * d);
-    double *v = malloc(sizeof(double) * nkv * d), *o = malloc(sizeof(double) * nq * d);
-    double *gt = malloc(sizeof(double) * I), *up = malloc(sizeof(double) * I);
-    uint16_t *hb = malloc(sizeof(uint16_t) * (H > I ? H : I));
-    uint16_t *ob = malloc(sizeof(uint16_t) * nq * d);
-
-    for (int b = 0; b < B; ++b) {
-        const int t = tokens[b], p = positions[b];
-        if (t < 0 || t >= V || p < 0 || p >= Smax) {
-            free(x); free(y); free(q); free(k); free(v); free(o); free(gt); free(up); free(hb); free(ob);
-            return -1;
-        }
-        for (int i = 0; i < H; ++i) x[i] = orc_bf16_to_double(wt->embed[(size_t)t * H + i]);
-
-        for (int l = 0; l < L; ++l) {
-            const orc_layer *w = &wt->layers[l];
+    const int L = c->n_layers, H = c->hidden, V = c->vocab;
+    if (B < 1 || B > Bmax) return -1;
+    for (int b = 0; b < B; ++b)
+        if (tokens[b] < 0 || tokens[b] >= V || positions[b] < 0 || positions[b] >= Smax) return -1;
+    double *x = malloc(sizeof(double) * H);
+    int rc = 0;
+    for (int b = 0; b < B && rc == 0; ++b) {
+        for (int i = 0; i < H; ++i) x[i] = orc_bf16_to_double(wt->embed[(size_t)tokens[b] * H + i]);
+        for (int l = 0; l < L && rc == 0; ++l) {
             if (x_trace) memcpy(x_trace + ((size_t)b * (L + 1) + l) * H, x, sizeof(double) * H);
-
-            orc_rmsnorm(H, x, w->attn_norm, c->rms_eps, y);
-            round_vec(H, y, hb);
-            orc_gemv(nq * d, H, w->wq, i8, w->sq, hb, q);
-            orc_gemv(nkv * d, H, w->wk, i8, w->sk, hb, k);
-            orc_gemv(nkv * d, H, w->wv, i8, w->sv, hb, v);
-            for (int j = 0; j < nq; ++j) orc_rope(d, p, c->rope_theta, q + (size_t)j * d);
-            for (int g = 0; g < nkv; ++g) orc_rope(d, p, c->rope_theta, k + (size_t)g * d);
-
-            for (int g = 0; g < nkv; ++g) {
-                size_t row = (((size_t)l * Bmax + b) * nkv + g) * (size_t)Smax;
-                for (int i = 0; i < d; ++i) {
-                    kcache[(row + p) * d + i] = orc_double_to_bf16(k[(size_t)g * d + i]);
-                    vcache[(row + p) * d + i] = orc_double_to_bf16(v[(size_t)g * d + i]);
-                }
-            }
-#pragma omp parallel for schedule(static)
-            for (int j = 0; j < nq; ++j) {
-                int g = j / G;
-                size_t row = (((size_t)l * Bmax + b) * nkv + g) * (size_t)Smax;
-                orc_attention(p + 1, d, q + (size_t)j * d, kcache + row * d, vcache + row * d, NULL,
-                              o + (size_t)j * d);
-            }
-            round_vec(nq * d, o, ob);
-            orc_gemv(H, nq * d, w->wo, i8, w->so, ob, y);
-            for (int i = 0; i < H; ++i) x[i] += y[i];
-
-            orc_rmsnorm(H, x, w->mlp_norm, c->rms_eps, y);
-            round_vec(H, y, hb);
-            orc_gemv(I, H, w->wg, i8, w->sg, hb, gt);
-            orc_gemv(I, H, w->wu, i8, w->su, hb, up);
-            for (int i = 0; i < I; ++i) hb[i] = orc_double_to_bf16(orc_silu(gt[i]) * up[i]);
-            orc_gemv(H, I, w->wd, i8, w->sd, hb, y);
-            for (int i = 0; i < H; ++i) x[i] += y[i];
+            rc = orc_layer_forward(c, &wt->layers[l], l, b, positions[b], x, kcache, vcache, Bmax, Smax, NULL);
         }
         if (x_trace) memcpy(x_trace + ((size_t)b * (L + 1) + L) * H, x, sizeof(double) * H);
-
-        orc_rmsnorm(H, x, wt->final_norm, c->rms_eps, y);
-        round_vec(H, y, hb);
-        orc_gemv(V, H, wt->lm_head, c->lm_head_int8, wt->s_lm, hb,
-                 logits + (size_t)b * V);
+        if (rc == 0) orc_lm_head(c, wt, x, logits + (size_t)b * V);
     }
-    free(x); free(y); free(q); free(k); free(v); free(o); free(gt); free(up); free(hb); free(ob);
-    return 0;
+    free(x);
+    return rc;
 }
 
 /* exposed for pins of the rounding helper */

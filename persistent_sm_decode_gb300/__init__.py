@@ -1,0 +1,284 @@
+"""GB300-native single-launch decode MegaKernel (sm_103a).
+
+One ``DecodeEngine.step`` runs a whole decode step of a Llama-style decoder
+stack plus LM head as a single persistent-kernel launch (the MegaKernel of the
+Ada-MK technical summary, gist.science, Problem Statement and Methodology).
+This module is the thin Python binding of the C ABI in ``include/amk.h``:
+it marshals arguments (torch tensors are used only as device memory and
+streams) and calls ``libamk.so``.  Every step of the decode path runs in the
+library's CUDA kernel; there is no Python or CPU fallback, and the binding
+raises if the library is missing or rejects a call.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Dict, List, Optional, Sequence
+
+from . import _build
+
+__all__ = ["AmkError", "Config", "ScheduleOptions", "DecodeEngine", "Plan", "lib", "build",
+           "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_OOM", "ERR_SCHEDULE",
+           "ERR_COOPERATIVE", "ERR_TIMEOUT", "WEIGHT_BF16", "WEIGHT_INT8"]
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_SCHEDULE, ERR_COOPERATIVE, ERR_TIMEOUT = range(8)
+WEIGHT_BF16, WEIGHT_INT8 = 0, 1
+OPS = ("QKV", "ATT", "OPR", "GUP", "DWN", "LMH")
+
+i32, i64, f32, f64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_double, ctypes.c_void_p
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("n_layers", i32), ("hidden", i32), ("n_heads", i32), ("n_kv_heads", i32), ("head_dim", i32),
+                ("intermediate", i32), ("vocab", i32), ("rms_eps", f32), ("rope_theta", f32),
+                ("max_batch", i32), ("max_seq", i32), ("weight_dtype", i32), ("tied_embeddings", i32)]
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [(n, vp) for n in ("attn_norm", "mlp_norm", "wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down",
+                                  "s_q", "s_k", "s_v", "s_o", "s_gate", "s_up", "s_down")]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("embed", vp), ("final_norm", vp), ("lm_head", vp), ("s_lm", vp),
+                ("layers", ctypes.POINTER(LayerWeights))]
+
+
+class ScheduleOptions(ctypes.Structure):
+    _fields_ = [("n_sm", i32), ("att_chunks", i32), ("slot_bytes", i32), ("n_slots", i32), ("ksplit", i32),
+                ("scratch_depth", i32), ("l2_prefetch_kb", i32), ("reserved", i32), ("wait_timeout_ns", i64)]
+
+
+class ErrorInfo(ctypes.Structure):
+    _fields_ = [("code", i32), ("sm", i32), ("task", i32), ("counter", i32), ("observed", ctypes.c_uint32),
+                ("target", ctypes.c_uint32)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [(n, i32) for n in ("n_sm", "n_tasks", "n_counters", "n_levels", "att_chunks", "slot_bytes",
+                                   "n_slots", "ksplit", "scratch_depth", "att_tile", "smem_bytes",
+                                   "max_tasks_per_sm")] + \
+               [("weight_bytes", i64), ("scratch_bytes", i64), ("modeled_us", f64), ("search_ms", f64),
+                ("candidates", i32), ("reserved", i32)]
+
+    def as_dict(self) -> dict:
+        return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
+
+
+class AmkError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what, lib().amk_status_string(status).decode(), status))
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libamk.so (nvcc, sm_103a) in-tree."""
+    return _build.build(force=force, verbose=verbose)
+
+
+def lib():
+    """The loaded C library.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_build.LIB):
+                raise RuntimeError("libamk.so is not built; run persistent_sm_decode_gb300.build() "
+                                   "(there is no fallback path)")
+            L = ctypes.CDLL(_build.LIB)
+            L.amk_status_string.argtypes = [ctypes.c_int]
+            L.amk_status_string.restype = ctypes.c_char_p
+            L.amk_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights),
+                                     ctypes.POINTER(ScheduleOptions), ctypes.POINTER(vp)]
+            L.amk_decode_step.argtypes = [vp, i32, vp, vp, vp, vp, vp]
+            L.amk_sync_status.argtypes = [vp]
+            L.amk_destroy.argtypes = [vp]
+            L.amk_last_error.argtypes = [vp, ctypes.POINTER(ErrorInfo)]
+            L.amk_get_plan_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
+            L.amk_debug_drop_signal.argtypes = [vp, i32, i32]
+            L.amk_debug_read_residuals.argtypes = [vp, vp, vp]
+            L.amk_plan_build.argtypes = [ctypes.POINTER(Config), i32, i32, i32, ctypes.POINTER(ScheduleOptions),
+                                         ctypes.POINTER(vp)]
+            L.amk_plan_validate.argtypes = [vp, ctypes.c_char_p, ctypes.c_size_t]
+            L.amk_plan_get_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
+            L.amk_plan_num_tasks.argtypes = [vp, i32]
+            L.amk_plan_num_tasks.restype = i32
+            L.amk_plan_get_task.argtypes = [vp, i32, i32, ctypes.POINTER(i32)]
+            L.amk_plan_mutate.argtypes = [vp, i32, ctypes.c_uint64]
+            L.amk_plan_last_message.restype = ctypes.c_char_p
+            L.amk_plan_destroy.argtypes = [vp]
+            L.amk_plan_destroy.restype = None
+            for f in ("amk_create", "amk_decode_step", "amk_sync_status", "amk_destroy", "amk_last_error",
+                      "amk_get_plan_info", "amk_debug_drop_signal", "amk_debug_read_residuals", "amk_plan_build", "amk_plan_validate",
+                      "amk_plan_get_info", "amk_plan_get_task", "amk_plan_mutate"):
+                getattr(L, f).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != OK:
+        raise AmkError(status, what)
+
+
+def _options(opts: Optional[dict]) -> Optional[ScheduleOptions]:
+    if not opts:
+        return None
+    o = ScheduleOptions()
+    for k, v in opts.items():
+        setattr(o, k, int(v))
+    return o
+
+
+def make_config(n_layers, hidden, n_heads, n_kv_heads, head_dim, intermediate, vocab, max_seq, max_batch=1,
+                rms_eps=1e-5, rope_theta=1e4, int8=False, tied=False) -> Config:
+    return Config(n_layers, hidden, n_heads, n_kv_heads, head_dim, intermediate, vocab, rms_eps, rope_theta,
+                  max_batch, max_seq, WEIGHT_INT8 if int8 else WEIGHT_BF16, int(bool(tied)))
+
+
+# --------------------------------------------------------------- planner
+
+class Plan:
+    """The offline schedule (DAG, search, solidified per-CTA tables, validator)
+    built on the host without a GPU."""
+
+    def __init__(self, cfg: Config, batch: int, n_sm: int, smem_per_cta: int = 232448, options=None):
+        self._p = vp()
+        o = _options(options)
+        st = lib().amk_plan_build(ctypes.byref(cfg), batch, n_sm, smem_per_cta,
+                                  ctypes.byref(o) if o else None, ctypes.byref(self._p))
+        if st != OK:
+            raise AmkError(st, "amk_plan_build: " + lib().amk_plan_last_message().decode())
+        self.n_sm = n_sm
+
+    def info(self) -> dict:
+        pi = PlanInfo()
+        _check(lib().amk_plan_get_info(self._p, ctypes.byref(pi)), "amk_plan_get_info")
+        return pi.as_dict()
+
+    def validate(self):
+        buf = ctypes.create_string_buffer(512)
+        st = lib().amk_plan_validate(self._p, buf, 512)
+        return st, buf.value.decode()
+
+    def tasks(self, sm: int) -> List[dict]:
+        out = []
+        n = lib().amk_plan_num_tasks(self._p, sm)
+        arr = (i32 * 16)()
+        for i in range(n):
+            _check(lib().amk_plan_get_task(self._p, sm, i, arr), "amk_plan_get_task")
+            v = list(arr)
+            out.append({"op": OPS[v[0]], "layer": v[1], "r0": v[2], "r1": v[3], "b": v[4], "g": v[5],
+                        "wait": v[6], "wait_count": v[7], "sig": v[9:9 + v[8]], "mat": v[15]})
+        return out
+
+    def mutate(self, kind: int, seed: int) -> int:
+        return lib().amk_plan_mutate(self._p, kind, seed)
+
+    def close(self):
+        if self._p:
+            lib().amk_plan_destroy(self._p)
+            self._p = vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# --------------------------------------------------------------- engine
+
+_LAYER_KEYS = ("attn_norm", "mlp_norm", "wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+_SCALE_KEYS = ("s_q", "s_k", "s_v", "s_o", "s_gate", "s_up", "s_down")
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("weights and buffers must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("weights and buffers must be contiguous")
+    return t.data_ptr()
+
+
+class DecodeEngine:
+    """A created amk handle plus references to the device tensors it reads.
+
+    ``layers`` is a list of dicts with keys attn_norm, mlp_norm, wq, wk, wv, wo,
+    w_gate, w_up, w_down (and s_q ... s_down for int8 weights); every matrix is
+    [out, in] row-major on the current CUDA device."""
+
+    def __init__(self, cfg: Config, embed, final_norm, layers: Sequence[Dict], lm_head=None, s_lm=None,
+                 options: Optional[dict] = None):
+        self.cfg = cfg
+        self._keep = [embed, final_norm, lm_head, s_lm] + [v for d in layers for v in d.values()]
+        arr = (LayerWeights * cfg.n_layers)()
+        for l, d in enumerate(layers):
+            for k in _LAYER_KEYS + _SCALE_KEYS:
+                setattr(arr[l], k, _ptr(d.get(k)))
+        self._arr = arr
+        w = Weights(_ptr(embed), _ptr(final_norm), _ptr(lm_head), _ptr(s_lm), arr)
+        o = _options(options)
+        self._h = vp()
+        st = lib().amk_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(o) if o else None,
+                              ctypes.byref(self._h))
+        _check(st, "amk_create")
+
+    @property
+    def handle(self) -> int:
+        return self._h.value
+
+    def step(self, tokens, positions, kv_cache, logits, stream=None, batch: Optional[int] = None) -> None:
+        """Enqueue one decode step (device int32 tokens/positions [B], bf16 KV
+        cache [2][L][Bmax][nkv][Smax][d], fp32 logits [B][V])."""
+        B = int(tokens.numel()) if batch is None else int(batch)
+        s = None if stream is None else (stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+        st = lib().amk_decode_step(self._h, B, _ptr(tokens), _ptr(positions), _ptr(kv_cache), _ptr(logits), s)
+        _check(st, "amk_decode_step")
+
+    def step_raw(self, batch: int, tokens: int, positions: int, kv_cache: int, logits: int, stream: int = 0) -> int:
+        """The same call with raw device addresses; returns the status."""
+        return lib().amk_decode_step(self._h, batch, tokens, positions, kv_cache, logits, stream or None)
+
+    def sync(self) -> int:
+        return lib().amk_sync_status(self._h)
+
+    def last_error(self) -> dict:
+        e = ErrorInfo()
+        lib().amk_last_error(self._h, ctypes.byref(e))
+        return {k: getattr(e, k) for k, _ in ErrorInfo._fields_}
+
+    def plan_info(self) -> dict:
+        pi = PlanInfo()
+        _check(lib().amk_get_plan_info(self._h, ctypes.byref(pi)), "amk_get_plan_info")
+        return pi.as_dict()
+
+    def drop_signal(self, sm: int, task: int) -> None:
+        _check(lib().amk_debug_drop_signal(self._h, sm, task), "amk_debug_drop_signal")
+
+    def read_residuals(self):
+        """(x_in [L+1][Bmax][H], x_mid [L][Bmax][H]) of the last step as numpy
+        float32; needs options={"scratch_depth": n_layers + 1}."""
+        import numpy as np
+        L, B, H = self.cfg.n_layers, self.cfg.max_batch, self.cfg.hidden
+        xi = np.empty((L + 1, B, H), dtype=np.float32)
+        xm = np.empty((L, B, H), dtype=np.float32)
+        _check(lib().amk_debug_read_residuals(self._h, xi.ctypes.data, xm.ctypes.data), "amk_debug_read_residuals")
+        return xi, xm
+
+    def close(self) -> None:
+        if self._h:
+            lib().amk_destroy(self._h)
+            self._h = vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,842 @@
+/*
+ * amk_plan.cpp — offline synthesis of the decode MegaKernel's schedule.
+ *
+ * Follows Phase I of the Ada-MK technical summary (gist.science,
+ * Methodology) and the schedule validator of the AutoMegaKernel abstract:
+ *
+ *  1. DAG.  One decode step becomes tile tasks: row blocks of each GEMV (QKV,
+ *     O projection, gate/up, down, LM head) and context chunks of attention
+ *     per (sequence, kv head).  Every task records the activation rectangles
+ *     it reads and writes (RAW/WAR edges are derived from them), and waits on
+ *     a dependency counter that its producers increment.
+ *  2. Shared-memory model.  hardware (bytes per CTA) x model (K, head_dim,
+ *     G) x workload (batch, context) fixes the activation buffer, the result
+ *     buffer and what is left for the weight ring; splitting K shrinks the
+ *     activation slice and so buys ring stages.
+ *  3. Search.  Every feasible (K split, ring slot size, context chunks)
+ *     point is costed with an analytic model of HBM streaming, cross-SM
+ *     dependency latency and what the ring can hide of it; the cheapest wins.
+ *     Options can pin any knob (offline profiling picks them).
+ *  4. Solidify.  The chosen point becomes a static task list per CTA.  The
+ *     kernel walks it without any data-dependent scheduling decision.
+ *  5. Validate.  Deadlock-freedom: program order plus producer->waiter edges
+ *     must be acyclic, every wait must have exactly its count of producers.
+ *     Race-freedom: with vector clocks over CTAs, every conflicting pair of
+ *     accesses (RAW, WAR, WAW, by data version) must be ordered, and every
+ *     read must be covered by writes of the version it expects.
+ */
+#include <algorithm>
+#include <chrono>
+#include <cstdarg>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <string>
+#include <vector>
+
+#include "amk_plan.h"
+#include "amk_plan_impl.h"
+
+using namespace amk;
+
+namespace {
+
+constexpr int MAX_TASK_ROWS = 512;
+
+/* cost-model constants (seconds, bytes/second); refined by offline measurement */
+constexpr double HBM_BPS = 6.5e12;     /* sustained streaming bandwidth of the device */
+constexpr double SM_BPS_MAX = 1.5e11;  /* what one CTA's bulk copies can pull alone */
+constexpr double L2_SM_BPS = 1.5e11;   /* one CTA reading activations from L2 */
+constexpr double T_SYNC = 2.0e-6;      /* producer signal -> consumer sees it -> inputs loaded */
+constexpr double T_TASK = 0.3e-6;      /* per-task fixed cost (barriers, epilogue, signal) */
+
+std::string fmt(const char *f, ...) __attribute__((format(printf, 1, 2)));
+std::string fmt(const char *f, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, f);
+    vsnprintf(buf, sizeof buf, f, ap);
+    va_end(ap);
+    return buf;
+}
+
+int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+struct SmemModel {
+    int act, result, scales, fixed;
+};
+
+int att_smem_need(const Geo &g) {
+    return align_up(g.G * g.d * 4, 16) + align_up(2 * g.d * 2, 16) + NCW * (g.d + PART_PAD) * 4 + 256;
+}
+
+int max_task_rows(const Geo &g, int op, int n_sm) {
+    return std::min(ceil_div(g.rows(op), n_sm), MAX_TASK_ROWS);
+}
+
+SmemModel smem_model(const Geo &g, int ks, int n_sm) {
+    SmemModel m{};
+    m.act = att_smem_need(g);
+    for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN, OP_LMH}) {
+        int kc = g.K(op) / ksplit_for(g, op, ks);
+        m.act = std::max(m.act, g.B * kc * 2);
+        int rows = max_task_rows(g, op, n_sm) + 1;  /* +1: a QKV matrix boundary can split a block */
+        m.result = std::max(m.result, rows * g.nmat(op) * g.B * 4);
+        if (g.scaled(op)) m.scales = std::max(m.scales, rows * g.nmat(op) * 4);
+    }
+    m.act = align_up(m.act, 128);
+    m.result = align_up(m.result, 128);
+    m.scales = align_up(m.scales, 128);
+    m.fixed = SMEM_BARRIERS + SMEM_MISC + m.act + m.result + m.scales;
+    return m;
+}
+
+double model_cost_us(const Geo &g, const Knobs &k, int n_sm) {
+    const double per_sm = HBM_BPS / n_sm;
+    const double ring_hide = (double)k.n_slots * k.slot_bytes / per_sm;
+    auto stall = [&](double pro) { return std::max(0.0, T_SYNC + pro - ring_hide); };
+    double t = 0;
+    for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN}) {
+        double bytes = (double)ceil_div(g.rows(op), n_sm) * g.nmat(op) * g.row_bytes(op);
+        double pro;
+        if (op == OP_OPR) pro = (double)g.B * g.nq * k.C * (g.d + PART_PAD) * 4 / L2_SM_BPS;
+        else if (op == OP_DWN) pro = (double)g.B * g.I * 2 / L2_SM_BPS;
+        else pro = (double)g.B * g.H * 4 / L2_SM_BPS;
+        int ks = ksplit_for(g, op, k.ksplit);
+        t += g.L * (bytes / per_sm + stall(pro) + T_TASK * ks);
+    }
+    {
+        int T = g.B * g.nkv * k.C;
+        double task_bytes = (double)g.Smax / k.C * g.d * 4;
+        int per = ceil_div(T, n_sm), active = std::min(T, n_sm);
+        double bw = std::min(SM_BPS_MAX, HBM_BPS / active);
+        double pro = (double)(g.G + 2) * g.d * 4 / L2_SM_BPS;
+        t += g.L * (per * task_bytes / bw + stall(pro) + T_TASK * per);
+    }
+    {
+        double bytes = (double)ceil_div(g.V, n_sm) * g.row_bytes(OP_LMH);
+        t += bytes / per_sm + stall((double)g.B * g.H * 4 / L2_SM_BPS) + T_TASK;
+    }
+    return t * 1e6;
+}
+
+/* ------------------------------------------------------------ solidify */
+
+struct Builder {
+    const Geo &g;
+    const Knobs &k;
+    int n_sm;
+    amk_plan *P;
+    int per_layer;  /* counters per layer: nkv QKV groups + ATT + OPR + GUP + DWN */
+
+    int cid_group(int l, int grp) const { return l * per_layer + grp; }
+    int cid_att(int l) const { return l * per_layer + g.nkv; }
+    int cid_opr(int l) const { return l * per_layer + g.nkv + 1; }
+    int cid_gup(int l) const { return l * per_layer + g.nkv + 2; }
+    int cid_dwn(int l) const { return l * per_layer + g.nkv + 3; }
+
+    Task base(int op, int l) const {
+        Task t;
+        std::memset(&t, 0, sizeof t);
+        t.op = (uint8_t)op;
+        t.layer = (uint16_t)l;
+        t.wait_id = NO_WAIT;
+        return t;
+    }
+    void add(int sm, const Task &t, std::vector<Access> a) {
+        P->sm_tasks[sm].push_back(t);
+        P->acc[sm].push_back(std::move(a));
+    }
+    Access acc(uint8_t buf, bool w, int version, int b0, int b1, int64_t e0, int64_t e1) const {
+        Access a;
+        a.buf = buf;
+        a.write = w;
+        a.slot = (uint16_t)(buf == BUF_KVNEW || buf == BUF_LOGITS ? 0 : version % k.depth);
+        if (buf == BUF_KVNEW) a.slot = (uint16_t)version;
+        a.version = version;
+        a.b0 = b0;
+        a.b1 = b1;
+        a.e0 = e0;
+        a.e1 = e1;
+        return a;
+    }
+    int rows_per_stage(int op, int ks) const {
+        int kc = g.K(op) / ks;
+        return std::max(1, std::min(256, k.slot_bytes / (kc * g.web(op))));
+    }
+
+    /* Even row split of `op` over CTAs; each CTA's range is cut into tasks of at
+     * most MAX_TASK_ROWS rows (and, for QKV, at matrix and signal-count limits). */
+    void gemv_level(int op, int l) {
+        int rows = g.rows(op);
+        int ks = ksplit_for(g, op, k.ksplit);
+        for (int s = 0; s < n_sm; ++s) {
+            int a = (int)((int64_t)s * rows / n_sm), e = (int)((int64_t)(s + 1) * rows / n_sm);
+            while (a < e) {
+                int b = std::min(e, a + MAX_TASK_ROWS);
+                Task t = base(op, l);
+                t.ksplit = (uint8_t)ks;
+                t.rows_per_stage = (uint16_t)rows_per_stage(op, ks);
+                std::vector<Access> ac;
+                if (op == OP_QKV) {
+                    /* stay inside one matrix and touch at most MAX_SIG groups */
+                    int qd = g.nq * g.d, kd = g.nkv * g.d;
+                    int mat = a < qd ? MAT_Q : a < qd + kd ? MAT_K : MAT_V;
+                    int mat_lo = mat == MAT_Q ? 0 : mat == MAT_K ? qd : qd + kd;
+                    int mat_hi = mat == MAT_Q ? qd : mat == MAT_K ? qd + kd : qd + 2 * kd;
+                    b = std::min(b, mat_hi);
+                    auto group_of = [&](int r) {
+                        int head = (r - mat_lo) / g.d;
+                        return mat == MAT_Q ? head / g.G : head;
+                    };
+                    int g0 = group_of(a);
+                    while (group_of(b - 1) - g0 + 1 > MAX_SIG) --b;
+                    t.mat = (uint8_t)mat;
+                    t.r0 = a - mat_lo;
+                    t.r1 = b - mat_lo;
+                    for (int grp = g0; grp <= group_of(b - 1); ++grp) t.sig[t.nsig++] = (uint16_t)cid_group(l, grp);
+                    if (l > 0) {
+                        t.wait_id = (uint16_t)cid_dwn(l - 1);
+                        ac.push_back(acc(BUF_XIN, false, l, 0, g.B, 0, g.H));
+                    }
+                    ac.push_back(acc(BUF_QKV, true, l, 0, g.B, a, b));
+                } else {
+                    t.r0 = a;
+                    t.r1 = b;
+                    if (op == OP_OPR) {
+                        t.wait_id = (uint16_t)cid_att(l);
+                        t.sig[t.nsig++] = (uint16_t)cid_opr(l);
+                        ac.push_back(acc(BUF_PART, false, l, 0, g.B, 0, (int64_t)g.nkv * k.C * g.G));
+                        if (l > 0) ac.push_back(acc(BUF_XIN, false, l, 0, g.B, a, b));
+                        ac.push_back(acc(BUF_XMID, true, l, 0, g.B, a, b));
+                    } else if (op == OP_GUP) {
+                        t.wait_id = (uint16_t)cid_opr(l);
+                        t.sig[t.nsig++] = (uint16_t)cid_gup(l);
+                        ac.push_back(acc(BUF_XMID, false, l, 0, g.B, 0, g.H));
+                        ac.push_back(acc(BUF_ACT, true, l, 0, g.B, a, b));
+                    } else if (op == OP_DWN) {
+                        t.wait_id = (uint16_t)cid_gup(l);
+                        t.sig[t.nsig++] = (uint16_t)cid_dwn(l);
+                        ac.push_back(acc(BUF_ACT, false, l, 0, g.B, 0, g.I));
+                        ac.push_back(acc(BUF_XMID, false, l, 0, g.B, a, b));
+                        ac.push_back(acc(BUF_XIN, true, l + 1, 0, g.B, a, b));
+                    } else { /* LMH */
+                        t.wait_id = (uint16_t)cid_dwn(g.L - 1);
+                        ac.push_back(acc(BUF_XIN, false, g.L, 0, g.B, 0, g.H));
+                        ac.push_back(acc(BUF_LOGITS, true, 0, 0, g.B, a, b));
+                    }
+                }
+                add(s, t, std::move(ac));
+                a = b;
+            }
+        }
+    }
+
+    void att_level(int l) {
+        int T = g.B * g.nkv * k.C;
+        int qd = g.nq * g.d, kd = g.nkv * g.d;
+        for (int t = 0; t < T; ++t) {
+            int c = t % k.C, grp = (t / k.C) % g.nkv, b = t / (k.C * g.nkv);
+            int sm = (int)((int64_t)t * n_sm / T);
+            Task x = base(OP_ATT, l);
+            x.r0 = c;
+            x.r1 = k.C;
+            x.b = (uint16_t)b;
+            x.g = (uint16_t)grp;
+            x.rows_per_stage = (uint16_t)k.att_tile;
+            x.wait_id = (uint16_t)cid_group(l, grp);
+            x.sig[x.nsig++] = (uint16_t)cid_att(l);
+            if (c == k.C - 1) x.flags |= TF_NEW_TOKEN;
+            std::vector<Access> ac;
+            ac.push_back(acc(BUF_QKV, false, l, b, b + 1, (int64_t)grp * g.G * g.d, (int64_t)(grp + 1) * g.G * g.d));
+            ac.push_back(acc(BUF_QKV, false, l, b, b + 1, qd + (int64_t)grp * g.d, qd + (int64_t)(grp + 1) * g.d));
+            ac.push_back(acc(BUF_QKV, false, l, b, b + 1, qd + kd + (int64_t)grp * g.d, qd + kd + (int64_t)(grp + 1) * g.d));
+            int64_t pr = ((int64_t)grp * k.C + c) * g.G;
+            ac.push_back(acc(BUF_PART, true, l, b, b + 1, pr, pr + g.G));
+            if (x.flags & TF_NEW_TOKEN) ac.push_back(acc(BUF_KVNEW, true, l, b, b + 1, grp, grp + 1));
+            add(sm, x, std::move(ac));
+        }
+    }
+
+    void run() {
+        P->sm_tasks.assign(n_sm, {});
+        P->acc.assign(n_sm, {});
+        per_layer = g.nkv + 4;
+        for (int l = 0; l < g.L; ++l) {
+            gemv_level(OP_QKV, l);
+            att_level(l);
+            gemv_level(OP_OPR, l);
+            gemv_level(OP_GUP, l);
+            gemv_level(OP_DWN, l);
+        }
+        gemv_level(OP_LMH, g.L - 1);
+        P->n_counters = g.L * per_layer;
+        P->n_levels = 5 * g.L + 1;
+        /* wait counts = producers per counter */
+        std::vector<uint32_t> prod(P->n_counters, 0);
+        for (auto &v : P->sm_tasks)
+            for (auto &t : v)
+                for (int i = 0; i < t.nsig; ++i) prod[t.sig[i]]++;
+        for (auto &v : P->sm_tasks)
+            for (auto &t : v)
+                if (t.wait_id != NO_WAIT) t.wait_count = prod[t.wait_id];
+    }
+};
+
+}  // namespace
+
+namespace amk {
+
+Geo make_geo(const amk_config &c, int batch) {
+    Geo g;
+    g.L = c.n_layers;
+    g.H = c.hidden;
+    g.nq = c.n_heads;
+    g.nkv = c.n_kv_heads;
+    g.d = c.head_dim;
+    g.I = c.intermediate;
+    g.V = c.vocab;
+    g.G = c.n_kv_heads > 0 ? c.n_heads / c.n_kv_heads : 0;
+    g.qkv_rows = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+    g.B = batch;
+    g.Smax = c.max_seq;
+    g.i8 = c.weight_dtype == AMK_WEIGHT_INT8;
+    g.lm_i8 = g.i8 && !c.tied_embeddings;
+    return g;
+}
+
+int ksplit_for(const Geo &g, int op, int ks) {
+    int k = std::max(1, ks);
+    while (k > 1 && (g.K(op) % k != 0 || ((g.K(op) / k) * g.web(op)) % 16 != 0)) k /= 2;
+    return k;
+}
+
+ScratchSizes scratch_sizes(const amk_plan &p) {
+    Geo g = make_geo(p.cfg, p.batch);
+    ScratchSizes s;
+    int64_t D = p.k.depth, B = p.cfg.max_batch;
+    s.x_in = D * B * g.H;
+    s.x_mid = D * B * g.H;
+    s.qkv = D * B * g.qkv_rows;
+    s.part = D * B * g.nkv * p.k.C * g.G * (g.d + PART_PAD);
+    s.act = D * B * g.I;
+    return s;
+}
+
+static std::string check_config(const amk_config &c, int batch) {
+    if (c.n_layers < 1 || c.hidden < 16 || c.n_heads < 1 || c.n_kv_heads < 1 || c.intermediate < 16 ||
+        c.vocab < 1 || c.max_seq < 1)
+        return "non-positive dimension";
+    if (c.n_heads % c.n_kv_heads) return "n_heads must be a multiple of n_kv_heads";
+    if (c.head_dim != 64 && c.head_dim != 128) return "head_dim must be 64 or 128";
+    if (c.n_heads / c.n_kv_heads > NCW) return "more than 8 query heads per kv head";
+    if (c.hidden % 16 || (c.n_heads * c.head_dim) % 16 || c.intermediate % 16)
+        return "hidden, n_heads*head_dim and intermediate must be multiples of 16";
+    if (c.hidden > 8192) return "hidden above 8192";
+    if (c.max_batch < 1 || c.max_batch > MAXB) return "max_batch must be 1..8";
+    if (batch < 1 || batch > c.max_batch) return "batch must be 1..max_batch";
+    if (c.weight_dtype != AMK_WEIGHT_BF16 && c.weight_dtype != AMK_WEIGHT_INT8) return "unknown weight dtype";
+    if (c.tied_embeddings && c.weight_dtype == AMK_WEIGHT_INT8) return "tied embeddings need bf16 weights";
+    if (!(c.rms_eps >= 0.0f) || !(c.rope_theta > 0.0f)) return "bad rms_eps or rope_theta";
+    if (c.n_layers > 4096 || (int64_t)c.n_layers * (c.n_kv_heads + 4) >= NO_WAIT) return "too many layers";
+    return "";
+}
+
+amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_cta,
+                      const amk_schedule_options *opt, amk_plan **out, std::string *msg) {
+    auto t0 = std::chrono::steady_clock::now();
+    if (!cfg || !out) {
+        *msg = "NULL argument";
+        return AMK_ERR_INVALID_ARG;
+    }
+    *out = nullptr;
+    std::string bad = check_config(*cfg, batch);
+    if (!bad.empty()) {
+        *msg = bad;
+        return bad.find("must be 64") != std::string::npos || bad.find("above") != std::string::npos ||
+                       bad.find("more than") != std::string::npos
+                   ? AMK_ERR_UNSUPPORTED
+                   : AMK_ERR_INVALID_ARG;
+    }
+    if (n_sm < 1 || n_sm > 4096 || smem_per_cta < 32768) {
+        *msg = "bad n_sm or shared-memory size";
+        return AMK_ERR_INVALID_ARG;
+    }
+    amk_schedule_options o{};
+    if (opt) o = *opt;
+    Geo g = make_geo(*cfg, batch);
+
+    /* ---- search ---- */
+    const int slot_choices[] = {8192, 12288, 16384, 24576, 32768, 49152, 65536};
+    const int ks_choices[] = {1, 2, 4};
+    Knobs best;
+    double best_cost = 1e300;
+    int cands = 0;
+    int maxC = std::max(1, std::min(64, (4 * n_sm) / std::max(1, g.B * g.nkv)));
+    for (int ks : ks_choices) {
+        if (o.ksplit && ks != o.ksplit) continue;
+        SmemModel sm = smem_model(g, ks, n_sm);
+        for (int slot : slot_choices) {
+            if (o.slot_bytes && slot != o.slot_bytes) continue;
+            int avail = smem_per_cta - sm.fixed;
+            int ns = avail / slot;
+            if (o.n_slots) ns = std::min(ns, o.n_slots);
+            ns = std::min(ns, MAX_SLOTS);
+            if (ns < 2) continue;
+            bool fits = true;
+            for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN, OP_LMH})
+                if ((int64_t)(g.K(op) / ksplit_for(g, op, ks)) * g.web(op) > slot) fits = false;
+            if (g.d * 4 > slot) fits = false;
+            if (!fits) continue;
+            for (int C = 1; C <= maxC; ++C) {
+                if (o.att_chunks && C != o.att_chunks) continue;
+                Knobs k;
+                k.C = C;
+                k.slot_bytes = slot;
+                k.n_slots = ns;
+                k.ksplit = ks;
+                k.depth = o.scratch_depth > 0 ? std::min(o.scratch_depth, cfg->n_layers + 1) : 2;
+                k.att_tile = std::min(256, slot / (4 * g.d));
+                k.l2_prefetch_kb = o.l2_prefetch_kb;
+                double c = model_cost_us(g, k, n_sm);
+                ++cands;
+                if (c < best_cost) {
+                    best_cost = c;
+                    best = k;
+                }
+            }
+        }
+    }
+    if (cands == 0) {
+        *msg = "no schedule point fits the shared-memory model";
+        return AMK_ERR_UNSUPPORTED;
+    }
+
+    /* ---- solidify ---- */
+    amk_plan *P = new amk_plan;
+    P->cfg = *cfg;
+    P->batch = batch;
+    P->n_sm = n_sm;
+    P->smem_per_cta = smem_per_cta;
+    P->k = best;
+    Builder bld{g, best, n_sm, P, 0};
+    bld.run();
+    SmemModel sm = smem_model(g, best.ksplit, n_sm);
+    P->act_bytes = sm.act;
+    P->result_bytes = sm.result;
+    P->scale_bytes = sm.scales;
+    P->smem_bytes = sm.fixed + best.n_slots * best.slot_bytes;
+    P->modeled_us = best_cost;
+    P->candidates = cands;
+    int64_t wb = 0;
+    for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN})
+        wb += (int64_t)g.L * g.rows(op) * g.nmat(op) * g.row_bytes(op);
+    wb += (int64_t)g.rows(OP_LMH) * g.row_bytes(OP_LMH);
+    P->weight_bytes = wb;
+    ScratchSizes ss = scratch_sizes(*P);
+    P->scratch_bytes = 4 * (ss.x_in + ss.x_mid + ss.qkv + ss.part) + 2 * ss.act;
+
+    /* ---- validate ---- */
+    std::string why;
+    if (!plan_validate(*P, &why)) {
+        *msg = "schedule rejected: " + why;
+        delete P;
+        return AMK_ERR_SCHEDULE;
+    }
+    P->search_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+    *out = P;
+    return AMK_OK;
+}
+
+/* ------------------------------------------------------------ validator */
+
+bool plan_validate(const amk_plan &p, std::string *msg) {
+    const int n_sm = (int)p.sm_tasks.size();
+    const int NC = p.n_counters;
+    if (n_sm != p.n_sm || p.acc.size() != p.sm_tasks.size()) {
+        *msg = "task and access tables disagree";
+        return false;
+    }
+    /* global ids */
+    std::vector<int> base(n_sm + 1, 0);
+    for (int s = 0; s < n_sm; ++s) base[s + 1] = base[s] + (int)p.sm_tasks[s].size();
+    const int NT = base[n_sm];
+    std::vector<int> sm_of(NT), idx_of(NT);
+    for (int s = 0; s < n_sm; ++s)
+        for (int i = 0; i < (int)p.sm_tasks[s].size(); ++i) {
+            sm_of[base[s] + i] = s;
+            idx_of[base[s] + i] = i;
+        }
+
+    /* 1. structure: counter ids, producers, wait counts */
+    std::vector<std::vector<int>> producers(NC), waiters(NC);
+    for (int s = 0; s < n_sm; ++s)
+        for (int i = 0; i < (int)p.sm_tasks[s].size(); ++i) {
+            const Task &t = p.sm_tasks[s][i];
+            if (t.op >= OP_COUNT) {
+                *msg = fmt("cta %d task %d: unknown op %d", s, i, t.op);
+                return false;
+            }
+            if (t.nsig > MAX_SIG) {
+                *msg = fmt("cta %d task %d: %d signals", s, i, t.nsig);
+                return false;
+            }
+            for (int k = 0; k < t.nsig; ++k) {
+                if (t.sig[k] >= NC) {
+                    *msg = fmt("cta %d task %d: signals unknown counter %d", s, i, t.sig[k]);
+                    return false;
+                }
+                for (int k2 = 0; k2 < k; ++k2)
+                    if (t.sig[k2] == t.sig[k]) {
+                        *msg = fmt("cta %d task %d: signals counter %d twice", s, i, t.sig[k]);
+                        return false;
+                    }
+                if (!(t.flags & TF_SKIP_SIGNAL)) producers[t.sig[k]].push_back(base[s] + i);
+            }
+            if (t.wait_id != NO_WAIT) {
+                if (t.wait_id >= NC) {
+                    *msg = fmt("cta %d task %d: waits on unknown counter %d", s, i, t.wait_id);
+                    return false;
+                }
+                waiters[t.wait_id].push_back(base[s] + i);
+            }
+        }
+    for (int c = 0; c < NC; ++c)
+        for (int w : waiters[c]) {
+            const Task &t = p.sm_tasks[sm_of[w]][idx_of[w]];
+            if (producers[c].empty()) {
+                *msg = fmt("cta %d task %d: waits on counter %d that nothing signals", sm_of[w], idx_of[w], c);
+                return false;
+            }
+            if (t.wait_count != producers[c].size()) {
+                *msg = fmt("cta %d task %d: waits for %u signals of counter %d, which has %zu producers", sm_of[w],
+                           idx_of[w], t.wait_count, c, producers[c].size());
+                return false;
+            }
+        }
+
+    /* 2. deadlock freedom: program order + producer->counter->waiter acyclic (Kahn) */
+    const int NN = NT + NC;
+    std::vector<int> indeg(NN, 0);
+    std::vector<std::vector<int>> out(NN);
+    for (int s = 0; s < n_sm; ++s)
+        for (int i = 1; i < (int)p.sm_tasks[s].size(); ++i) {
+            out[base[s] + i - 1].push_back(base[s] + i);
+            indeg[base[s] + i]++;
+        }
+    for (int c = 0; c < NC; ++c) {
+        for (int pr : producers[c]) {
+            out[pr].push_back(NT + c);
+            indeg[NT + c]++;
+        }
+        for (int w : waiters[c]) {
+            out[NT + c].push_back(w);
+            indeg[w]++;
+        }
+    }
+    std::vector<int> order;
+    order.reserve(NN);
+    for (int v = 0; v < NN; ++v)
+        if (indeg[v] == 0) order.push_back(v);
+    for (size_t h = 0; h < order.size(); ++h)
+        for (int v : out[order[h]])
+            if (--indeg[v] == 0) order.push_back(v);
+    if ((int)order.size() != NN) {
+        for (int v = 0; v < NT; ++v)
+            if (indeg[v] > 0) {
+                *msg = fmt("deadlock: cta %d task %d can never start (cycle through its waits)", sm_of[v], idx_of[v]);
+                return false;
+            }
+        *msg = "deadlock: dependency cycle";
+        return false;
+    }
+
+    /* 3. vector clocks over CTAs */
+    std::vector<int32_t> vc((size_t)NN * n_sm, -1);
+    auto VC = [&](int v) { return &vc[(size_t)v * n_sm]; };
+    std::vector<int> wait_of(NT, -1);
+    for (int c = 0; c < NC; ++c)
+        for (int w : waiters[c]) wait_of[w] = c;
+    for (int v : order) {
+        int32_t *mine = VC(v);
+        if (v < NT) {
+            int s = sm_of[v], i = idx_of[v];
+            if (i > 0) {
+                const int32_t *pv = VC(v - 1);
+                for (int q = 0; q < n_sm; ++q) mine[q] = std::max(mine[q], pv[q]);
+            }
+            if (wait_of[v] >= 0) {
+                const int32_t *cv = VC(NT + wait_of[v]);
+                for (int q = 0; q < n_sm; ++q) mine[q] = std::max(mine[q], cv[q]);
+            }
+            mine[s] = i;
+        } else {
+            for (int pr : producers[v - NT]) {
+                const int32_t *pv = VC(pr);
+                for (int q = 0; q < n_sm; ++q) mine[q] = std::max(mine[q], pv[q]);
+            }
+        }
+    }
+    auto hb = [&](int a, int b) {  /* a's completion happens before b starts */
+        if (a == b) return false;
+        if (sm_of[a] == sm_of[b]) return idx_of[a] < idx_of[b];
+        return VC(b)[sm_of[a]] >= idx_of[a];
+    };
+
+    /* 4. races on activation buffers, by (buffer, slot) and data version */
+    struct Rec {
+        int task;
+        const Access *a;
+    };
+    std::map<std::pair<int, int>, std::map<int, std::pair<std::vector<Rec>, std::vector<Rec>>>> groups;
+    for (int s = 0; s < n_sm; ++s)
+        for (int i = 0; i < (int)p.acc[s].size(); ++i)
+            for (const Access &a : p.acc[s][i]) {
+                auto &vv = groups[{a.buf, a.slot}][a.version];
+                (a.write ? vv.second : vv.first).push_back(Rec{base[s] + i, &a});
+            }
+    auto overlap = [](const Access *x, const Access *y) {
+        return x->b0 < y->b1 && y->b0 < x->b1 && x->e0 < y->e1 && y->e0 < x->e1;
+    };
+    static const char *bufname[BUF_COUNT] = {"x_in", "x_mid", "qkv", "attn_partials", "swiglu_act", "kv_slot", "logits"};
+    auto where = [&](int t) { return fmt("cta %d task %d", sm_of[t], idx_of[t]); };
+    for (auto &gk : groups) {
+        const char *bn = bufname[gk.first.first];
+        auto &byver = gk.second;
+        for (auto it = byver.begin(); it != byver.end(); ++it) {
+            int ver = it->first;
+            auto &reads = it->second.first;
+            auto &writes = it->second.second;
+            /* WAW within a version: one writer per element */
+            for (size_t x = 0; x < writes.size(); ++x)
+                for (size_t y = x + 1; y < writes.size(); ++y)
+                    if (overlap(writes[x].a, writes[y].a)) {
+                        *msg = fmt("%s version %d written twice (%s and %s)", bn, ver, where(writes[x].task).c_str(),
+                                   where(writes[y].task).c_str());
+                        return false;
+                    }
+            /* next version in the same slot */
+            auto nx = std::next(it);
+            const std::vector<Rec> *next_writes = nx != byver.end() ? &nx->second.second : nullptr;
+            for (const Rec &r : reads) {
+                /* RAW: every overlapping writer of this version precedes the read, and they cover it */
+                for (int b = r.a->b0; b < r.a->b1; ++b) {
+                    std::vector<std::pair<int64_t, int64_t>> iv;
+                    for (const Rec &w : writes) {
+                        if (!overlap(r.a, w.a) || b < w.a->b0 || b >= w.a->b1) continue;
+                        if (!hb(w.task, r.task)) {
+                            *msg = fmt("RAW race on %s version %d: %s reads before %s has written", bn, ver,
+                                       where(r.task).c_str(), where(w.task).c_str());
+                            return false;
+                        }
+                        iv.push_back({w.a->e0, w.a->e1});
+                    }
+                    std::sort(iv.begin(), iv.end());
+                    int64_t cur = r.a->e0;
+                    for (auto &pr : iv)
+                        if (pr.first <= cur) cur = std::max(cur, pr.second);
+                    if (cur < r.a->e1) {
+                        *msg = fmt("%s version %d: %s reads element %lld of row %d that no task writes", bn, ver,
+                                   where(r.task).c_str(), (long long)cur, b);
+                        return false;
+                    }
+                }
+                /* WAR: the next version's writers wait for this read */
+                if (next_writes)
+                    for (const Rec &w : *next_writes)
+                        if (overlap(r.a, w.a) && !hb(r.task, w.task)) {
+                            *msg = fmt("WAR race on %s slot %d: %s overwrites (version %d) data %s still reads (version %d)",
+                                       bn, gk.first.second, where(w.task).c_str(), nx->first, where(r.task).c_str(), ver);
+                            return false;
+                        }
+            }
+            /* WAW across versions: older writes precede newer ones */
+            if (next_writes)
+                for (const Rec &w0 : writes)
+                    for (const Rec &w1 : *next_writes)
+                        if (overlap(w0.a, w1.a) && !hb(w0.task, w1.task)) {
+                            *msg = fmt("WAW race on %s slot %d between %s and %s", bn, gk.first.second,
+                                       where(w0.task).c_str(), where(w1.task).c_str());
+                            return false;
+                        }
+        }
+    }
+    return true;
+}
+
+}  // namespace amk
+
+/* ------------------------------------------------------------ C ABI */
+
+static thread_local std::string g_plan_msg;
+
+extern "C" {
+
+amk_status amk_plan_build(const amk_config *config, int32_t batch, int32_t n_sm, int32_t smem_per_cta,
+                          const amk_schedule_options *options, amk_plan **out) {
+    g_plan_msg.clear();
+    return plan_build(config, batch, n_sm, smem_per_cta, options, out, &g_plan_msg);
+}
+
+amk_status amk_plan_validate(const amk_plan *plan, char *msg, size_t msg_len) {
+    if (!plan) return AMK_ERR_INVALID_ARG;
+    std::string why;
+    bool ok = plan_validate(*plan, &why);
+    g_plan_msg = why;
+    if (msg && msg_len) {
+        std::snprintf(msg, msg_len, "%s", why.c_str());
+    }
+    return ok ? AMK_OK : AMK_ERR_SCHEDULE;
+}
+
+amk_status amk_plan_get_info(const amk_plan *p, amk_plan_info *info) {
+    if (!p || !info) return AMK_ERR_INVALID_ARG;
+    std::memset(info, 0, sizeof *info);
+    info->n_sm = p->n_sm;
+    int nt = 0, mx = 0;
+    for (auto &v : p->sm_tasks) {
+        nt += (int)v.size();
+        mx = std::max(mx, (int)v.size());
+    }
+    info->n_tasks = nt;
+    info->max_tasks_per_sm = mx;
+    info->n_counters = p->n_counters;
+    info->n_levels = p->n_levels;
+    info->att_chunks = p->k.C;
+    info->slot_bytes = p->k.slot_bytes;
+    info->n_slots = p->k.n_slots;
+    info->ksplit = p->k.ksplit;
+    info->scratch_depth = p->k.depth;
+    info->att_tile = p->k.att_tile;
+    info->smem_bytes = p->smem_bytes;
+    info->weight_bytes = p->weight_bytes;
+    info->scratch_bytes = p->scratch_bytes;
+    info->modeled_us = p->modeled_us;
+    info->search_ms = p->search_ms;
+    info->candidates = p->candidates;
+    return AMK_OK;
+}
+
+int32_t amk_plan_num_tasks(const amk_plan *p, int32_t sm) {
+    if (!p || sm < 0 || sm >= p->n_sm) return -1;
+    return (int32_t)p->sm_tasks[sm].size();
+}
+
+amk_status amk_plan_get_task(const amk_plan *p, int32_t sm, int32_t idx, int32_t out[16]) {
+    if (!p || !out || sm < 0 || sm >= p->n_sm || idx < 0 || idx >= (int)p->sm_tasks[sm].size())
+        return AMK_ERR_INVALID_ARG;
+    const Task &t = p->sm_tasks[sm][idx];
+    for (int i = 0; i < 16; ++i) out[i] = -1;
+    out[0] = t.op;
+    out[1] = t.layer;
+    out[2] = t.r0;
+    out[3] = t.r1;
+    out[4] = t.b;
+    out[5] = t.g;
+    out[6] = t.wait_id == NO_WAIT ? -1 : t.wait_id;
+    out[7] = (int32_t)t.wait_count;
+    out[8] = t.nsig;
+    for (int i = 0; i < t.nsig && i < MAX_SIG; ++i) out[9 + i] = t.sig[i];
+    out[15] = t.mat;
+    return AMK_OK;
+}
+
+amk_status amk_plan_mutate(amk_plan *p, int32_t kind, uint64_t seed) {
+    if (!p) return AMK_ERR_INVALID_ARG;
+    /* deterministic victim choice */
+    uint64_t x = seed * 0x9E3779B97F4A7C15ull + 0x632BE59BD9B4E019ull;
+    auto rnd = [&](uint64_t n) {
+        x ^= x >> 31;
+        x *= 0xBF58476D1CE4E5B9ull;
+        x ^= x >> 29;
+        return n ? x % n : 0;
+    };
+    std::vector<std::pair<int, int>> waiting, signalling;
+    for (int s = 0; s < p->n_sm; ++s)
+        for (int i = 0; i < (int)p->sm_tasks[s].size(); ++i) {
+            const Task &t = p->sm_tasks[s][i];
+            if (t.wait_id != NO_WAIT) waiting.push_back({s, i});
+            if (t.nsig > 0) signalling.push_back({s, i});
+        }
+    if (waiting.empty() || signalling.empty()) return AMK_ERR_INVALID_ARG;
+    switch (kind) {
+    case 0: {
+        auto v = signalling[rnd(signalling.size())];
+        Task &t = p->sm_tasks[v.first][v.second];
+        int k = (int)rnd(t.nsig);
+        t.sig[k] = t.sig[t.nsig - 1];
+        t.nsig--;
+        return AMK_OK;
+    }
+    case 1: {
+        for (int tries = 0; tries < 64; ++tries) {
+            auto v = waiting[rnd(waiting.size())];
+            Task &t = p->sm_tasks[v.first][v.second];
+            if (t.wait_count > 1) {
+                t.wait_count--;
+                return AMK_OK;
+            }
+        }
+        return AMK_ERR_INVALID_ARG;
+    }
+    case 2: {
+        auto v = waiting[rnd(waiting.size())];
+        Task &t = p->sm_tasks[v.first][v.second];
+        t.wait_id = NO_WAIT;
+        t.wait_count = 0;
+        return AMK_OK;
+    }
+    case 3: {
+        /* move a task that waits in front of the previous task on its CTA that it
+         * (transitively) depends on: pick a task with a wait and hoist it to the
+         * CTA's first position */
+        for (int tries = 0; tries < 64; ++tries) {
+            auto v = waiting[rnd(waiting.size())];
+            if (v.second == 0) continue;
+            auto &list = p->sm_tasks[v.first];
+            auto &al = p->acc[v.first];
+            Task t = list[v.second];
+            auto a = al[v.second];
+            list.erase(list.begin() + v.second);
+            al.erase(al.begin() + v.second);
+            list.insert(list.begin(), t);
+            al.insert(al.begin(), a);
+            return AMK_OK;
+        }
+        return AMK_ERR_INVALID_ARG;
+    }
+    case 4: {
+        /* redirect a wait to another counter with its producer count, so only the
+         * race check can tell */
+        std::vector<uint32_t> prod(p->n_counters, 0);
+        for (auto &v : p->sm_tasks)
+            for (auto &t : v)
+                for (int i = 0; i < t.nsig; ++i)
+                    if (!(t.flags & TF_SKIP_SIGNAL)) prod[t.sig[i]]++;
+        for (int tries = 0; tries < 64; ++tries) {
+            auto v = waiting[rnd(waiting.size())];
+            Task &t = p->sm_tasks[v.first][v.second];
+            int c = (int)rnd(p->n_counters);
+            if (c == t.wait_id || prod[c] == 0) continue;
+            t.wait_id = (uint16_t)c;
+            t.wait_count = prod[c];
+            return AMK_OK;
+        }
+        return AMK_ERR_INVALID_ARG;
+    }
+    case 5: {
+        auto v = waiting[rnd(waiting.size())];
+        p->sm_tasks[v.first][v.second].wait_count++;
+        return AMK_OK;
+    }
+    default:
+        return AMK_ERR_INVALID_ARG;
+    }
+}
+
+const char *amk_plan_last_message(void) { return g_plan_msg.c_str(); }
+
+void amk_plan_destroy(amk_plan *plan) { delete plan; }
+
+}  // extern "C"

@@ -1,0 +1,148 @@
+"""GPU parity: the decode MegaKernel, called through the C ABI, against the CPU
+oracle on seeded synthetic workloads (teacher-forced, see gpu_harness)."""
+import numpy as np
+import pytest
+
+import synth
+from tests.gpu_harness import assert_end_to_end, assert_layers_ok, assert_ok, layerwise, teacher_forced
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import persistent_sm_decode_gb300 as amk
+    amk.build()
+
+
+def test_tiny_32_greedy_steps():
+    res = teacher_forced(synth.workload("tiny"))
+    assert_ok(res)
+    assert res.checked_argmax > 20
+
+
+def test_tiny_w8a16_jittered_scales():
+    wl = synth.workload("tiny", weight_dtype="int8", scale_jitter=0.5)
+    assert_ok(teacher_forced(wl))
+
+
+def test_tiny_batch3_ragged_positions():
+    wl = synth.workload("tiny", batch=3)
+    assert_ok(teacher_forced(wl, steps=8, positions0=[16, 9, 2]))
+
+
+def test_tiny_empty_cache_position_zero():
+    # p = 0 with nothing cached: attention over the single new token returns V
+    wl = synth.workload("tiny", ctx=0)
+    assert_ok(teacher_forced(wl, steps=6))
+
+
+def test_tiny_last_cache_slot():
+    wl = synth.workload("tiny")
+    assert_ok(teacher_forced(wl, steps=3, positions0=[wl.max_seq - 3]))
+
+
+@pytest.mark.parametrize("opts", [
+    {"ksplit": 2}, {"ksplit": 4, "slot_bytes": 8192}, {"att_chunks": 1}, {"att_chunks": 7},
+    {"n_slots": 2, "slot_bytes": 8192}, {"scratch_depth": 1}, {"scratch_depth": 3}, {"n_sm": 5},
+])
+def test_tiny_schedule_variants(opts):
+    wl = synth.workload("tiny", batch=2)
+    assert_ok(teacher_forced(wl, steps=4, options=opts))
+
+
+def test_tiny_32_steps_bit_identical_across_runs():
+    import torch
+    from synth.device import kv_from_device, kv_to_device, model_to_device
+    from tests.gpu_harness import make_engine
+    wl = synth.workload("tiny")
+    model = synth.make_model(wl)
+    kc, vc = synth.make_kv(wl)
+    eng = make_engine(wl, model_to_device(model))
+    runs = []
+    for _ in range(2):
+        kv = kv_to_device(kc, vc)
+        lg = torch.empty((1, wl.vocab), device="cuda")
+        tok, seq = 1, []
+        for s in range(wl.steps):
+            eng.step(torch.tensor([tok], dtype=torch.int32, device="cuda"),
+                     torch.tensor([wl.ctx + s], dtype=torch.int32, device="cuda"), kv, lg)
+            assert eng.sync() == 0
+            seq.append(lg.cpu().numpy().copy())
+            tok = int(np.argmax(seq[-1]))
+        runs.append((np.array(seq), kv_from_device(kv)))
+    np.testing.assert_array_equal(runs[0][0], runs[1][0])
+    np.testing.assert_array_equal(runs[0][1][0], runs[1][1][0])
+    np.testing.assert_array_equal(runs[0][1][1], runs[1][1][1])
+    eng.close()
+
+
+def test_determinism_bit_identical():
+    import torch
+    from synth.device import kv_to_device, model_to_device
+    from tests.gpu_harness import make_engine
+    wl = synth.workload("smollm2_135m")
+    model = synth.make_model(wl)
+    kc, vc = synth.make_kv(wl)
+    dev = model_to_device(model)
+    eng = make_engine(wl, dev)
+    outs = []
+    for _ in range(2):
+        kv = kv_to_device(kc, vc)
+        lg = torch.empty((1, wl.vocab), device="cuda")
+        eng.step(torch.tensor([5], dtype=torch.int32, device="cuda"),
+                 torch.tensor([wl.ctx], dtype=torch.int32, device="cuda"), kv, lg)
+        assert eng.sync() == 0
+        outs.append(lg.cpu().numpy())
+    np.testing.assert_array_equal(outs[0], outs[1])
+    eng.close()
+
+
+# ---- per-layer parity from a shared state, full sizes (the gate) ----
+
+def test_smollm2_135m_per_layer():
+    assert_layers_ok(layerwise(synth.workload("smollm2_135m"), steps=3))
+
+
+def test_tinyllama_1b1_per_layer():
+    assert_layers_ok(layerwise(synth.workload("tinyllama_1b1"), steps=3))
+
+
+def test_tinyllama_1b1_w8a16_per_layer():
+    assert_layers_ok(layerwise(synth.workload("tinyllama_1b1_w8a16", scale_jitter=0.5), steps=3))
+
+
+def test_llama2_7b_per_layer():
+    assert_layers_ok(layerwise(synth.workload("llama2_7b"), steps=2))
+
+
+def test_llama2_7b_batch8_per_layer_sampled_rows():
+    assert_layers_ok(layerwise(synth.workload("llama2_7b_b8"), steps=1, check_rows=[0, 5, 7]))
+
+
+def test_tiny_per_layer_batch4_ragged():
+    wl = synth.workload("tiny", batch=4)
+    assert_layers_ok(layerwise(wl, steps=4, positions0=[16, 0, 30, 47 - 4]))
+
+
+# ---- end to end, teacher-forced over the workloads' step counts ----
+
+def test_smollm2_135m_end_to_end_128_steps():
+    assert_end_to_end(teacher_forced(synth.workload("smollm2_135m"), floor=True))
+
+
+def test_tinyllama_1b1_end_to_end_128_steps():
+    assert_end_to_end(teacher_forced(synth.workload("tinyllama_1b1"), floor=True))
+
+
+def test_tinyllama_1b1_w8a16_end_to_end_128_steps():
+    assert_end_to_end(teacher_forced(synth.workload("tinyllama_1b1_w8a16"), floor=True))
+
+
+def test_llama2_7b_end_to_end():
+    assert_end_to_end(teacher_forced(synth.workload("llama2_7b"), steps=8, check_cache=False, floor=True))
+
+
+def test_llama2_7b_batch8_end_to_end_sampled_rows():
+    wl = synth.workload("llama2_7b_b8")
+    assert_end_to_end(teacher_forced(wl, steps=4, check_rows=[0, 7], check_cache=False, floor=True))

@@ -35,8 +35,8 @@ MUTANTS = {
     "cache_stores_v_as_k": ("kcache[(row + p) * d + i] = orc_double_to_bf16(k[(size_t)g * d + i]);",
                             "kcache[(row + p) * d + i] = orc_double_to_bf16(v[(size_t)g * d + i]);"),
     "k_not_rotated": ("for (int g = 0; g < nkv; ++g) orc_rope(d, p, c->rope_theta, k + (size_t)g * d);", ""),
-    "attn_residual_dropped": ("orc_gemv(H, nq * d, w->wo, i8, w->so, ob, y);\n            for (int i = 0; i < H; ++i) x[i] += y[i];",
-                              "orc_gemv(H, nq * d, w->wo, i8, w->so, ob, y);\n            for (int i = 0; i < H; ++i) x[i] = y[i];"),
+    "attn_residual_dropped": ("orc_gemv(H, nq * d, w->wo, i8, w->so, ob, y);\n    for (int i = 0; i < H; ++i) x[i] += y[i];",
+                              "orc_gemv(H, nq * d, w->wo, i8, w->so, ob, y);\n    for (int i = 0; i < H; ++i) x[i] = y[i];"),
     "swiglu_gate_up_swapped": ("orc_silu(gt[i]) * up[i]", "orc_silu(up[i]) * gt[i]"),
     "silu_wrong_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
     "norm_gains_swapped": ("orc_rmsnorm(H, x, w->attn_norm, c->rms_eps, y);", "orc_rmsnorm(H, x, w->mlp_norm, c->rms_eps, y);"),
