@@ -1,0 +1,357 @@
+"""Benchmark: decode tokens/s and µs/token of the single-launch decode
+MegaKernel on one GB300, with its HBM-roofline fraction.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...      # the CPU oracle on the host cores
+
+A step is one decode step of the whole stack plus LM head (one kernel
+launch) for the workload's batch.  Steps walk the workload's decode window
+(positions ctx .. ctx + steps_of_workload - 1) and wrap around it, so every
+timed step has the workload's context length.  Inputs (weights, KV cache,
+tokens) are seeded, synthetic and resident in HBM before timing; the weights
+alone are larger than L2, so no flush is needed between steps.
+
+Under torchrun (N > 1) every rank runs an independent replica (the decode
+step does not shard: replicas only); the value is the tokens of all ranks
+divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s & µs/token at batch 1 (1 GB300); % of 8 TB/s HBM roofline"
+DEFAULT_WORKLOAD = "tinyllama_1b1"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["persistent_sm_decode_gb300/csrc/amk_kernel.cu", "persistent_sm_decode_gb300/csrc/amk_internal.h"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    try:
+        mp = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return float(mp["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def step_bytes(wl, position: int, batch: int) -> int:
+    """Algorithmic HBM bytes of one decode step: every linear weight (+ int8
+    scales) and norm gain once, one embedding row per sequence, K and V of
+    positions 0..p-1 read, K and V of slot p written, fp32 logits written."""
+    kv = batch * wl.n_layers * wl.n_kv_heads * wl.head_dim * 2 * 2 * (position + 1)
+    return wl.weight_bytes() + batch * wl.hidden * 2 + kv + batch * wl.vocab * 4
+
+
+class ClockSampler:
+    """nvidia-smi samples of the GPU clocks and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_model() -> str:
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu part")):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def time_oracle(model, kc, vc, wl, budget_s: float, max_steps: int):
+    """The oracle as it stands on the host cores: decode steps of the workload
+    until the budget or max_steps is reached.  Returns (tokens/s, steps, threads)."""
+    import numpy as np
+    import oracle
+    orc = oracle.Oracle(model, kc, vc)
+    B = kc.shape[1]
+    tok = np.array([(1 + 7919 * b) % wl.vocab for b in range(B)], dtype=np.int32)
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_steps:
+        lg = orc.step(tok, np.full(B, wl.ctx + (n % wl.steps), dtype=np.int32))
+        tok = np.argmax(lg, axis=1).astype(np.int32)
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return B * n / dt, n, oracle.num_threads(), dt
+
+
+def traffic_from_profile(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source."""
+    try:
+        t = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+        e = t.get(workload)
+        if e and e.get("kernel_sha") == kernel_hash():
+            return e["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+def reference_arm(args, wl, rank, world):
+    """The oracle on host cores, on this arm's config/metric/unit."""
+    if rank != 0:
+        return 0
+    import numpy as np
+    import synth
+    model = synth.make_model(wl, seed=1)
+    kc, vc = synth.make_kv(wl, seed=2)
+    # warm-up steps, then the timed ones, within a few minutes in total
+    time_oracle(model, kc, vc, wl, budget_s=10.0, max_steps=args.warmup)
+    tps, n, threads, dt = time_oracle(model, kc, vc, wl, budget_s=90.0, max_steps=args.steps)
+    line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": world,
+            "steps": n, "warmup": args.warmup, "ms_per_step": 1e3 * dt / n, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_block(wl),
+            "cpu_baseline": {"kind": "oracle", "value": tps, "unit": "tokens/s", "cores": threads,
+                             "sample": "%d of %d requested decode steps of %s timed (%.1f s budget) on %s"
+                                       % (n, args.steps, wl.name, 90.0, cpu_model())},
+            "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_block(wl):
+    return {"workload": wl.name, "batch": wl.batch, "context": wl.ctx, "decode_window": wl.steps,
+            "shape": "L%d H%d q%d kv%d d%d I%d V%d %s%s" % (wl.n_layers, wl.hidden, wl.n_heads, wl.n_kv_heads,
+                                                        wl.head_dim, wl.intermediate, wl.vocab, wl.weight_dtype,
+                                                        " tied" if wl.tied else ""),
+            "l2": "weights %.2f GB per step > 129 MB L2: no flush needed" % (wl.weight_bytes() / 1e9)}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2560)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="amk", choices=["amk", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--option", action="append", default=[], help="schedule option key=value (offline tuning)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    import synth
+    wl = synth.workload(args.workload)
+
+    if args.impl == "reference":
+        return reference_arm(args, wl, rank, world)
+
+    import numpy as np
+    import torch
+    import persistent_sm_decode_gb300 as amk
+    from synth.device import kv_to_device, model_to_device
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    amk.build()
+    model = synth.make_model(wl, seed=1)
+    kc, vc = synth.make_kv(wl, seed=2)
+    dev = model_to_device(model)
+    kv = kv_to_device(kc, vc)
+    opts = {}
+    for kvp in args.option:
+        k, v = kvp.split("=")
+        opts[k] = int(v)
+    cfg = amk.make_config(wl.n_layers, wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.intermediate,
+                          wl.vocab, wl.max_seq, wl.batch, wl.rms_eps, wl.rope_theta,
+                          int8=wl.weight_dtype == "int8", tied=wl.tied)
+    eng = amk.DecodeEngine(cfg, dev["embed"], dev["final_norm"], dev["layers"], dev["lm_head"], dev["s_lm"],
+                           opts or None)
+    B = wl.batch
+    stream = torch.cuda.current_stream()
+    window = wl.steps
+    # token and position streams, resident on the device
+    rng = np.random.default_rng(3)
+    tok_host = rng.integers(0, wl.vocab, size=(window, B)).astype(np.int32)
+    pos_host = (wl.ctx + np.arange(window, dtype=np.int32))[:, None].repeat(B, axis=1)
+    tok_dev = torch.from_numpy(tok_host).cuda()
+    pos_dev = torch.from_numpy(np.ascontiguousarray(pos_host)).cuda()
+    logits = torch.empty((B, wl.vocab), dtype=torch.float32, device="cuda")
+    h = eng.handle
+    lib = amk.lib()
+    s_ptr = stream.cuda_stream
+
+    def launch(i):
+        j = i % window
+        st = lib.amk_decode_step(h, B, tok_dev[j].data_ptr(), pos_dev[j].data_ptr(), kv.data_ptr(),
+                                 logits.data_ptr(), s_ptr)
+        if st != amk.OK:
+            raise amk.AmkError(st, "amk_decode_step")
+
+    for i in range(args.warmup):
+        launch(i)
+    st = eng.sync()
+    if st != amk.OK:
+        raise amk.AmkError(st, "warm-up: %s" % eng.last_error())
+
+    # ---- device-timed region: inputs resident, one launch per step ----
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        ev0.record(stream)
+        for i in range(args.steps):
+            launch(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    st = eng.sync()
+    if st != amk.OK:
+        raise amk.AmkError(st, "timed region: %s" % eng.last_error())
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * B * args.steps / (ms / 1e3)
+
+    # ---- roofline of the (single) kernel ----
+    positions = [wl.ctx + (i % window) for i in range(args.steps)]
+    alg_bytes = statistics.fmean(step_bytes(wl, p, B) for p in positions)
+    peak, peak_src = measured_peak()
+    achieved = alg_bytes / (ms_per_step / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic_from_profile(wl.name), "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": alg_bytes,
+                "frac_of_8TBps": achieved / NOMINAL_HBM_GBS, "kernel": "amk_decode_kernel"}
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        tok_pin = torch.from_numpy(tok_host).pin_memory()
+        pos_pin = torch.from_numpy(np.ascontiguousarray(pos_host)).pin_memory()
+        out_pin = torch.empty((B, wl.vocab), dtype=torch.float32).pin_memory()
+        t_in = torch.empty((B,), dtype=torch.int32, device="cuda")
+        p_in = torch.empty((B,), dtype=torch.int32, device="cuda")
+        n_e2e = min(args.steps, 512)
+        for i in range(8):
+            t_in.copy_(tok_pin[i % window], non_blocking=True)
+            p_in.copy_(pos_pin[i % window], non_blocking=True)
+            eng.step(t_in, p_in, kv, logits, stream=stream)
+            out_pin.copy_(logits, non_blocking=True)
+            stream.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(n_e2e):
+            t_in.copy_(tok_pin[i % window], non_blocking=True)
+            p_in.copy_(pos_pin[i % window], non_blocking=True)
+            eng.step(t_in, p_in, kv, logits, stream=stream)
+            out_pin.copy_(logits, non_blocking=True)
+            stream.synchronize()   # the host needs the logits before it can pick the next token
+        dt = time.perf_counter() - t0
+        if dist:
+            t = torch.tensor([dt], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            dt = float(t.item())
+        e2e = {"value": world * B * n_e2e / dt, "unit": "tokens/s", "h2d_bytes_per_step": 2 * B * 4,
+               "d2h_bytes_per_step": B * wl.vocab * 4, "steps": n_e2e, "us_per_token": 1e6 * dt / (B * n_e2e)}
+        assert eng.sync() == amk.OK
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, n, threads, dt = time_oracle(model, kc, vc, wl, budget_s=15.0, max_steps=10 ** 6)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": "%d decode steps of %s (%.1f s) on %s" % (n, wl.name, dt, cpu_model())}
+
+    plan = eng.plan_info()
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_token": 1e3 * ms_per_step / B,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": config_block(wl),
+                "clocks": clocks.summary(), "e2e": e2e, "gpu_launches": args.steps,
+                "roofline": roofline, "cpu_baseline": cpu,
+                "schedule": {k: plan[k] for k in ("n_sm", "att_chunks", "slot_bytes", "n_slots", "ksplit",
+                                                  "scratch_depth", "smem_bytes", "n_tasks")}}
+        print(json.dumps(line), flush=True)
+    eng.close()
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -115,7 +115,7 @@ typedef struct amk_schedule_options {
     int32_t ksplit;          /* K-dimension split of GEMV tiles (1, 2, 4) */
     int32_t scratch_depth;   /* layers of activation scratch kept before reuse (>= 1) */
     int32_t l2_prefetch_kb;  /* bytes the loader prefetches into L2 ahead of the ring, KB; -1 none */
-    int32_t reserved;
+    int32_t trace;           /* 1: record per-task timestamps of every step (amk_debug_read_trace) */
     int64_t wait_timeout_ns; /* bound on every device-side wait; 0: 1 s */
 } amk_schedule_options;
 
@@ -194,6 +194,18 @@ amk_status amk_debug_drop_signal(amk_handle *h, int32_t sm, int32_t task);
  * [n_layers][max_batch][hidden], the residual after each layer's attention.
  * Synchronises the device first. */
 amk_status amk_debug_read_residuals(const amk_handle *h, float *x_in, float *x_mid);
+
+/* Test and tuning support: per-task timings of the last step of a handle
+ * created with options.trace = 1 (else AMK_ERR_UNSUPPORTED).  For every task
+ * of every CTA, in CTA order then task order, sixteen uint64 entries:
+ * globaltimer times (ns) [0] task start, [1] dependency met, [2] first tile
+ * arrived, [3] end (after the completion signal), [6] prologue done (GEMV),
+ * [7] last tile consumed (GEMV), [8] epilogue written (GEMV); durations (ns)
+ * [4] consumer warp 0 waiting for tiles, [5] consumer warp 0 computing tiles,
+ * [9] the loader waiting for free ring slots while issuing the task's tiles;
+ * other entries are unused (0).  `out` holds n_tasks * 16 entries (n_tasks
+ * from amk_get_plan_info); synchronises the device first. */
+amk_status amk_debug_read_trace(const amk_handle *h, uint64_t *out, size_t n_entries);
 
 #ifdef __cplusplus
 }

@@ -24,7 +24,7 @@ __all__ = ["AmkError", "Config", "ScheduleOptions", "DecodeEngine", "Plan", "lib
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_SCHEDULE, ERR_COOPERATIVE, ERR_TIMEOUT = range(8)
 WEIGHT_BF16, WEIGHT_INT8 = 0, 1
-OPS = ("QKV", "ATT", "OPR", "GUP", "DWN", "LMH")
+OPS = ("QKV", "ATT", "OPR", "GUP", "DWN", "LMH", "MRG")
 
 i32, i64, f32, f64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_double, ctypes.c_void_p
 
@@ -47,7 +47,7 @@ class Weights(ctypes.Structure):
 
 class ScheduleOptions(ctypes.Structure):
     _fields_ = [("n_sm", i32), ("att_chunks", i32), ("slot_bytes", i32), ("n_slots", i32), ("ksplit", i32),
-                ("scratch_depth", i32), ("l2_prefetch_kb", i32), ("reserved", i32), ("wait_timeout_ns", i64)]
+                ("scratch_depth", i32), ("l2_prefetch_kb", i32), ("trace", i32), ("wait_timeout_ns", i64)]
 
 
 class ErrorInfo(ctypes.Structure):
@@ -101,6 +101,7 @@ def lib():
             L.amk_get_plan_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
             L.amk_debug_drop_signal.argtypes = [vp, i32, i32]
             L.amk_debug_read_residuals.argtypes = [vp, vp, vp]
+            L.amk_debug_read_trace.argtypes = [vp, vp, ctypes.c_size_t]
             L.amk_plan_build.argtypes = [ctypes.POINTER(Config), i32, i32, i32, ctypes.POINTER(ScheduleOptions),
                                          ctypes.POINTER(vp)]
             L.amk_plan_validate.argtypes = [vp, ctypes.c_char_p, ctypes.c_size_t]
@@ -113,7 +114,7 @@ def lib():
             L.amk_plan_destroy.argtypes = [vp]
             L.amk_plan_destroy.restype = None
             for f in ("amk_create", "amk_decode_step", "amk_sync_status", "amk_destroy", "amk_last_error",
-                      "amk_get_plan_info", "amk_debug_drop_signal", "amk_debug_read_residuals", "amk_plan_build", "amk_plan_validate",
+                      "amk_get_plan_info", "amk_debug_drop_signal", "amk_debug_read_residuals", "amk_debug_read_trace", "amk_plan_build", "amk_plan_validate",
                       "amk_plan_get_info", "amk_plan_get_task", "amk_plan_mutate"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
@@ -271,6 +272,15 @@ class DecodeEngine:
         xm = np.empty((L, B, H), dtype=np.float32)
         _check(lib().amk_debug_read_residuals(self._h, xi.ctypes.data, xm.ctypes.data), "amk_debug_read_residuals")
         return xi, xm
+
+    def read_trace(self):
+        """[n_tasks][16] timestamps and durations (ns) of the last step (needs
+        options={"trace": 1}), tasks in CTA order; see amk_debug_read_trace."""
+        import numpy as np
+        n = self.plan_info()["n_tasks"]
+        out = np.zeros((n, 16), dtype=np.uint64)
+        _check(lib().amk_debug_read_trace(self._h, out.ctypes.data, out.size), "amk_debug_read_trace")
+        return out
 
     def close(self) -> None:
         if self._h:

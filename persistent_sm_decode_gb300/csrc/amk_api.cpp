@@ -28,11 +28,11 @@ struct amk_handle {
     Task *d_tasks = nullptr;
     int32_t *d_start = nullptr;
     LayerPtrs *d_layers = nullptr;
-    uint32_t *d_counters = nullptr;
     uint32_t *d_err = nullptr;
     float *d_rope = nullptr;
     uint8_t *d_scratch = nullptr;
-    size_t counters_bytes = 0;
+    size_t scratch_bytes = 0;
+    unsigned long long *d_trace = nullptr;
     Params params;
     uint32_t epoch = 0;
     cudaStream_t last_stream = nullptr;
@@ -55,10 +55,10 @@ void free_handle(amk_handle *h) {
     cudaFree(h->d_tasks);
     cudaFree(h->d_start);
     cudaFree(h->d_layers);
-    cudaFree(h->d_counters);
     cudaFree(h->d_err);
     cudaFree(h->d_rope);
     cudaFree(h->d_scratch);
+    cudaFree(h->d_trace);
     if (h->plan) amk_plan_destroy(h->plan);
     delete h;
 }
@@ -184,13 +184,14 @@ amk_status amk_create(const amk_config *config, const amk_weights *weights, cons
             rope[(size_t)p * d + 2 * i] = (float)std::cos(th);
             rope[(size_t)p * d + 2 * i + 1] = (float)std::sin(th);
         }
+    /* activation scratch: epoch-tagged 8-byte words, zero (epoch 0) at start */
     ScratchSizes ss = scratch_sizes(P);
-    const size_t f4 = 4;
-    size_t off_xin = 0, off_xmid = off_xin + ss.x_in * f4, off_qkv = off_xmid + ss.x_mid * f4;
-    size_t off_part = off_qkv + ss.qkv * f4, off_act = off_part + ss.part * f4;
-    size_t scratch_bytes = ((off_act + ss.act * 2) + 255) / 256 * 256;
-    h->counters_bytes = (size_t)P.n_counters * COUNTER_STRIDE * 4;
-
+    const size_t w8 = 8;
+    size_t off_xin = 0, off_xmid = off_xin + ss.x_in * w8, off_qkv = off_xmid + ss.x_mid * w8;
+    size_t off_part = off_qkv + ss.qkv * w8, off_aout = off_part + ss.part * w8;
+    size_t off_act = off_aout + ss.aout * w8;
+    size_t scratch_bytes = ((off_act + ss.act * w8) + 255) / 256 * 256;
+    h->scratch_bytes = scratch_bytes;
     cudaError_t e = cudaSuccess;
     auto chk = [&](cudaError_t x) {
         if (e == cudaSuccess) e = x;
@@ -198,16 +199,16 @@ amk_status amk_create(const amk_config *config, const amk_weights *weights, cons
     chk(cudaMalloc(&h->d_tasks, sizeof(Task) * std::max<size_t>(1, h->h_tasks.size())));
     chk(cudaMalloc(&h->d_start, sizeof(int32_t) * (n_sm + 1)));
     chk(cudaMalloc(&h->d_layers, sizeof(LayerPtrs) * L));
-    chk(cudaMalloc(&h->d_counters, h->counters_bytes));
     chk(cudaMalloc(&h->d_err, sizeof(uint32_t) * ERR_WORDS));
     chk(cudaMalloc(&h->d_rope, sizeof(float) * rope.size()));
     chk(cudaMalloc(&h->d_scratch, scratch_bytes));
+    if (options && options->trace)
+        chk(cudaMalloc(&h->d_trace, sizeof(unsigned long long) * 16 * std::max<size_t>(1, h->h_tasks.size())));
     if (e == cudaSuccess) {
         chk(cudaMemcpy(h->d_tasks, h->h_tasks.data(), sizeof(Task) * h->h_tasks.size(), cudaMemcpyHostToDevice));
         chk(cudaMemcpy(h->d_start, h->h_start.data(), sizeof(int32_t) * (n_sm + 1), cudaMemcpyHostToDevice));
         chk(cudaMemcpy(h->d_layers, lp.data(), sizeof(LayerPtrs) * L, cudaMemcpyHostToDevice));
         chk(cudaMemcpy(h->d_rope, rope.data(), sizeof(float) * rope.size(), cudaMemcpyHostToDevice));
-        chk(cudaMemset(h->d_counters, 0, h->counters_bytes));
         chk(cudaMemset(h->d_err, 0, sizeof(uint32_t) * ERR_WORDS));
         chk(cudaMemset(h->d_scratch, 0, scratch_bytes));
         chk(cudaDeviceSynchronize());
@@ -245,21 +246,23 @@ amk_status amk_create(const amk_config *config, const amk_weights *weights, cons
     p.act_bytes = P.act_bytes;
     p.result_bytes = P.result_bytes;
     p.scale_bytes = P.scale_bytes;
+    p.fac_bytes = P.fac_bytes;
     p.l2_prefetch_bytes = P.k.l2_prefetch_kb > 0 ? P.k.l2_prefetch_kb * 1024 : 0;
     p.layers = h->d_layers;
     p.embed = (const uint16_t *)weights->embed;
     p.final_norm = (const uint16_t *)weights->final_norm;
     p.lm = config->tied_embeddings ? weights->embed : weights->lm_head;
     p.s_lm = config->tied_embeddings ? nullptr : weights->s_lm;
-    p.x_in = (float *)(h->d_scratch + off_xin);
-    p.x_mid = (float *)(h->d_scratch + off_xmid);
-    p.qkv = (float *)(h->d_scratch + off_qkv);
-    p.part = (float *)(h->d_scratch + off_part);
-    p.act = (uint16_t *)(h->d_scratch + off_act);
-    p.counters = h->d_counters;
+    p.x_in = (uint64_t *)(h->d_scratch + off_xin);
+    p.x_mid = (uint64_t *)(h->d_scratch + off_xmid);
+    p.qkv = (uint64_t *)(h->d_scratch + off_qkv);
+    p.part = (uint64_t *)(h->d_scratch + off_part);
+    p.aout = (uint64_t *)(h->d_scratch + off_aout);
+    p.act = (uint64_t *)(h->d_scratch + off_act);
     p.err = h->d_err;
     p.rope = h->d_rope;
     p.timeout_ns = (options && options->wait_timeout_ns > 0) ? options->wait_timeout_ns : 1000000000LL;
+    p.trace = h->d_trace;
     *out = h;
     return AMK_OK;
 }
@@ -280,6 +283,7 @@ amk_status amk_decode_step(amk_handle *h, int32_t batch, const int32_t *tokens, 
     p.logits = logits;
     p.batch = batch;
     p.epoch = ++h->epoch;
+    p.epoch_base = p.epoch * (uint32_t)(h->cfg.n_layers + 1);
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = launch_decode(h->fn, p, h->n_sm, h->plan->smem_bytes, s);
     if (e != cudaSuccess) {
@@ -303,11 +307,11 @@ amk_status amk_sync_status(amk_handle *h) {
     h->last_err.counter = (int32_t)err[3];
     h->last_err.observed = err[4];
     h->last_err.target = err[5];
-    /* counters may be anywhere after an aborted step: restart the epochs */
-    cudaError_t e = cudaMemset(h->d_counters, 0, h->counters_bytes);
-    if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(uint32_t) * ERR_WORDS);
+    /* Words an aborted step published carry its epoch; later steps use larger
+     * epochs, so none of them can be taken for current data.  Only the error
+     * word needs clearing. */
+    cudaError_t e = cudaMemset(h->d_err, 0, sizeof(uint32_t) * ERR_WORDS);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
-    h->epoch = 0;
     if (e != cudaSuccess) return cuda_fail(e);
     return err[0] == 4 ? AMK_ERR_INVALID_ARG : AMK_ERR_TIMEOUT;
 }
@@ -347,9 +351,28 @@ amk_status amk_debug_read_residuals(const amk_handle *h, float *x_in, float *x_m
     if (h->params.depth != L + 1) return AMK_ERR_UNSUPPORTED;
     const size_t per = (size_t)h->cfg.max_batch * h->cfg.hidden;
     if (cudaDeviceSynchronize() != cudaSuccess) return cuda_fail(cudaErrorUnknown);
-    cudaError_t e = cudaMemcpy(x_in, h->params.x_in, sizeof(float) * per * (L + 1), cudaMemcpyDeviceToHost);
-    if (e == cudaSuccess) e = cudaMemcpy(x_mid, h->params.x_mid, sizeof(float) * per * L, cudaMemcpyDeviceToHost);
-    return cuda_fail(e);
+    std::vector<uint64_t> w(per * (L + 1));
+    cudaError_t e = cudaMemcpy(w.data(), h->params.x_in, sizeof(uint64_t) * per * (L + 1), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    for (size_t i = 0; i < w.size(); ++i) {
+        const uint32_t u = (uint32_t)w[i];
+        std::memcpy(&x_in[i], &u, 4);
+    }
+    e = cudaMemcpy(w.data(), h->params.x_mid, sizeof(uint64_t) * per * L, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    for (size_t i = 0; i < per * L; ++i) {
+        const uint32_t u = (uint32_t)w[i];
+        std::memcpy(&x_mid[i], &u, 4);
+    }
+    return AMK_OK;
+}
+
+amk_status amk_debug_read_trace(const amk_handle *h, uint64_t *out, size_t n_entries) {
+    if (!h || !out) return AMK_ERR_INVALID_ARG;
+    if (!h->d_trace) return AMK_ERR_UNSUPPORTED;
+    if (n_entries < 16 * h->h_tasks.size()) return AMK_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return cuda_fail(cudaErrorUnknown);
+    return cuda_fail(cudaMemcpy(out, h->d_trace, sizeof(uint64_t) * 16 * h->h_tasks.size(), cudaMemcpyDeviceToHost));
 }
 
 }  // extern "C"

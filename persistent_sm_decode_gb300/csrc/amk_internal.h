@@ -16,8 +16,9 @@ namespace amk {
 
 /* Task kinds: one per operator of the decode step.  QKV, OPR, GUP, DWN and
  * LMH are row blocks of a GEMV (each fused with its prologue/epilogue),
- * ATT is one context chunk of one (sequence, kv head). */
-enum : uint8_t { OP_QKV = 0, OP_ATT = 1, OP_OPR = 2, OP_GUP = 3, OP_DWN = 4, OP_LMH = 5, OP_COUNT = 6 };
+ * ATT is one context chunk of one (sequence, kv head), MRG merges the chunks
+ * of one (sequence, kv head) into its heads' attention output. */
+enum : uint8_t { OP_QKV = 0, OP_ATT = 1, OP_OPR = 2, OP_GUP = 3, OP_DWN = 4, OP_LMH = 5, OP_MRG = 6, OP_COUNT = 7 };
 
 enum : uint8_t {
     TF_SKIP_SIGNAL = 1u, /* debug: do not signal on completion (timeout tests) */
@@ -32,7 +33,6 @@ constexpr int MAX_SIG = 6;
 constexpr int NCW = 8;                    /* consumer warps per CTA */
 constexpr int NTHREADS = (NCW + 1) * 32;  /* + one loader warp */
 constexpr int MAXB = 8;                   /* sequences per step */
-constexpr int COUNTER_STRIDE = 32;        /* uint32 words per counter: one 128-byte line each */
 constexpr int MAX_SLOTS = 32;
 constexpr int PART_PAD = 4;               /* attention partial: o[d], m, l, 2 pad floats */
 constexpr int ERR_WORDS = 8;
@@ -43,16 +43,17 @@ struct Task {
     uint8_t flags;
     uint16_t layer;
     int32_t r0, r1;          /* GEMV: output rows [r0, r1) within matrix `mat` (QKV) or the op;
-                                ATT: r0 = chunk index c, r1 = number of chunks C */
-    uint16_t b, g;           /* ATT: sequence and kv head */
+                                ATT: r0 = chunk index c, r1 = number of chunks C; MRG: r1 = C */
+    uint16_t b, g;           /* ATT, MRG: sequence and kv head */
     uint16_t rows_per_stage; /* GEMV: rows per ring slot; ATT: positions per tile */
     uint8_t ksplit;          /* GEMV: K split (k-outer loop over ksplit slices) */
     uint8_t nsig;            /* number of valid entries of sig[] */
-    uint16_t wait_id;        /* counter awaited before the task reads its inputs, or NO_WAIT */
+    uint16_t wait_id;        /* dependency the task waits on (the producers of the region it reads), or NO_WAIT */
     uint8_t mat;             /* QKV: MAT_Q/K/V */
-    uint8_t pad0;
-    uint32_t wait_count;     /* producers of wait_id per step (target = epoch * wait_count) */
-    uint16_t sig[MAX_SIG];   /* counters incremented once the task's writes are visible */
+    uint8_t seg;             /* GEMV: K segments per row (consumer warps per row), 1, 2, 4 or 8 */
+    uint32_t wait_count;     /* number of producers of wait_id */
+    uint16_t sig[MAX_SIG];   /* dependencies the task's outputs take part in; the kernel realises a
+                                dependency as epoch-tagged words that its consumers poll */
     uint32_t pad1[2];
 };
 static_assert(sizeof(Task) == 48, "Task layout");
@@ -76,21 +77,27 @@ struct Params {
     const Task *tasks;
     const int32_t *task_start; /* [n_sm + 1] */
     int C, depth, slot_bytes, n_slots, att_tile;
-    int act_bytes, result_bytes, scale_bytes;
+    int act_bytes, result_bytes, scale_bytes, fac_bytes;
     int l2_prefetch_bytes;
     /* weights */
     const LayerPtrs *layers;
     const uint16_t *embed, *final_norm;
     const void *lm;
     const float *s_lm;
-    /* scratch (device, handle-owned) */
-    float *x_in;     /* [depth][Bmax][H]   residual at a layer's input (slot l % depth) */
-    float *x_mid;    /* [depth][Bmax][H]   residual after attention */
-    float *qkv;      /* [depth][Bmax][qkv_rows] */
-    float *part;     /* [depth][Bmax][nkv][C][G][d + PART_PAD] */
-    uint16_t *act;   /* [depth][Bmax][I]   SwiGLU output, bf16 */
-    uint32_t *counters;
-    uint32_t *err;   /* [ERR_WORDS] */
+    /* scratch (device, handle-owned).  Every word is {payload, flag}: the low
+     * 32 bits hold an fp32 value or two bf16 values, the high 32 bits the flag
+     * epoch * (L + 1) + version, where version is the layer whose data the
+     * word holds (x_in: the layer it is the input of).  A consumer polls the
+     * words it needs until they carry the flag of the current step and
+     * version: the data is its own dependency flag, and neither an older step
+     * nor another layer sharing the slot can be mistaken for it. */
+    uint64_t *x_in;   /* [depth][Bmax][H]         residual at a layer's input, fp32 */
+    uint64_t *x_mid;  /* [depth][Bmax][H]         residual after attention, fp32 */
+    uint64_t *qkv;    /* [depth][Bmax][qkv_rows]  fp32 */
+    uint64_t *part;   /* [depth][Bmax][nkv][C][G][d + PART_PAD]  chunk partials, fp32 */
+    uint64_t *aout;   /* [depth][Bmax][nq * d / 2]  attention output, bf16 pairs */
+    uint64_t *act;    /* [depth][Bmax][I / 2]       SwiGLU output, bf16 pairs */
+    uint32_t *err;    /* [ERR_WORDS] */
     const float *rope;  /* [Smax][d/2][2]: cos, sin of position * theta^(-2i/d) */
     /* step */
     const int32_t *tokens, *positions;
@@ -98,8 +105,28 @@ struct Params {
     float *logits;       /* [batch][V] */
     int batch;
     uint32_t epoch;
+    uint32_t epoch_base; /* epoch * (L + 1): flags of this step are epoch_base + version */
     long long timeout_ns;
+    unsigned long long *trace; /* NULL, or [n_tasks][16] timings */
 };
+
+/* Batch-1 GEMV: a consumer warp keeps the activations of its K segment in
+ * registers for a whole task; a segment holds at most this many elements. */
+constexpr int SEGMAX_BF16 = 2048;
+constexpr int SEGMAX_INT8 = 1024;
+
+/* K segments per row for a GEMV task: batch 1 -> enough segments that each
+ * fits in registers; larger batches read activations from shared memory and
+ * use 8 / rows_per_stage segments when a tile has fewer than 8 rows. */
+AMK_HD inline int gemv_segments(int batch_max, int Kc, bool int8, int rows_per_stage) {
+    if (batch_max == 1) {
+        const int segmax = int8 ? SEGMAX_INT8 : SEGMAX_BF16;
+        int S = 1;
+        while (S < NCW && Kc > S * segmax) S *= 2;
+        return S;
+    }
+    return rows_per_stage < NCW ? NCW / rows_per_stage : 1;
+}
 
 /* shared-memory layout (bytes), common to host sizing and device carving */
 constexpr int SMEM_BARRIERS = 2 * MAX_SLOTS * 8;

@@ -10,8 +10,7 @@
  * with compute) and Phase I "Path Solidification" (no runtime scheduling
  * branches: every CTA walks its task table).  The AutoMegaKernel abstract
  * names cross-SM synchronisation as what limits such kernels on
- * high-bandwidth GPUs; this kernel synchronises only through per-dependency
- * counters and never through a grid-wide barrier.
+ * high-bandwidth GPUs; this kernel never uses a grid-wide barrier.
  *
  * GB300 (sm_103a) design:
  *  - grid = one CTA per SM (cooperative launch, so every CTA is resident);
@@ -20,21 +19,22 @@
  *    cp.async.bulk (TMA bulk copies) completing on mbarriers.  Weights and
  *    the cached prefix never depend on this step's activations, so the
  *    loader runs ahead across dependency waits and keeps HBM busy;
- *  - warps 0-7 are CONSUMERS: per task, thread 0 acts as CONTROLLER (waits
- *    on the task's dependency counter with ld.acquire, bounded by a
- *    globaltimer limit), all consumers run the prologue (RMSNorm, attention
- *    partial merge, or activation copy into shared memory), the GEMV or
- *    attention tiles from the ring, and the epilogue (residual, SwiGLU,
- *    partials, logits); thread 0 then acts as STORER (fence + counter
- *    increment) so that consumers of the result may start;
- *  - GEMV: CUDA-core dot products with fp32 accumulation, warp-shuffle
- *    reductions, 16-byte shared-memory reads;
- *  - attention: split-context flash-decoding; each chunk keeps an online
- *    softmax (log2 domain) and writes (m, l, o) partials that the O
- *    projection's prologue merges;
- *  - every wait is bounded: on timeout the CTA records the error, stops, waits
- *    for its own bulk copies in flight and returns; later launches see the
- *    error word and do nothing until the host clears it.
+ *  - warps 0-7 are CONSUMERS.  As CONTROLLER they wait for a task's inputs,
+ *    then run its prologue (RMSNorm, merged attention output, SwiGLU output
+ *    into shared memory), its tiles from the ring, and as STORER its
+ *    epilogue (residual, SwiGLU, attention partials, logits);
+ *  - cross-SM dependencies ride on the data: every activation word is
+ *    {payload, epoch}, written with one 8-byte store, and a consumer polls
+ *    the words it needs until they carry the current step's epoch.  One
+ *    cross-SM round trip per dependency, no fences, no counters;
+ *  - batch-1 GEMV: CUDA cores, each consumer warp keeps the activations of a
+ *    fixed K segment in registers and streams 16-byte weight chunks from the
+ *    ring with short independent FMA chains; fp32 accumulation;
+ *  - attention: split-context flash decoding per (sequence, kv head) chunk
+ *    with an online softmax in log2 units; MRG tasks merge the chunks;
+ *  - every wait is bounded: on timeout the CTA records the error, stops,
+ *    waits for its own bulk copies in flight and returns; later launches see
+ *    the error word and do nothing until the host clears it.
  */
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -85,20 +85,10 @@ __device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
-__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ uint64_t now_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
-}
-
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
 }
 
 __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p) {
@@ -106,6 +96,27 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p) {
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+
+/* epoch-tagged words: one 8-byte store publishes payload and flag together;
+ * a two-word load returns each 8-byte element whole */
+__device__ __forceinline__ void st_ll(uint64_t *p, uint32_t payload, uint32_t epoch) {
+    asm volatile("st.volatile.global.u64 [%0], %1;" ::"l"(p), "l"(((uint64_t)epoch << 32) | payload) : "memory");
+}
+
+__device__ __forceinline__ ulonglong2 ld_ll2(const uint64_t *p) {
+    ulonglong2 v;
+    asm volatile("ld.volatile.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint64_t ld_ll1(const uint64_t *p) {
+    uint64_t v;
+    asm volatile("ld.volatile.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ll_flag(uint64_t w) { return (uint32_t)(w >> 32); }
+__device__ __forceinline__ float ll_f(uint64_t w) { return __uint_as_float((uint32_t)w); }
 
 /* consumer-warps-only barrier; returns the OR of `pred` over all consumers,
  * so that every consumer takes the same abort decision */
@@ -134,6 +145,8 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
 __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
     return (uint32_t)f2bf(lo) | ((uint32_t)f2bf(hi) << 16);
 }
+/* the bf16 value nearest to f, as fp32 */
+__device__ __forceinline__ float round_bf(float f) { return bf2f(f2bf(f)); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -148,6 +161,12 @@ struct Misc {
     int issued;
     float red[MAXB][NCW];
     float rnorm[MAXB];
+    unsigned long long t_first;     /* trace: first tile of the current task arrived */
+    unsigned long long t_wait_full; /* trace: consumer warp 0 waiting for tiles (ns) */
+    unsigned long long t_tiles;     /* trace: consumer warp 0 computing tiles (ns) */
+    unsigned long long t_pro;       /* trace: prologue done */
+    unsigned long long t_stages;    /* trace: last tile consumed */
+    unsigned long long t_epi;       /* trace: epilogue written */
 };
 
 struct Smem {
@@ -155,17 +174,17 @@ struct Smem {
     Misc *misc;
     float *res;
     float *sc;
+    float *fac;
     uint8_t *act;
     uint8_t *ring;
 };
 
 /* first error wins; every CTA then stops at its next check */
-__device__ void raise_error(const Params &p, Smem &s, int code, int task, int counter, uint32_t seen,
-                            uint32_t target) {
+__device__ void raise_error(const Params &p, Smem &s, int code, int task, int what, uint32_t seen, uint32_t target) {
     if (atomicCAS(&p.err[0], 0u, (uint32_t)code) == 0u) {
         p.err[1] = blockIdx.x;
         p.err[2] = (uint32_t)task;
-        p.err[3] = (uint32_t)counter;
+        p.err[3] = (uint32_t)what;
         p.err[4] = seen;
         p.err[5] = target;
         __threadfence();
@@ -173,7 +192,9 @@ __device__ void raise_error(const Params &p, Smem &s, int code, int task, int co
     s.misc->abort = 1;
 }
 
-/* bounded wait on an mbarrier phase; false on abort or timeout */
+/* Bounded wait on an mbarrier phase; false on abort or timeout.  Ring waits
+ * only follow from a dependency wait elsewhere, so they get twice the limit:
+ * the dependency that is really stuck reports first. */
 __device__ bool wait_phase(const Params &p, Smem &s, uint64_t *bar, uint32_t parity, int code, int task) {
     if (mbar_test(bar, parity)) return true;
     uint64_t t0 = now_ns();
@@ -185,7 +206,7 @@ __device__ bool wait_phase(const Params &p, Smem &s, uint64_t *bar, uint32_t par
                 s.misc->abort = 1;
                 return false;
             }
-            if ((long long)(now_ns() - t0) > p.timeout_ns) {
+            if ((long long)(now_ns() - t0) > 2 * p.timeout_ns) {
                 raise_error(p, s, code, task, -1, 0, parity);
                 return false;
             }
@@ -193,24 +214,51 @@ __device__ bool wait_phase(const Params &p, Smem &s, uint64_t *bar, uint32_t par
     }
 }
 
-/* controller: wait until counter `id` reaches epoch * count; false on abort or timeout */
-__device__ bool wait_counter(const Params &p, Smem &s, int id, uint32_t count, int task) {
-    const uint32_t *c = p.counters + (size_t)id * COUNTER_STRIDE;
-    const uint32_t target = p.epoch * count;
-    uint32_t v = ld_acquire(c);
-    if ((int32_t)(v - target) >= 0) return true;
-    uint64_t t0 = now_ns();
-    for (uint32_t n = 1;; ++n) {
-        v = ld_acquire(c);
-        if ((int32_t)(v - target) >= 0) return true;
-        if ((n & 15u) == 0u) {
+/* Which activation buffer a poll waits on (reported in the error word). */
+enum : int { WB_XIN = 0, WB_XMID = 1, WB_QKV = 2, WB_PART = 3, WB_AOUT = 4, WB_ACT = 5 };
+
+/* flag of the current step for data of layer `version` */
+__device__ __forceinline__ uint32_t ver(const Params &p, int version) { return p.epoch_base + (uint32_t)version; }
+
+__device__ __forceinline__ bool ll_ok(uint32_t f, const ulonglong2 &v) { return ll_flag(v.x) == f && ll_flag(v.y) == f; }
+
+/* Re-read two tagged words until both carry flag f (the first read was
+ * issued by the caller).  False on abort or timeout. */
+__device__ __noinline__ bool ll_settle(const Params &p, Smem &s, const uint64_t *src, ulonglong2 &v, uint32_t f,
+                                       int task, int which) {
+    const uint64_t t0 = now_ns();
+    for (uint32_t n = 0;; ++n) {
+        if (ll_ok(f, v)) return true;
+        if (s.misc->abort) return false;
+        if ((n & 63u) == 63u) {
             if (ld_relaxed(p.err) != 0u) {
                 s.misc->abort = 1;
                 return false;
             }
             if ((long long)(now_ns() - t0) > p.timeout_ns) {
-                raise_error(p, s, 1, task, id, v, target);
+                raise_error(p, s, 1, task, which, ll_flag(v.x) != f ? ll_flag(v.x) : ll_flag(v.y), f);
                 return false;
+            }
+        }
+        v = ld_ll2(src);
+    }
+}
+
+/* wait for one word with flag f */
+__device__ __noinline__ float ll_wait1(const Params &p, Smem &s, const uint64_t *src, uint32_t f, int task, int which) {
+    const uint64_t t0 = now_ns();
+    for (uint32_t n = 0;; ++n) {
+        const uint64_t w = ld_ll1(src);
+        if (ll_flag(w) == f) return ll_f(w);
+        if (s.misc->abort) return 0.f;
+        if ((n & 63u) == 63u) {
+            if (ld_relaxed(p.err) != 0u) {
+                s.misc->abort = 1;
+                return 0.f;
+            }
+            if ((long long)(now_ns() - t0) > p.timeout_ns) {
+                raise_error(p, s, 1, task, which, ll_flag(w), f);
+                return 0.f;
             }
         }
     }
@@ -272,12 +320,6 @@ __device__ __forceinline__ AttGeo att_geo(const Params &p, const Task &t) {
     return a;
 }
 
-__device__ __forceinline__ int num_stages(const Params &p, const Task &t) {
-    if (t.op == OP_ATT) return att_geo(p, t).ntile;
-    GemvGeo g = gemv_geo(p, t);
-    return g.ks * g.nrb * g.nmat;
-}
-
 __device__ __forceinline__ void load_task(const Task *src, Task &t) {
     const uint4 *s = reinterpret_cast<const uint4 *>(src);
     uint4 *d = reinterpret_cast<uint4 *>(&t);
@@ -286,90 +328,142 @@ __device__ __forceinline__ void load_task(const Task *src, Task &t) {
     d[2] = __ldg(s + 2);
 }
 
+/* Position in the ring: slot and pass (how many times the ring wrapped).  The
+ * k-th fill of a slot completes phase k of its full barrier; the k-th release
+ * completes phase k of its empty barrier. */
+struct Ring {
+    int slot;
+    uint32_t pass;
+    uint32_t count; /* stages so far */
+    __device__ __forceinline__ void advance(int NS) {
+        ++count;
+        if (++slot == NS) {
+            slot = 0;
+            ++pass;
+        }
+    }
+};
+
 /* ----------------------------------------------------------- loader */
+
+/* claim the next slot (bounded wait for its release) and arm its full barrier */
+__device__ __forceinline__ uint8_t *loader_claim(const Params &p, Smem &s, Ring &r, uint32_t bytes, int ti) {
+    const unsigned long long t0 = p.trace ? now_ns() : 0;
+    if (r.pass > 0 && !wait_phase(p, s, &s.empty[r.slot], (r.pass - 1u) & 1u, 3, ti)) return nullptr;
+    if (p.trace) p.trace[16 * (size_t)ti + 9] += now_ns() - t0;
+    if (s.misc->abort) return nullptr;
+    mbar_arrive_expect_tx(&s.full[r.slot], bytes);
+    return s.ring + (size_t)r.slot * p.slot_bytes;
+}
 
 __device__ void loader(const Params &p, Smem &s, int tbeg, int tend) {
     const int NS = p.n_slots;
-    uint32_t it = 0;
+    Ring r{0, 0, 0};
     for (int ti = tbeg; ti < tend; ++ti) {
         Task t;
         load_task(p.tasks + ti, t);
-        const int ns = num_stages(p, t);
-        GemvGeo g;
-        AttGeo a;
-        const uint8_t *kbase = nullptr, *vbase = nullptr;
+        if (p.trace) p.trace[16 * (size_t)ti + 9] = 0;
+        if (t.op == OP_MRG) continue;
         if (t.op == OP_ATT) {
-            a = att_geo(p, t);
-            size_t row = (((size_t)t.layer * p.Bmax + t.b) * p.nkv + t.g) * (size_t)p.Smax;
-            kbase = (const uint8_t *)(p.kc + row * p.d);
-            vbase = (const uint8_t *)(p.vc + row * p.d);
-        } else {
-            g = gemv_geo(p, t);
-        }
-        for (int st = 0; st < ns; ++st, ++it) {
-            const int slot = (int)(it % (uint32_t)NS);
-            if (it >= (uint32_t)NS && !wait_phase(p, s, &s.empty[slot], ((it / NS) - 1u) & 1u, 3, ti)) {
-                s.misc->issued = (int)it;
-                return;
-            }
-            if (s.misc->abort) {
-                s.misc->issued = (int)it;
-                return;
-            }
-            uint8_t *dst = s.ring + (size_t)slot * p.slot_bytes;
-            uint64_t *bar = &s.full[slot];
-            if (t.op == OP_ATT) {
-                const int t0 = a.s0 + st * t.rows_per_stage;
+            const AttGeo a = att_geo(p, t);
+            const size_t row = (((size_t)t.layer * p.Bmax + t.b) * p.nkv + t.g) * (size_t)p.Smax;
+            const uint8_t *kb = (const uint8_t *)(p.kc + row * p.d), *vb = (const uint8_t *)(p.vc + row * p.d);
+            const size_t tb = (size_t)t.rows_per_stage * p.d * 2;
+            for (int t0 = a.s0; t0 < a.e; t0 += t.rows_per_stage) {
                 const int t1 = min(a.e, t0 + (int)t.rows_per_stage);
                 const uint32_t bytes = (uint32_t)(t1 - t0) * p.d * 2;
-                mbar_arrive_expect_tx(bar, 2 * bytes);
-                bulk_copy(dst, kbase + (size_t)t0 * p.d * 2, bytes, bar);
-                bulk_copy(dst + (size_t)t.rows_per_stage * p.d * 2, vbase + (size_t)t0 * p.d * 2, bytes, bar);
-            } else {
-                const int kp = st / (g.nrb * g.nmat), rem = st % (g.nrb * g.nmat);
-                const int rb = rem / g.nmat, m = rem % g.nmat;
-                const int ra = t.r0 + rb * g.R, re = min(t.r1, ra + g.R);
-                const int web = (t.op == OP_LMH ? p.lm_int8 : p.wint8) ? 1 : 2;
-                const uint8_t *W = op_weights(p, t, m);
-                const size_t rowb = (size_t)g.K * web, segb = (size_t)g.Kc * web;
+                uint8_t *dst = loader_claim(p, s, r, 2 * bytes, ti);
+                if (!dst) {
+                    s.misc->issued = (int)r.count;
+                    return;
+                }
+                bulk_copy(dst, kb + (size_t)t0 * p.d * 2, bytes, &s.full[r.slot]);
+                bulk_copy(dst + tb, vb + (size_t)t0 * p.d * 2, bytes, &s.full[r.slot]);
+                r.advance(NS);
+            }
+            continue;
+        }
+        const GemvGeo g = gemv_geo(p, t);
+        const int web = (t.op == OP_LMH ? p.lm_int8 : p.wint8) ? 1 : 2;
+        const uint8_t *W[2] = {op_weights(p, t, 0), op_weights(p, t, g.nmat - 1)};
+        const size_t rowb = (size_t)g.K * web, segb = (size_t)g.Kc * web;
+        for (int kp = 0; kp < g.ks; ++kp) {
+            for (int ra = t.r0; ra < t.r1; ra += g.R) {
+                const int re = min(t.r1, ra + g.R);
                 const uint32_t bytes = (uint32_t)((re - ra) * segb);
-                mbar_arrive_expect_tx(bar, bytes);
-                if (g.ks == 1) {
-                    bulk_copy(dst, W + (size_t)ra * rowb, bytes, bar);
-                } else {
-                    for (int r = ra; r < re; ++r)
-                        bulk_copy(dst + (size_t)(r - ra) * segb, W + (size_t)r * rowb + (size_t)kp * segb, (uint32_t)segb, bar);
+                for (int m = 0; m < g.nmat; ++m) {
+                    uint8_t *dst = loader_claim(p, s, r, bytes, ti);
+                    if (!dst) {
+                        s.misc->issued = (int)r.count;
+                        return;
+                    }
+                    if (g.ks == 1) {
+                        bulk_copy(dst, W[m] + (size_t)ra * rowb, bytes, &s.full[r.slot]);
+                    } else {
+                        const uint8_t *src = W[m] + (size_t)ra * rowb + (size_t)kp * segb;
+                        for (int q = 0; q < re - ra; ++q)
+                            bulk_copy(dst + (size_t)q * segb, src + (size_t)q * rowb, (uint32_t)segb, &s.full[r.slot]);
+                    }
+                    r.advance(NS);
                 }
             }
         }
     }
-    s.misc->issued = (int)it;
+    s.misc->issued = (int)r.count;
 }
 
 /* ----------------------------------------------------------- prologues */
 
-/* x (fp32 residual) that a norm or residual reads: layer-0 input is the
- * token's embedding row */
-__device__ __forceinline__ float4 load_x4(const Params &p, const float *xs, const uint16_t *emb, int i4) {
+constexpr int MAXG = 4; /* float4 of x (and of the gain) per consumer thread kept in registers: H <= 4096 */
+
+/* batch 1 with the whole row in one K slice: x and the gain stay in registers */
+template <int NB>
+__device__ __forceinline__ bool norm_keeps_x(const Params &p, int k0, int k1) {
+    return NB == 1 && p.H / 4 <= MAXG * NCW * 32 && k0 == 0 && k1 == p.H;
+}
+
+/* four consecutive x values: the token's embedding row (layer 0) or epoch-
+ * tagged residual words (waited for) */
+__device__ __forceinline__ float4 load_x4(const Params &p, Smem &s, const uint64_t *xs, const uint16_t *emb, int i4,
+                                          uint32_t f, int task, int which) {
     if (emb) {
         uint2 w = __ldg(reinterpret_cast<const uint2 *>(emb) + i4);
         return make_float4(bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
     }
-    return __ldcg(reinterpret_cast<const float4 *>(xs) + i4);
+    const uint64_t *src = xs + 4 * (size_t)i4;
+    ulonglong2 a = ld_ll2(src), b = ld_ll2(src + 2);
+    if (!ll_ok(f, a)) ll_settle(p, s, src, a, f, task, which);
+    if (!ll_ok(f, b)) ll_settle(p, s, src + 2, b, f, task, which);
+    return make_float4(ll_f(a.x), ll_f(a.y), ll_f(b.x), ll_f(b.y));
 }
 
-/* RMSNorm prologue: act[b][k - k0] = bf16(x[b][k] * r_b * gain[k]) for k in [k0, k1) */
-__device__ void norm_prologue(const Params &p, Smem &s, const float *xbase, bool from_embed, const uint16_t *gain,
-                              int k0, int k1, bool need_r, int ctid, int warp, int lane) {
+/* RMSNorm prologue: act[b][k - k0] = bf16(x[b][k] * r_b * gain[k]) for k in
+ * [k0, k1), stored as fp32 (the bf16 value exactly).  r_b is computed once per
+ * task (need_r) from the whole of x[b].  Reading x waits for its producers. */
+template <int NB>
+__device__ void norm_prologue(const Params &p, Smem &s, const uint64_t *xbase, bool from_embed, const uint16_t *gain,
+                              int k0, int k1, bool need_r, const uint2 *gpre, uint32_t f, int task, int which, int ctid,
+                              int warp, int lane) {
     const int H = p.H, H4 = H / 4;
+    const bool keep = norm_keeps_x<NB>(p, k0, k1);
+    float4 xr[MAXG];
     if (need_r) {
         for (int b = 0; b < p.batch; ++b) {
-            const float *xs = from_embed ? nullptr : xbase + (size_t)b * H;
+            const uint64_t *xs = from_embed ? nullptr : xbase + (size_t)b * H;
             const uint16_t *emb = from_embed ? p.embed + (size_t)__ldg(p.tokens + b) * H : nullptr;
             float ss = 0.f;
-            for (int i4 = ctid; i4 < H4; i4 += NCW * 32) {
-                float4 v = load_x4(p, xs, emb, i4);
-                ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+            if (keep) {
+#pragma unroll
+                for (int g = 0; g < MAXG; ++g) {
+                    const int i4 = ctid + g * NCW * 32;
+                    xr[g] = i4 < H4 ? load_x4(p, s, xs, emb, i4, f, task, which) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    ss += xr[g].x * xr[g].x + xr[g].y * xr[g].y + xr[g].z * xr[g].z + xr[g].w * xr[g].w;
+                }
+            } else {
+                for (int i4 = ctid; i4 < H4; i4 += NCW * 32) {
+                    float4 v = load_x4(p, s, xs, emb, i4, f, task, which);
+                    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+                }
             }
             ss = warp_sum(ss);
             if (lane == 0) s.misc->red[b][warp] = ss;
@@ -381,186 +475,259 @@ __device__ void norm_prologue(const Params &p, Smem &s, const float *xbase, bool
             for (int w = 0; w < NCW; ++w) ss += s.misc->red[ctid][w];
             s.misc->rnorm[ctid] = rsqrtf(ss / (float)H + p.eps);
         }
+        if (keep) {
+            /* every thread derives r itself: no second barrier */
+            float ss = 0.f;
+#pragma unroll
+            for (int w = 0; w < NCW; ++w) ss += s.misc->red[0][w];
+            const float r = rsqrtf(ss / (float)H + p.eps);
+            float4 *dst = reinterpret_cast<float4 *>(s.act);
+#pragma unroll
+            for (int g = 0; g < MAXG; ++g) {
+                const int i4 = ctid + g * NCW * 32;
+                if (i4 < H4) {
+                    const uint2 gw = gpre[g];
+                    dst[i4] = make_float4(round_bf(xr[g].x * r * bf_lo(gw.x)), round_bf(xr[g].y * r * bf_hi(gw.x)),
+                                          round_bf(xr[g].z * r * bf_lo(gw.y)), round_bf(xr[g].w * r * bf_hi(gw.y)));
+                }
+            }
+            return;
+        }
         cbar();
     }
     const int kc = k1 - k0;
     for (int b = 0; b < p.batch; ++b) {
-        const float *xs = from_embed ? nullptr : xbase + (size_t)b * H;
+        const uint64_t *xs = from_embed ? nullptr : xbase + (size_t)b * H;
         const uint16_t *emb = from_embed ? p.embed + (size_t)__ldg(p.tokens + b) * H : nullptr;
         const float r = s.misc->rnorm[b];
-        uint2 *dst = reinterpret_cast<uint2 *>(s.act + (size_t)b * kc * 2);
+        float4 *dst = reinterpret_cast<float4 *>(s.act + (size_t)b * kc * 4);
         for (int i4 = k0 / 4 + ctid; i4 < k1 / 4; i4 += NCW * 32) {
-            float4 v = load_x4(p, xs, emb, i4);
+            float4 v = load_x4(p, s, xs, emb, i4, f, task, which);
             uint2 gw = __ldg(reinterpret_cast<const uint2 *>(gain) + i4);
-            uint2 o;
-            o.x = pack_bf2(v.x * r * bf_lo(gw.x), v.y * r * bf_hi(gw.x));
-            o.y = pack_bf2(v.z * r * bf_lo(gw.y), v.w * r * bf_hi(gw.y));
-            dst[i4 - k0 / 4] = o;
+            dst[i4 - k0 / 4] = make_float4(round_bf(v.x * r * bf_lo(gw.x)), round_bf(v.y * r * bf_hi(gw.x)),
+                                           round_bf(v.z * r * bf_lo(gw.y)), round_bf(v.w * r * bf_hi(gw.y)));
         }
     }
 }
 
-/* O-projection prologue: merge the attention partials of every chunk into
- * bf16(o) for k in [k0, k1) of the concatenated heads */
-__device__ void merge_prologue(const Params &p, Smem &s, int layer, int k0, int k1, int ctid) {
-    const int d = p.d, dq = d / 4, C = p.C, G = p.G, slot = layer % p.depth;
+/* O-projection and down-projection prologues: bf16 activations [k0, k1) of
+ * rows of `len` elements (attention output, SwiGLU output), held two per
+ * epoch-tagged word, as fp32; waits for their producers */
+__device__ void copy_prologue(const Params &p, Smem &s, const uint64_t *src0, int len, int k0, int k1, uint32_t f,
+                              int task, int which, int ctid) {
     const int kc = k1 - k0;
-    const int items = p.batch * (kc / 4);
-    for (int it = ctid; it < items; it += NCW * 32) {
-        const int b = it / (kc / 4);
-        const int k = k0 + (it % (kc / 4)) * 4;
-        const int j = k / d, e4 = (k % d) / 4, grp = j / G, h = j % G;
-        const float *base = p.part + ((((size_t)slot * p.Bmax + b) * p.nkv + grp) * C * G + h) * (d + PART_PAD);
-        const size_t cstride = (size_t)G * (d + PART_PAD);
-        float M = -INFINITY;
-        for (int c = 0; c < C; ++c) M = fmaxf(M, __ldcg(base + c * cstride + d));
-        float den = 0.f;
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = 0; c < C; ++c) {
-            const float *pc = base + c * cstride;
-            const float mc = __ldcg(pc + d);
-            if (mc == -INFINITY) continue;
-            const float f = exp2f(mc - M);
-            den += f * __ldcg(pc + d + 1);
-            float4 oc = __ldcg(reinterpret_cast<const float4 *>(pc) + e4);
-            o.x += f * oc.x;
-            o.y += f * oc.y;
-            o.z += f * oc.z;
-            o.w += f * oc.w;
-        }
-        const float inv = 1.f / den;
-        uint2 w;
-        w.x = pack_bf2(o.x * inv, o.y * inv);
-        w.y = pack_bf2(o.z * inv, o.w * inv);
-        reinterpret_cast<uint2 *>(s.act + (size_t)b * kc * 2)[(k - k0) / 4] = w;
-        (void)dq;
-    }
-}
-
-/* down-projection prologue: copy bf16 SwiGLU activations [k0, k1) */
-__device__ void copy_prologue(const Params &p, Smem &s, int layer, int k0, int k1, int ctid) {
-    const int slot = layer % p.depth, kc = k1 - k0;
     for (int b = 0; b < p.batch; ++b) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.act + ((size_t)slot * p.Bmax + b) * p.I + k0);
-        uint4 *dst = reinterpret_cast<uint4 *>(s.act + (size_t)b * kc * 2);
-        for (int i = ctid; i < kc / 8; i += NCW * 32) dst[i] = __ldcg(src + i);
+        const uint64_t *src = src0 + ((size_t)b * len + k0) / 2;
+        float4 *dst = reinterpret_cast<float4 *>(s.act + (size_t)b * kc * 4);
+        for (int i = ctid; i < kc / 4; i += NCW * 32) {
+            ulonglong2 v = ld_ll2(src + 2 * i);
+            if (!ll_ok(f, v)) ll_settle(p, s, src + 2 * i, v, f, task, which);
+            const uint32_t a = (uint32_t)v.x, c = (uint32_t)v.y;
+            dst[i] = make_float4(bf_lo(a), bf_hi(a), bf_lo(c), bf_hi(c));
+        }
     }
 }
 
-/* ----------------------------------------------------------- GEMV tile */
+/* ----------------------------------------------------------- GEMV tiles */
 
+/* int8 -> fp32, exact: byte b of x becomes (2^23 + 128 + b) by placing b ^ 0x80
+ * under the exponent bits of 2^23, then 2^23 + 128 is subtracted. */
+__device__ __forceinline__ float i8_to_f(uint32_t xflip, int k) {
+    return __uint_as_float(__byte_perm(xflip, 0x4B000000u, 0x7540u | (unsigned)k)) - 8388736.0f;
+}
+
+/* Dot product of one 16-byte weight chunk (8 bf16 or 16 int8) with EPC fp32
+ * activations at h. */
 template <bool I8>
-__device__ __forceinline__ void unpack16(const uint4 &w, float *f) {
+__device__ __forceinline__ float dot_chunk(const uint4 &w, const float *h) {
+    const float4 *h4 = reinterpret_cast<const float4 *>(h);
+    float s0 = 0.f, s1 = 0.f;
     if constexpr (I8) {
-        const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+        const uint32_t x[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) f[4 * q + k] = (float)(int8_t)(x[q] >> (8 * k));
+            const float4 a = h4[q];
+            s0 = fmaf(i8_to_f(x[q], 0), a.x, s0);
+            s1 = fmaf(i8_to_f(x[q], 1), a.y, s1);
+            s0 = fmaf(i8_to_f(x[q], 2), a.z, s0);
+            s1 = fmaf(i8_to_f(x[q], 3), a.w, s1);
         }
     } else {
-        f[0] = bf_lo(w.x);
-        f[1] = bf_hi(w.x);
-        f[2] = bf_lo(w.y);
-        f[3] = bf_hi(w.y);
-        f[4] = bf_lo(w.z);
-        f[5] = bf_hi(w.z);
-        f[6] = bf_lo(w.w);
-        f[7] = bf_hi(w.w);
+        const float4 a = h4[0], c = h4[1];
+        s0 = fmaf(bf_lo(w.x), a.x, s0);
+        s1 = fmaf(bf_hi(w.x), a.y, s1);
+        s0 = fmaf(bf_lo(w.y), a.z, s0);
+        s1 = fmaf(bf_hi(w.y), a.w, s1);
+        s0 = fmaf(bf_lo(w.z), c.x, s0);
+        s1 = fmaf(bf_hi(w.z), c.y, s1);
+        s0 = fmaf(bf_lo(w.w), c.z, s0);
+        s1 = fmaf(bf_hi(w.w), c.w, s1);
+    }
+    return s0 + s1;
+}
+
+/* Batch-1 tile with the activations in registers: warp w owns K segment
+ * w % S (chunks [c0, c1)) and rows w / S, w / S + 8 / S, ...; hv holds this
+ * lane's chunks c0 + lane + 32 j of the activation slice.  All of a row's
+ * 16-byte shared loads are issued first, then the products go into eight
+ * independent accumulators (short dependency chains). */
+template <bool I8>
+__device__ __forceinline__ void gemv_tile_b1(const uint8_t *tile, int nrows, int S, int Kc, const float4 (*hv)[I8 ? 4 : 2],
+                                             int c0, int c1, float *res, bool first, int warp, int lane) {
+    constexpr int EPC = I8 ? 16 : 8;
+    constexpr int MAXJ = (I8 ? SEGMAX_INT8 : SEGMAX_BF16) / (32 * EPC);
+    const int RG = NCW / S, seg = warp % S;
+    const size_t rowb = (size_t)Kc * (I8 ? 1 : 2);
+    for (int rr = warp / S; rr < nrows; rr += RG) {
+        const uint4 *w = reinterpret_cast<const uint4 *>(tile + rr * rowb);
+        uint4 wv[MAXJ];
+#pragma unroll
+        for (int j = 0; j < MAXJ; ++j) {
+            const int c = c0 + lane + 32 * j;
+            wv[j] = c < c1 ? w[c] : make_uint4(0u, 0u, 0u, 0u);
+        }
+        float a[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a[e] = 0.f;
+#pragma unroll
+        for (int j = 0; j < MAXJ; ++j) {
+            if constexpr (I8) {
+                const uint32_t x[4] = {wv[j].x ^ 0x80808080u, wv[j].y ^ 0x80808080u, wv[j].z ^ 0x80808080u,
+                                       wv[j].w ^ 0x80808080u};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 h = hv[j][q];
+                    a[2 * q] = fmaf(i8_to_f(x[q], 0), h.x, a[2 * q]);
+                    a[2 * q + 1] = fmaf(i8_to_f(x[q], 1), h.y, a[2 * q + 1]);
+                    a[2 * q] = fmaf(i8_to_f(x[q], 2), h.z, a[2 * q]);
+                    a[2 * q + 1] = fmaf(i8_to_f(x[q], 3), h.w, a[2 * q + 1]);
+                }
+            } else {
+                const float4 x = hv[j][0], y = hv[j][1];
+                a[0] = fmaf(bf_lo(wv[j].x), x.x, a[0]);
+                a[1] = fmaf(bf_hi(wv[j].x), x.y, a[1]);
+                a[2] = fmaf(bf_lo(wv[j].y), x.z, a[2]);
+                a[3] = fmaf(bf_hi(wv[j].y), x.w, a[3]);
+                a[4] = fmaf(bf_lo(wv[j].z), y.x, a[4]);
+                a[5] = fmaf(bf_hi(wv[j].z), y.y, a[5]);
+                a[6] = fmaf(bf_lo(wv[j].w), y.z, a[6]);
+                a[7] = fmaf(bf_hi(wv[j].w), y.w, a[7]);
+            }
+        }
+        const float v = warp_sum(((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7])));
+        if (lane == 0) {
+            float *r = res + (size_t)rr * S + seg;
+            *r = first ? v : *r + v;
+        }
     }
 }
 
-/* rows [0, nrows) of a tile of width Kc in shared memory, times the bf16
- * activation slice act[b][0..Kc); warp-per-row, two rows per pass sharing the
- * activation loads; results (or partial sums for K split) into res[rr][b] */
+/* Batched tile: activations act[b][0..Kc) in shared memory.  With S > 1
+ * segments per row warp w takes row w / S, K segment w % S; with S == 1 warp
+ * w takes rows w, w + 8, ...  Partial sums go to res[(row * S + seg) * Bmax + b]
+ * (accumulating over K-split passes); the epilogue adds the S segments in a
+ * fixed order, so results do not depend on timing. */
 template <bool I8, int NB>
-__device__ void gemv_tile(const uint8_t *tile, int nrows, int Kc, const uint8_t *act, int batch, float *res, int Bmax,
-                          bool first, int warp, int lane) {
+__device__ void gemv_tile(const uint8_t *tile, int nrows, int S, int Kc, const float *act, int batch, float *res,
+                          int Bmax, bool first, int warp, int lane) {
     constexpr int EPC = I8 ? 16 : 8;
     const int nch = Kc / EPC;
     const size_t rowb = (size_t)Kc * (I8 ? 1 : 2);
-    for (int rr = warp; rr < nrows; rr += 2 * NCW) {
-        const int rr2 = rr + NCW;
-        const bool two = rr2 < nrows;
-        float a0[NB], a1[NB];
+    const int RG = NCW / S, seg = warp % S;
+    const int c0 = seg * nch / S, c1 = (seg + 1) * nch / S;
+    for (int rr = warp / S; rr < nrows; rr += RG) {
+        float a[NB];
 #pragma unroll
-        for (int b = 0; b < NB; ++b) a0[b] = a1[b] = 0.f;
-        const uint4 *w0 = reinterpret_cast<const uint4 *>(tile + rr * rowb);
-        const uint4 *w1 = reinterpret_cast<const uint4 *>(tile + (two ? rr2 : rr) * rowb);
-        for (int c = lane; c < nch; c += 32) {
-            float f0[EPC], f1[EPC];
-            unpack16<I8>(w0[c], f0);
-            if (two) unpack16<I8>(w1[c], f1);
+        for (int b = 0; b < NB; ++b) a[b] = 0.f;
+        const uint4 *w = reinterpret_cast<const uint4 *>(tile + rr * rowb);
+        for (int c = c0 + lane; c < c1; c += 32) {
+            const uint4 wv = w[c];
 #pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                if (b < batch) {
-                    const uint4 *hp = reinterpret_cast<const uint4 *>(act + ((size_t)b * Kc + (size_t)c * EPC) * 2);
-                    float h[EPC];
-                    unpack16<false>(hp[0], h);
-                    if constexpr (I8) unpack16<false>(hp[1], h + 8);
-                    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-                    for (int e = 0; e < EPC; ++e) s0 = fmaf(f0[e], h[e], s0);
-                    a0[b] += s0;
-                    if (two) {
-#pragma unroll
-                        for (int e = 0; e < EPC; ++e) s1 = fmaf(f1[e], h[e], s1);
-                        a1[b] += s1;
-                    }
-                }
-            }
+            for (int b = 0; b < NB; ++b)
+                if (b < batch) a[b] += dot_chunk<I8>(wv, act + (size_t)b * Kc + (size_t)c * EPC);
         }
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             if (b < batch) {
-                float v0 = warp_sum(a0[b]);
-                float v1 = two ? warp_sum(a1[b]) : 0.f;
+                const float v = warp_sum(a[b]);
                 if (lane == 0) {
-                    float *r0 = res + (size_t)rr * Bmax + b;
-                    *r0 = first ? v0 : *r0 + v0;
-                    if (two) {
-                        float *r1 = res + (size_t)rr2 * Bmax + b;
-                        *r1 = first ? v1 : *r1 + v1;
-                    }
+                    float *r = res + ((size_t)rr * S + seg) * Bmax + b;
+                    *r = first ? v : *r + v;
                 }
             }
         }
     }
 }
 
+/* residual value x[b][row] of a layer's input: the embedding row at layer 0 */
+__device__ __forceinline__ float x_in_value(const Params &p, Smem &s, int l, int b, int row, int task) {
+    if (l == 0) return bf2f(__ldg(p.embed + (size_t)__ldg(p.tokens + b) * p.H + row));
+    return ll_wait1(p, s, p.x_in + ((size_t)(l % p.depth) * p.Bmax + b) * p.H + row, ver(p, l), task, WB_XIN);
+}
+
 template <bool I8, int NB>
-__device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, uint32_t &it, int ctid, int warp, int lane) {
+__device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring &rg, const uint2 *gpre, int ctid,
+                          int warp, int lane) {
     const GemvGeo g = gemv_geo(p, t);
     const int NS = p.n_slots;
     const int l = t.layer, slot = l % p.depth;
-    constexpr bool i8 = I8; /* the LM head has the layers' weight type (tied heads are bf16) */
+    const int S = t.seg;
     for (int kp = 0; kp < g.ks; ++kp) {
         const int k0 = kp * g.Kc, k1 = k0 + g.Kc;
         if (t.op == OP_QKV) {
             const bool emb = l == 0;
-            norm_prologue(p, s, emb ? nullptr : p.x_in + (size_t)slot * p.Bmax * p.H, emb, p.layers[l].attn_norm, k0, k1,
-                          kp == 0, ctid, warp, lane);
+            norm_prologue<NB>(p, s, emb ? nullptr : p.x_in + (size_t)slot * p.Bmax * p.H, emb, p.layers[l].attn_norm, k0,
+                              k1, kp == 0, gpre, ver(p, l), ti, WB_XIN, ctid, warp, lane);
         } else if (t.op == OP_GUP) {
-            norm_prologue(p, s, p.x_mid + (size_t)slot * p.Bmax * p.H, false, p.layers[l].mlp_norm, k0, k1, kp == 0, ctid,
-                          warp, lane);
+            norm_prologue<NB>(p, s, p.x_mid + (size_t)slot * p.Bmax * p.H, false, p.layers[l].mlp_norm, k0, k1, kp == 0,
+                              gpre, ver(p, l), ti, WB_XMID, ctid, warp, lane);
         } else if (t.op == OP_LMH) {
-            norm_prologue(p, s, p.x_in + (size_t)(p.L % p.depth) * p.Bmax * p.H, false, p.final_norm, k0, k1, kp == 0,
-                          ctid, warp, lane);
+            norm_prologue<NB>(p, s, p.x_in + (size_t)(p.L % p.depth) * p.Bmax * p.H, false, p.final_norm, k0, k1,
+                              kp == 0, gpre, ver(p, p.L), ti, WB_XIN, ctid, warp, lane);
         } else if (t.op == OP_OPR) {
-            merge_prologue(p, s, l, k0, k1, ctid);
+            copy_prologue(p, s, p.aout + (size_t)slot * p.Bmax * p.nq * p.d / 2, p.nq * p.d, k0, k1, ver(p, l), ti,
+                          WB_AOUT, ctid);
         } else {
-            copy_prologue(p, s, l, k0, k1, ctid);
+            copy_prologue(p, s, p.act + (size_t)slot * p.Bmax * p.I / 2, p.I, k0, k1, ver(p, l), ti, WB_ACT, ctid);
         }
         if (cbar_or(s.misc->abort != 0)) return false;
+        if (p.trace && kp == 0 && ctid == 0) s.misc->t_pro = now_ns();
+        /* batch 1: this warp's K segment of the activations into registers */
+        constexpr int EPC = I8 ? 16 : 8;
+        constexpr int MAXJ = (I8 ? SEGMAX_INT8 : SEGMAX_BF16) / (32 * EPC);
+        float4 hv[NB == 1 ? MAXJ : 1][I8 ? 4 : 2];
+        const int nch = g.Kc / EPC, seg = warp % S;
+        const int c0 = seg * nch / S, c1 = (seg + 1) * nch / S;
+        if constexpr (NB == 1) {
+            const float4 *a4 = reinterpret_cast<const float4 *>(s.act);
+#pragma unroll
+            for (int j = 0; j < MAXJ; ++j) {
+                const int c = c0 + lane + 32 * j;
+#pragma unroll
+                for (int q = 0; q < EPC / 4; ++q)
+                    hv[j][q] = c < c1 ? a4[(size_t)c * (EPC / 4) + q] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
         for (int rb = 0; rb < g.nrb; ++rb) {
             const int ra = t.r0 + rb * g.R, re = min(t.r1, ra + g.R);
-            for (int m = 0; m < g.nmat; ++m, ++it) {
-                const int sl = (int)(it % (uint32_t)NS);
+            for (int m = 0; m < g.nmat; ++m, rg.advance(NS)) {
+                const int sl = rg.slot;
                 if (s.misc->abort) continue;
-                if (!wait_phase(p, s, &s.full[sl], (it / NS) & 1u, 2, ti)) continue;
-                float *res = s.res + ((size_t)m * g.nrows + (ra - t.r0)) * p.Bmax;
+                const unsigned long long tw0 = p.trace ? now_ns() : 0;
+                if (!wait_phase(p, s, &s.full[sl], rg.pass & 1u, 2, ti)) continue;
+                const unsigned long long tw1 = p.trace ? now_ns() : 0;
+                if (p.trace && kp == 0 && rb == 0 && m == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
+                float *res = s.res + ((size_t)m * g.nrows + (ra - t.r0)) * S * p.Bmax;
                 const uint8_t *tile = s.ring + (size_t)sl * p.slot_bytes;
-                gemv_tile<I8, NB>(tile, re - ra, g.Kc, s.act, p.batch, res, p.Bmax, kp == 0, warp, lane);
+                if constexpr (NB == 1)
+                    gemv_tile_b1<I8>(tile, re - ra, S, g.Kc, hv, c0, c1, res, kp == 0, warp, lane);
+                else
+                    gemv_tile<I8, NB>(tile, re - ra, S, g.Kc, reinterpret_cast<const float *>(s.act), p.batch, res,
+                                      p.Bmax, kp == 0, warp, lane);
+                if (p.trace && warp == 0 && lane == 0) {
+                    s.misc->t_wait_full += tw1 - tw0;
+                    s.misc->t_tiles += now_ns() - tw1;
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s.empty[sl]);
             }
@@ -568,41 +735,59 @@ __device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, uint3
         if (cbar_or(s.misc->abort != 0)) return false;
     }
 
-    /* epilogue */
+    /* epilogue: publish the task's rows as epoch-tagged words; a task marked
+     * TF_SKIP_SIGNAL publishes them with a stale epoch (timeout tests) */
+    if (p.trace && ctid == 0) s.misc->t_stages = now_ns();
+    const uint32_t stale = (t.flags & TF_SKIP_SIGNAL) ? (uint32_t)(p.L + 1) : 0u;
+    const uint32_t ep = ver(p, l) - stale, ep_next = ver(p, l + 1) - stale;
     const int n = g.nrows, B = p.batch;
-    for (int i = ctid; i < n * B; i += NCW * 32) {
-        const int rr = i / B, b = i % B, row = t.r0 + rr;
-        float y0 = s.res[(size_t)rr * p.Bmax + b];
-        if (i8) y0 *= s.sc[rr];
-        switch (t.op) {
-        case OP_QKV: {
-            const int base = t.mat == MAT_Q ? 0 : t.mat == MAT_K ? p.nq * p.d : (p.nq + p.nkv) * p.d;
-            p.qkv[((size_t)slot * p.Bmax + b) * p.qkv_rows + base + row] = y0;
-            break;
+    auto y_of = [&](int m, int rr, int b) {
+        float y = 0.f;
+        for (int sg = 0; sg < S; ++sg) y += s.res[(((size_t)m * n + rr) * S + sg) * p.Bmax + b];
+        return I8 ? y * s.sc[m * n + rr] : y;
+    };
+    if (t.op == OP_GUP) {
+        /* two SwiGLU outputs per word: task rows start at an even row and come in pairs */
+        for (int i = ctid; i < (n / 2) * B; i += NCW * 32) {
+            const int pr = i / B, b = i % B, rr = 2 * pr;
+            float a2[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const float gte = y_of(0, rr + q, b), up = y_of(1, rr + q, b);
+                a2[q] = gte / (1.f + __expf(-gte)) * up;
+            }
+            st_ll(p.act + (((size_t)slot * p.Bmax + b) * p.I + t.r0 + rr) / 2, pack_bf2(a2[0], a2[1]), ep);
         }
-        case OP_OPR: {
-            const float xr = l == 0 ? bf2f(__ldg(p.embed + (size_t)__ldg(p.tokens + b) * p.H + row))
-                                    : __ldcg(p.x_in + ((size_t)slot * p.Bmax + b) * p.H + row);
-            p.x_mid[((size_t)slot * p.Bmax + b) * p.H + row] = xr + y0;
-            break;
-        }
-        case OP_GUP: {
-            float y1 = s.res[((size_t)n + rr) * p.Bmax + b];
-            if (i8) y1 *= s.sc[n + rr];
-            const float a = y0 / (1.f + __expf(-y0)) * y1;
-            p.act[((size_t)slot * p.Bmax + b) * p.I + row] = f2bf(a);
-            break;
-        }
-        case OP_DWN: {
-            const float xm = __ldcg(p.x_mid + ((size_t)slot * p.Bmax + b) * p.H + row);
-            p.x_in[((size_t)((l + 1) % p.depth) * p.Bmax + b) * p.H + row] = xm + y0;
-            break;
-        }
-        default:
-            p.logits[(size_t)b * p.V + row] = y0;
+    } else {
+        for (int i = ctid; i < n * B; i += NCW * 32) {
+            const int rr = i / B, b = i % B, row = t.r0 + rr;
+            const float y0 = y_of(0, rr, b);
+            switch (t.op) {
+            case OP_QKV: {
+                const int base = t.mat == MAT_Q ? 0 : t.mat == MAT_K ? p.nq * p.d : (p.nq + p.nkv) * p.d;
+                st_ll(p.qkv + ((size_t)slot * p.Bmax + b) * p.qkv_rows + base + row, __float_as_uint(y0), ep);
+                break;
+            }
+            case OP_OPR: {
+                const float xr = x_in_value(p, s, l, b, row, ti);
+                st_ll(p.x_mid + ((size_t)slot * p.Bmax + b) * p.H + row, __float_as_uint(xr + y0), ep);
+                break;
+            }
+            case OP_DWN: {
+                const float xm =
+                    ll_wait1(p, s, p.x_mid + ((size_t)slot * p.Bmax + b) * p.H + row, ver(p, l), ti, WB_XMID);
+                st_ll(p.x_in + ((size_t)((l + 1) % p.depth) * p.Bmax + b) * p.H + row, __float_as_uint(xm + y0),
+                      ep_next);
+                break;
+            }
+            default:
+                p.logits[(size_t)b * p.V + row] = y0;
+            }
         }
     }
-    return !cbar_or(s.misc->abort != 0);
+    const bool ok = !cbar_or(s.misc->abort != 0);
+    if (p.trace && ctid == 0) s.misc->t_epi = now_ns();
+    return ok;
 }
 
 /* ----------------------------------------------------------- attention */
@@ -612,6 +797,7 @@ struct AttSmem {
     uint16_t *knew;  /* [d] bf16(rope(k)) of position p */
     uint16_t *vnew;  /* [d] */
     float *wst;      /* [NCW][d + PART_PAD]: per-warp (o, m, l) */
+    float *sbuf;     /* [NCW][32]: per-warp scores, then probabilities, of a block */
 };
 
 __device__ __forceinline__ AttSmem att_smem(const Params &p, Smem &s) {
@@ -623,83 +809,113 @@ __device__ __forceinline__ AttSmem att_smem(const Params &p, Smem &s) {
     a.vnew = a.knew + p.d;
     base += align_up(2 * p.d * 2, 16);
     a.wst = reinterpret_cast<float *>(base);
+    a.sbuf = a.wst + NCW * (p.d + PART_PAD);
     return a;
 }
 
-/* per-warp online-softmax state; a warp owns one head and a subset of positions */
+/* Online-softmax state of one warp, which owns one head and a subset of the
+ * positions.  LP = d / 8 lanes share a position when scoring (8 elements
+ * each); for the P.V product every lane owns d / 32 output elements. */
 template <int LP>
 struct AttState {
     float q[8];
-    float o[8];
-    float m, l;
+    float o[LP / 4];
+    float m;  /* running max, warp-uniform (log2 units) */
+    float l;  /* this lane's share of the running sum */
 };
 
+/* positions j0 .. j0 + nb - 1 (nb <= 32) of a K/V tile in shared memory */
 template <int LP>
-__device__ __forceinline__ void att_tile(AttState<LP> &st, const uint16_t *Kt, const uint16_t *Vt, int nt, int d,
-                                         int sub, int wph, int lane) {
-    constexpr int PW = 32 / LP;
+__device__ __forceinline__ void att_block(AttState<LP> &st, const uint16_t *Kt, const uint16_t *Vt, int j0, int nb,
+                                          int d, float *sb, int lane) {
+    constexpr int PW = 32 / LP, EL = LP / 4;
     const int pg = lane / LP, ch = lane % LP;
-    for (int j0 = sub * PW; j0 < nt; j0 += wph * PW) {
-        const int j = j0 + pg;
-        const bool valid = j < nt;
+#pragma unroll
+    for (int it = 0; it < LP; ++it) {
+        const int jj = it * PW + pg;
         float sc = -INFINITY;
-        uint4 vv = make_uint4(0, 0, 0, 0);
-        if (valid) {
-            const uint4 kv = reinterpret_cast<const uint4 *>(Kt + (size_t)j * d)[ch];
-            vv = reinterpret_cast<const uint4 *>(Vt + (size_t)j * d)[ch];
-            sc = st.q[0] * bf_lo(kv.x) + st.q[1] * bf_hi(kv.x) + st.q[2] * bf_lo(kv.y) + st.q[3] * bf_hi(kv.y) +
-                 st.q[4] * bf_lo(kv.z) + st.q[5] * bf_hi(kv.z) + st.q[6] * bf_lo(kv.w) + st.q[7] * bf_hi(kv.w);
+        if (jj < nb) {
+            const uint4 kv = reinterpret_cast<const uint4 *>(Kt + (size_t)(j0 + jj) * d)[ch];
+            const float s0 = st.q[0] * bf_lo(kv.x) + st.q[1] * bf_hi(kv.x) + st.q[2] * bf_lo(kv.y) + st.q[3] * bf_hi(kv.y);
+            const float s1 = st.q[4] * bf_lo(kv.z) + st.q[5] * bf_hi(kv.z) + st.q[6] * bf_lo(kv.w) + st.q[7] * bf_hi(kv.w);
+            sc = s0 + s1;
         }
 #pragma unroll
         for (int o = LP / 2; o > 0; o >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o);
-        float mit = sc;
-#pragma unroll
-        for (int o = LP; o < 32; o <<= 1) mit = fmaxf(mit, __shfl_xor_sync(0xffffffffu, mit, o));
-        const float mnew = fmaxf(st.m, mit);
-        if (mnew == -INFINITY) continue;
-        const float alpha = exp2f(st.m - mnew);
-        const float pj = valid ? exp2f(sc - mnew) : 0.f;
-        st.l = st.l * alpha + pj;
-        const float v[8] = {bf_lo(vv.x), bf_hi(vv.x), bf_lo(vv.y), bf_hi(vv.y),
-                            bf_lo(vv.z), bf_hi(vv.z), bf_lo(vv.w), bf_hi(vv.w)};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) st.o[e] = st.o[e] * alpha + pj * v[e];
-        st.m = mnew;
+        if (ch == 0) sb[jj] = sc;
     }
+    __syncwarp();
+    const float si = sb[lane];
+    float mb = si;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+    const float mnew = fmaxf(st.m, mb);
+    const float alpha = exp2f(st.m - mnew);
+    const float pi = lane < nb ? exp2f(si - mnew) : 0.f;
+    st.l = st.l * alpha + pi;
+    st.m = mnew;
+#pragma unroll
+    for (int e = 0; e < EL; ++e) st.o[e] *= alpha;
+    __syncwarp();
+    sb[lane] = pi;
+    __syncwarp();
+    const uint16_t *vcol = Vt + (size_t)j0 * d + lane * EL;
+    for (int i = 0; i < nb; ++i) {
+        const float w = sb[i];
+        if constexpr (EL == 2) {
+            const uint32_t v = *reinterpret_cast<const uint32_t *>(vcol + (size_t)i * d);
+            st.o[0] = fmaf(w, bf_lo(v), st.o[0]);
+            st.o[1] = fmaf(w, bf_hi(v), st.o[1]);
+        } else {
+            const uint2 v = *reinterpret_cast<const uint2 *>(vcol + (size_t)i * d);
+            st.o[0] = fmaf(w, bf_lo(v.x), st.o[0]);
+            st.o[1] = fmaf(w, bf_hi(v.x), st.o[1]);
+            st.o[2] = fmaf(w, bf_lo(v.y), st.o[2]);
+            st.o[3] = fmaf(w, bf_hi(v.y), st.o[3]);
+        }
+    }
+    __syncwarp();
 }
 
 template <int LP>
-__device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, uint32_t &it, int ctid, int warp,
-                              int lane) {
-    constexpr int PW = 32 / LP;
+__device__ __forceinline__ void att_tile(AttState<LP> &st, const uint16_t *Kt, const uint16_t *Vt, int nt, int d,
+                                         int sub, int wph, float *sb, int lane) {
+    for (int j0 = sub * 32; j0 < nt; j0 += wph * 32) att_block<LP>(st, Kt, Vt, j0, min(32, nt - j0), d, sb, lane);
+}
+
+template <int LP>
+__device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, Ring &rg, int ctid, int warp, int lane) {
     const int d = p.d, G = p.G, NS = p.n_slots;
     const int l = t.layer, slot = l % p.depth, b = t.b, grp = t.g;
     const AttGeo ag = att_geo(p, t);
     const bool active_seq = b < p.batch;
     AttSmem as = att_smem(p, s);
 
-    /* prologue: rotate q and the new k, round k and v to bf16 */
+    /* prologue: wait for q, k, v of this kv head, rotate q and the new k,
+     * round k and v to bf16 */
     if (active_seq) {
-        const float *qkv = p.qkv + ((size_t)slot * p.Bmax + b) * p.qkv_rows;
-        const float *rope = p.rope + (size_t)ag.p * d;  /* [d/2][2] */
+        const uint64_t *qkv = p.qkv + ((size_t)slot * p.Bmax + b) * p.qkv_rows;
+        const float *rope = p.rope + (size_t)ag.p * d; /* [d/2][2] */
         const int half = d / 2;
         for (int i = ctid; i < (G + 2) * half; i += NCW * 32) {
             const int h = i / half, e = i % half;
             const float c = __ldg(rope + 2 * e), sn = __ldg(rope + 2 * e + 1);
+            const uint64_t *src = h < G ? qkv + (size_t)(grp * G + h) * d
+                                 : h == G ? qkv + (size_t)p.nq * d + grp * d
+                                          : qkv + (size_t)(p.nq + p.nkv) * d + grp * d;
+            const uint32_t f = ver(p, l);
+            uint64_t wa = ld_ll1(src + e), wb = ld_ll1(src + e + half);
+            const float a = ll_flag(wa) == f ? ll_f(wa) : ll_wait1(p, s, src + e, f, ti, WB_QKV);
+            const float bb = ll_flag(wb) == f ? ll_f(wb) : ll_wait1(p, s, src + e + half, f, ti, WB_QKV);
             if (h < G) {
-                const float *src = qkv + (size_t)(grp * G + h) * d;
-                const float a = __ldcg(src + e), bb = __ldcg(src + e + half);
                 as.q[h * d + e] = (a * c - bb * sn) * p.qk_scale_log2;
                 as.q[h * d + e + half] = (bb * c + a * sn) * p.qk_scale_log2;
             } else if (h == G) {
-                const float *src = qkv + (size_t)p.nq * d + grp * d;
-                const float a = __ldcg(src + e), bb = __ldcg(src + e + half);
                 as.knew[e] = f2bf(a * c - bb * sn);
                 as.knew[e + half] = f2bf(bb * c + a * sn);
             } else {
-                const float *src = qkv + (size_t)(p.nq + p.nkv) * d + grp * d;
-                as.vnew[e] = f2bf(__ldcg(src + e));
-                as.vnew[e + half] = f2bf(__ldcg(src + e + half));
+                as.vnew[e] = f2bf(a);
+                as.vnew[e + half] = f2bf(bb);
             }
         }
     }
@@ -716,40 +932,43 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, u
     const bool wactive = warp < wph * G;
     const int h = warp % G, sub = warp / G;
     const int ch = lane % LP;
+    constexpr int EL = LP / 4;
+    float *sb = as.sbuf + warp * 32;
     AttState<LP> st;
     st.m = -INFINITY;
     st.l = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        st.o[e] = 0.f;
-        st.q[e] = wactive ? as.q[h * d + ch * 8 + e] : 0.f;
-    }
+    for (int e = 0; e < 8; ++e) st.q[e] = wactive ? as.q[h * d + ch * 8 + e] : 0.f;
+#pragma unroll
+    for (int e = 0; e < EL; ++e) st.o[e] = 0.f;
 
-    for (int k = 0; k < ag.ntile; ++k, ++it) {
-        const int sl = (int)(it % (uint32_t)NS);
+    for (int k = 0; k < ag.ntile; ++k, rg.advance(NS)) {
+        const int sl = rg.slot;
         if (s.misc->abort) continue;
-        if (!wait_phase(p, s, &s.full[sl], (it / NS) & 1u, 2, ti)) continue;
+        const unsigned long long tw0 = p.trace ? now_ns() : 0;
+        if (!wait_phase(p, s, &s.full[sl], rg.pass & 1u, 2, ti)) continue;
+        const unsigned long long tw1 = p.trace ? now_ns() : 0;
+        if (p.trace && k == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
         const int t0 = ag.s0 + k * t.rows_per_stage;
         const int nt = min(ag.e, t0 + (int)t.rows_per_stage) - t0;
         const uint16_t *Kt = reinterpret_cast<const uint16_t *>(s.ring + (size_t)sl * p.slot_bytes);
         const uint16_t *Vt = Kt + (size_t)t.rows_per_stage * d;
-        if (wactive) att_tile<LP>(st, Kt, Vt, nt, d, sub, wph, lane);
+        if (wactive) att_tile<LP>(st, Kt, Vt, nt, d, sub, wph, sb, lane);
+        if (p.trace && warp == 0 && lane == 0) {
+            s.misc->t_wait_full += tw1 - tw0;
+            s.misc->t_tiles += now_ns() - tw1;
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.empty[sl]);
     }
-    if (active_seq && (t.flags & TF_NEW_TOKEN) && wactive) att_tile<LP>(st, as.knew, as.vnew, 1, d, sub, wph, lane);
+    if (active_seq && (t.flags & TF_NEW_TOKEN) && wactive) att_tile<LP>(st, as.knew, as.vnew, 1, d, sub, wph, sb, lane);
 
-    /* reduce l and o over the position groups of the warp */
-#pragma unroll
-    for (int o = LP; o < 32; o <<= 1) {
-        st.l += __shfl_xor_sync(0xffffffffu, st.l, o);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) st.o[e] += __shfl_xor_sync(0xffffffffu, st.o[e], o);
-    }
-    if (wactive && lane < LP) {
+    /* the warp's state: l summed over lanes, o spread EL elements per lane */
+    st.l = warp_sum(st.l);
+    if (wactive) {
         float *w = as.wst + (size_t)warp * (d + PART_PAD);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) w[ch * 8 + e] = st.o[e];
+        for (int e = 0; e < EL; ++e) w[lane * EL + e] = st.o[e];
         if (lane == 0) {
             w[d] = st.m;
             w[d + 1] = st.l;
@@ -757,28 +976,86 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, u
     }
     if (cbar_or(s.misc->abort != 0)) return false;
 
-    /* merge the warps of each head; write the chunk's partial (o unnormalised, m, l) */
+    /* merge the warps of each head; publish the chunk's partial (o unnormalised, m, l) */
     if (active_seq) {
-        float *part = p.part + ((((size_t)slot * p.Bmax + b) * p.nkv + grp) * p.C + t.r0) * G * (d + PART_PAD);
+        const uint32_t ep = ver(p, l) - ((t.flags & TF_SKIP_SIGNAL) ? (uint32_t)(p.L + 1) : 0u);
+        uint64_t *part = p.part + ((((size_t)slot * p.Bmax + b) * p.nkv + grp) * p.C + t.r0) * G * (d + PART_PAD);
         for (int i = ctid; i < G * (d + 2); i += NCW * 32) {
             const int hh = i / (d + 2), e = i % (d + 2);
             float M = -INFINITY;
-            for (int sb = 0; sb < wph; ++sb) M = fmaxf(M, as.wst[(size_t)(sb * G + hh) * (d + PART_PAD) + d]);
+            for (int w2 = 0; w2 < wph; ++w2) M = fmaxf(M, as.wst[(size_t)(w2 * G + hh) * (d + PART_PAD) + d]);
             float v = 0.f;
             if (e == d) {
                 v = M;
             } else if (M != -INFINITY) {
-                for (int sb = 0; sb < wph; ++sb) {
-                    const float *w = as.wst + (size_t)(sb * G + hh) * (d + PART_PAD);
+                for (int w2 = 0; w2 < wph; ++w2) {
+                    const float *w = as.wst + (size_t)(w2 * G + hh) * (d + PART_PAD);
                     const float mw = w[d];
                     if (mw == -INFINITY) continue;
                     v += exp2f(mw - M) * (e == d + 1 ? w[d + 1] : w[e]);
                 }
             }
-            part[(size_t)hh * (d + PART_PAD) + e] = v;
+            st_ll(part + (size_t)hh * (d + PART_PAD) + e, __float_as_uint(v), ep);
         }
     }
-    (void)PW;
+    return !cbar_or(s.misc->abort != 0);
+}
+
+/* Merge the C chunk partials of one (sequence, kv head) into bf16 attention
+ * outputs of its G heads: o = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c
+ * (the log-sum-exp combination of split softmax), in chunk order. */
+__device__ bool mrg_task(const Params &p, Smem &s, const Task &t, int ti, int ctid) {
+    const int d = p.d, G = p.G, C = t.r1, slot = t.layer % p.depth, b = t.b, grp = t.g;
+    if (b < p.batch) {
+        const uint32_t f = ver(p, t.layer);
+        const uint32_t ep = f - ((t.flags & TF_SKIP_SIGNAL) ? (uint32_t)(p.L + 1) : 0u);
+        const uint64_t *base = p.part + (((size_t)slot * p.Bmax + b) * p.nkv + grp) * C * G * (d + PART_PAD);
+        float *ml = s.fac;         /* [G][C] m, then factors */
+        float *lv = s.fac + G * C; /* [G][C] l */
+        for (int i = ctid; i < G * C; i += NCW * 32) {
+            const int h = i / C, c = i % C;
+            const uint64_t *pc = base + ((size_t)c * G + h) * (d + PART_PAD) + d;
+            ulonglong2 v = ld_ll2(pc);
+            if (!ll_ok(f, v)) ll_settle(p, s, pc, v, f, ti, WB_PART);
+            ml[i] = ll_f(v.x);
+            lv[i] = ll_f(v.y);
+        }
+        if (cbar_or(s.misc->abort != 0)) return false;
+        if (ctid < G) {
+            float M = -INFINITY;
+            for (int c = 0; c < C; ++c) M = fmaxf(M, ml[ctid * C + c]);
+            float den = 0.f;
+            for (int c = 0; c < C; ++c) {
+                const float mc = ml[ctid * C + c];
+                const float f = mc == -INFINITY ? 0.f : exp2f(mc - M);
+                ml[ctid * C + c] = f;
+                den += f * lv[ctid * C + c];
+            }
+            const float inv = 1.f / den;
+            for (int c = 0; c < C; ++c) ml[ctid * C + c] *= inv;
+        }
+        cbar();
+        uint64_t *out = p.aout + (((size_t)slot * p.Bmax + b) * p.nq * d + (size_t)grp * G * d) / 2;
+        const int q4 = d / 4;
+        for (int i = ctid; i < G * q4; i += NCW * 32) {
+            const int h = i / q4, e4 = i % q4;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int c = 0; c < C; ++c) {
+                const float w = ml[h * C + c];
+                const uint64_t *src = base + ((size_t)c * G + h) * (d + PART_PAD) + 4 * e4;
+                ulonglong2 u = ld_ll2(src), v = ld_ll2(src + 2);
+                if (!ll_ok(f, u)) ll_settle(p, s, src, u, f, ti, WB_PART);
+                if (!ll_ok(f, v)) ll_settle(p, s, src + 2, v, f, ti, WB_PART);
+                o.x = fmaf(w, ll_f(u.x), o.x);
+                o.y = fmaf(w, ll_f(u.y), o.y);
+                o.z = fmaf(w, ll_f(v.x), o.z);
+                o.w = fmaf(w, ll_f(v.y), o.w);
+            }
+            st_ll(out + ((size_t)h * d + 4 * e4) / 2, pack_bf2(o.x, o.y), ep);
+            st_ll(out + ((size_t)h * d + 4 * e4) / 2 + 1, pack_bf2(o.z, o.w), ep);
+        }
+    }
     return !cbar_or(s.misc->abort != 0);
 }
 
@@ -793,7 +1070,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p)
     s.misc = reinterpret_cast<Misc *>(smem + SMEM_BARRIERS);
     s.res = reinterpret_cast<float *>(smem + SMEM_BARRIERS + SMEM_MISC);
     s.sc = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(s.res) + p.result_bytes);
-    s.act = reinterpret_cast<uint8_t *>(s.sc) + p.scale_bytes;
+    s.fac = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(s.sc) + p.scale_bytes);
+    s.act = reinterpret_cast<uint8_t *>(s.fac) + p.fac_bytes;
     s.ring = s.act + p.act_bytes;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -825,30 +1103,54 @@ __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p)
         if (lane == 0) loader(p, s, tbeg, tend);
     } else {
         const int ctid = tid;
-        uint32_t it = 0;
+        Ring rg{0, 0, 0};
         for (int ti = tbeg; ti < tend; ++ti) {
             Task t;
             load_task(p.tasks + ti, t);
-            /* weights-only inputs can be fetched before the dependency is met */
-            if (I8 && t.op != OP_ATT) {
+            /* weights-only inputs are fetched before the task's inputs are ready */
+            if (I8 && t.op != OP_ATT && t.op != OP_MRG) {
                 const int n = t.r1 - t.r0, nm = t.op == OP_GUP ? 2 : 1;
                 for (int i = ctid; i < n * nm; i += NCW * 32) {
                     const int m = i / n, rr = i % n;
                     s.sc[i] = __ldg(op_scales(p, t, m) + t.r0 + rr);
                 }
             }
-            if (ctid == 0 && t.wait_id != NO_WAIT) wait_counter(p, s, t.wait_id, t.wait_count, ti);
-            if (cbar_or(s.misc->abort != 0)) break;
+            uint2 gpre[MAXG];
+            if (NB == 1 && (t.op == OP_QKV || t.op == OP_GUP || t.op == OP_LMH) && t.ksplit == 1) {
+                const uint16_t *gain = t.op == OP_QKV   ? p.layers[t.layer].attn_norm
+                                       : t.op == OP_GUP ? p.layers[t.layer].mlp_norm
+                                                        : p.final_norm;
+#pragma unroll
+                for (int g = 0; g < MAXG; ++g) {
+                    const int i4 = ctid + g * NCW * 32;
+                    gpre[g] = i4 < p.H / 4 ? __ldg(reinterpret_cast<const uint2 *>(gain) + i4) : make_uint2(0, 0);
+                }
+            }
+            unsigned long long *tr = p.trace ? p.trace + 16 * (size_t)ti : nullptr;
+            if (tr && ctid == 0) {
+                tr[0] = tr[1] = now_ns();
+                s.misc->t_first = 0;
+                s.misc->t_wait_full = 0;
+                s.misc->t_tiles = 0;
+                s.misc->t_pro = s.misc->t_stages = s.misc->t_epi = 0;
+            }
             bool ok;
             if (t.op == OP_ATT)
-                ok = p.d == 64 ? att_task_impl<8>(p, s, t, ti, it, ctid, warp, lane)
-                               : att_task_impl<16>(p, s, t, ti, it, ctid, warp, lane);
+                ok = p.d == 64 ? att_task_impl<8>(p, s, t, ti, rg, ctid, warp, lane)
+                               : att_task_impl<16>(p, s, t, ti, rg, ctid, warp, lane);
+            else if (t.op == OP_MRG)
+                ok = mrg_task(p, s, t, ti, ctid);
             else
-                ok = gemv_task<I8, NB>(p, s, t, ti, it, ctid, warp, lane);
+                ok = gemv_task<I8, NB>(p, s, t, ti, rg, gpre, ctid, warp, lane);
             if (!ok) break;
-            if (ctid == 0 && !(t.flags & TF_SKIP_SIGNAL)) {
-                __threadfence();
-                for (int k = 0; k < t.nsig; ++k) atomicAdd(p.counters + (size_t)t.sig[k] * COUNTER_STRIDE, 1u);
+            if (tr && ctid == 0) {
+                tr[2] = s.misc->t_first;
+                tr[3] = now_ns();
+                tr[4] = s.misc->t_wait_full;
+                tr[5] = s.misc->t_tiles;
+                tr[6] = s.misc->t_pro;
+                tr[7] = s.misc->t_stages;
+                tr[8] = s.misc->t_epi;
             }
         }
     }
@@ -865,8 +1167,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p)
 }
 
 /* ----------------------------------------------------------- host entry */
-
-typedef void (*KernelFn)(const Params);
 
 KernelFn select_kernel(bool int8, int max_batch) {
     if (int8) return max_batch == 1 ? amk_decode_kernel<true, 1> : amk_decode_kernel<true, MAXB>;

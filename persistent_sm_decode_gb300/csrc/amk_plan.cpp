@@ -50,6 +50,7 @@ constexpr double SM_BPS_MAX = 1.5e11;  /* what one CTA's bulk copies can pull al
 constexpr double L2_SM_BPS = 1.5e11;   /* one CTA reading activations from L2 */
 constexpr double T_SYNC = 2.0e-6;      /* producer signal -> consumer sees it -> inputs loaded */
 constexpr double T_TASK = 0.3e-6;      /* per-task fixed cost (barriers, epilogue, signal) */
+constexpr double T_COPY = 0.33e-6;     /* one bulk copy through a CTA's ring (measured floor per slot) */
 
 std::string fmt(const char *f, ...) __attribute__((format(printf, 1, 2)));
 std::string fmt(const char *f, ...) {
@@ -64,55 +65,75 @@ std::string fmt(const char *f, ...) {
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
 struct SmemModel {
-    int act, result, scales, fixed;
+    int act, result, scales, fac, fixed;
 };
 
 int att_smem_need(const Geo &g) {
-    return align_up(g.G * g.d * 4, 16) + align_up(2 * g.d * 2, 16) + NCW * (g.d + PART_PAD) * 4 + 256;
+    return align_up(g.G * g.d * 4, 16) + align_up(2 * g.d * 2, 16) + NCW * (g.d + PART_PAD) * 4 + NCW * 32 * 4 + 256;
 }
 
 int max_task_rows(const Geo &g, int op, int n_sm) {
     return std::min(ceil_div(g.rows(op), n_sm), MAX_TASK_ROWS);
 }
 
-SmemModel smem_model(const Geo &g, int ks, int n_sm) {
+int rows_per_slot(const Geo &g, int op, int ks, int slot) {
+    int kc = g.K(op) / ksplit_for(g, op, ks);
+    return std::max(1, std::min(256, slot / (kc * g.web(op))));
+}
+
+/* Shared memory besides the ring: fp32 activation slice [B][K/ks], GEMV
+ * partial sums [rows][segments][B] (a tile of R < 8 rows is split into 8/R
+ * K segments so every consumer warp works), int8 row scales, attention merge
+ * factors [B][n_heads][C]. */
+SmemModel smem_model(const Geo &g, int ks, int slot, int C, int n_sm) {
     SmemModel m{};
     m.act = att_smem_need(g);
     for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN, OP_LMH}) {
         int kc = g.K(op) / ksplit_for(g, op, ks);
-        m.act = std::max(m.act, g.B * kc * 2);
+        m.act = std::max(m.act, g.B * kc * 4);
+        int R = rows_per_slot(g, op, ks, slot);
+        int S = gemv_segments(g.B, kc, g.web(op) == 1, R);
         int rows = max_task_rows(g, op, n_sm) + 1;  /* +1: a QKV matrix boundary can split a block */
-        m.result = std::max(m.result, rows * g.nmat(op) * g.B * 4);
+        m.result = std::max(m.result, rows * g.nmat(op) * S * g.B * 4);
         if (g.scaled(op)) m.scales = std::max(m.scales, rows * g.nmat(op) * 4);
     }
+    m.fac = g.B * g.nq * C * 4;
     m.act = align_up(m.act, 128);
     m.result = align_up(m.result, 128);
     m.scales = align_up(m.scales, 128);
-    m.fixed = SMEM_BARRIERS + SMEM_MISC + m.act + m.result + m.scales;
+    m.fac = align_up(m.fac, 128);
+    m.fixed = SMEM_BARRIERS + SMEM_MISC + m.act + m.result + m.scales + m.fac;
     return m;
 }
 
 double model_cost_us(const Geo &g, const Knobs &k, int n_sm) {
-    const double per_sm = HBM_BPS / n_sm;
+    /* a CTA streams at most one ring slot per T_COPY, and its share of HBM */
+    const double per_sm = std::min(HBM_BPS / n_sm, k.slot_bytes / T_COPY);
     const double ring_hide = (double)k.n_slots * k.slot_bytes / per_sm;
     auto stall = [&](double pro) { return std::max(0.0, T_SYNC + pro - ring_hide); };
     double t = 0;
     for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN}) {
-        double bytes = (double)ceil_div(g.rows(op), n_sm) * g.nmat(op) * g.row_bytes(op);
+        int ks = ksplit_for(g, op, k.ksplit);
+        int R = rows_per_slot(g, op, k.ksplit, k.slot_bytes);
+        double rows = ceil_div(g.rows(op), n_sm);
+        double stages = std::ceil(rows / R) * ks * g.nmat(op);
+        double bytes = rows * g.nmat(op) * g.row_bytes(op);
+        double fill = bytes / (stages * k.slot_bytes); /* slot fraction actually used */
         double pro;
-        if (op == OP_OPR) pro = (double)g.B * g.nq * k.C * (g.d + PART_PAD) * 4 / L2_SM_BPS;
+        if (op == OP_OPR) pro = (double)g.B * g.nq * g.d * 2 / L2_SM_BPS;
         else if (op == OP_DWN) pro = (double)g.B * g.I * 2 / L2_SM_BPS;
         else pro = (double)g.B * g.H * 4 / L2_SM_BPS;
-        int ks = ksplit_for(g, op, k.ksplit);
-        t += g.L * (bytes / per_sm + stall(pro) + T_TASK * ks);
+        t += g.L * (bytes / (per_sm * std::max(fill, 1e-3)) + stall(pro) + T_TASK * ks);
     }
     {
+        /* attention chunks, then the merge of each (sequence, kv head) */
         int T = g.B * g.nkv * k.C;
         double task_bytes = (double)g.Smax / k.C * g.d * 4;
         int per = ceil_div(T, n_sm), active = std::min(T, n_sm);
-        double bw = std::min(SM_BPS_MAX, HBM_BPS / active);
+        double bw = std::min(std::min(SM_BPS_MAX, HBM_BPS / active), k.slot_bytes / T_COPY);
         double pro = (double)(g.G + 2) * g.d * 4 / L2_SM_BPS;
-        t += g.L * (per * task_bytes / bw + stall(pro) + T_TASK * per);
+        double merge = (double)k.C * g.G * (g.d + PART_PAD) * 4 / L2_SM_BPS;
+        t += g.L * (per * task_bytes / bw + stall(pro) + T_TASK * per + T_SYNC + merge);
     }
     {
         double bytes = (double)ceil_div(g.V, n_sm) * g.row_bytes(OP_LMH);
@@ -128,13 +149,14 @@ struct Builder {
     const Knobs &k;
     int n_sm;
     amk_plan *P;
-    int per_layer;  /* counters per layer: nkv QKV groups + ATT + OPR + GUP + DWN */
+    int per_layer;  /* counters per layer: nkv QKV groups, B*nkv attention chunks, MRG, OPR, GUP, DWN */
 
     int cid_group(int l, int grp) const { return l * per_layer + grp; }
-    int cid_att(int l) const { return l * per_layer + g.nkv; }
-    int cid_opr(int l) const { return l * per_layer + g.nkv + 1; }
-    int cid_gup(int l) const { return l * per_layer + g.nkv + 2; }
-    int cid_dwn(int l) const { return l * per_layer + g.nkv + 3; }
+    int cid_chunk(int l, int b, int grp) const { return l * per_layer + g.nkv + b * g.nkv + grp; }
+    int cid_att(int l) const { return l * per_layer + g.nkv + g.B * g.nkv; }
+    int cid_opr(int l) const { return cid_att(l) + 1; }
+    int cid_gup(int l) const { return cid_att(l) + 2; }
+    int cid_dwn(int l) const { return cid_att(l) + 3; }
 
     Task base(int op, int l) const {
         Task t;
@@ -161,23 +183,24 @@ struct Builder {
         a.e1 = e1;
         return a;
     }
-    int rows_per_stage(int op, int ks) const {
-        int kc = g.K(op) / ks;
-        return std::max(1, std::min(256, k.slot_bytes / (kc * g.web(op))));
-    }
+    int rows_per_stage(int op, int ks) const { return rows_per_slot(g, op, ks, k.slot_bytes); }
 
     /* Even row split of `op` over CTAs; each CTA's range is cut into tasks of at
      * most MAX_TASK_ROWS rows (and, for QKV, at matrix and signal-count limits). */
     void gemv_level(int op, int l) {
         int rows = g.rows(op);
         int ks = ksplit_for(g, op, k.ksplit);
+        /* gate/up tasks start on even rows: two SwiGLU outputs share a word */
+        const int unit = op == OP_GUP ? 2 : 1;
         for (int s = 0; s < n_sm; ++s) {
-            int a = (int)((int64_t)s * rows / n_sm), e = (int)((int64_t)(s + 1) * rows / n_sm);
+            int a = unit * (int)((int64_t)s * (rows / unit) / n_sm);
+            int e = unit * (int)((int64_t)(s + 1) * (rows / unit) / n_sm);
             while (a < e) {
                 int b = std::min(e, a + MAX_TASK_ROWS);
                 Task t = base(op, l);
                 t.ksplit = (uint8_t)ks;
                 t.rows_per_stage = (uint16_t)rows_per_stage(op, ks);
+                t.seg = (uint8_t)gemv_segments(g.B, g.K(op) / ks, g.web(op) == 1, t.rows_per_stage);
                 std::vector<Access> ac;
                 if (op == OP_QKV) {
                     /* stay inside one matrix and touch at most MAX_SIG groups */
@@ -207,7 +230,7 @@ struct Builder {
                     if (op == OP_OPR) {
                         t.wait_id = (uint16_t)cid_att(l);
                         t.sig[t.nsig++] = (uint16_t)cid_opr(l);
-                        ac.push_back(acc(BUF_PART, false, l, 0, g.B, 0, (int64_t)g.nkv * k.C * g.G));
+                        ac.push_back(acc(BUF_AOUT, false, l, 0, g.B, 0, (int64_t)g.nq * g.d));
                         if (l > 0) ac.push_back(acc(BUF_XIN, false, l, 0, g.B, a, b));
                         ac.push_back(acc(BUF_XMID, true, l, 0, g.B, a, b));
                     } else if (op == OP_GUP) {
@@ -246,7 +269,7 @@ struct Builder {
             x.g = (uint16_t)grp;
             x.rows_per_stage = (uint16_t)k.att_tile;
             x.wait_id = (uint16_t)cid_group(l, grp);
-            x.sig[x.nsig++] = (uint16_t)cid_att(l);
+            x.sig[x.nsig++] = (uint16_t)cid_chunk(l, b, grp);
             if (c == k.C - 1) x.flags |= TF_NEW_TOKEN;
             std::vector<Access> ac;
             ac.push_back(acc(BUF_QKV, false, l, b, b + 1, (int64_t)grp * g.G * g.d, (int64_t)(grp + 1) * g.G * g.d));
@@ -256,13 +279,26 @@ struct Builder {
             ac.push_back(acc(BUF_PART, true, l, b, b + 1, pr, pr + g.G));
             if (x.flags & TF_NEW_TOKEN) ac.push_back(acc(BUF_KVNEW, true, l, b, b + 1, grp, grp + 1));
             add(sm, x, std::move(ac));
+            if (c == k.C - 1) {
+                /* the merge of this (sequence, kv head) follows its last chunk on the same CTA */
+                Task m = base(OP_MRG, l);
+                m.r1 = k.C;
+                m.b = (uint16_t)b;
+                m.g = (uint16_t)grp;
+                m.wait_id = (uint16_t)cid_chunk(l, b, grp);
+                m.sig[m.nsig++] = (uint16_t)cid_att(l);
+                std::vector<Access> am;
+                am.push_back(acc(BUF_PART, false, l, b, b + 1, (int64_t)grp * k.C * g.G, (int64_t)(grp + 1) * k.C * g.G));
+                am.push_back(acc(BUF_AOUT, true, l, b, b + 1, (int64_t)grp * g.G * g.d, (int64_t)(grp + 1) * g.G * g.d));
+                add(sm, m, std::move(am));
+            }
         }
     }
 
     void run() {
         P->sm_tasks.assign(n_sm, {});
         P->acc.assign(n_sm, {});
-        per_layer = g.nkv + 4;
+        per_layer = g.nkv + g.B * g.nkv + 4;
         for (int l = 0; l < g.L; ++l) {
             gemv_level(OP_QKV, l);
             att_level(l);
@@ -272,7 +308,7 @@ struct Builder {
         }
         gemv_level(OP_LMH, g.L - 1);
         P->n_counters = g.L * per_layer;
-        P->n_levels = 5 * g.L + 1;
+        P->n_levels = 6 * g.L + 1;
         /* wait counts = producers per counter */
         std::vector<uint32_t> prod(P->n_counters, 0);
         for (auto &v : P->sm_tasks)
@@ -320,7 +356,8 @@ ScratchSizes scratch_sizes(const amk_plan &p) {
     s.x_mid = D * B * g.H;
     s.qkv = D * B * g.qkv_rows;
     s.part = D * B * g.nkv * p.k.C * g.G * (g.d + PART_PAD);
-    s.act = D * B * g.I;
+    s.aout = D * B * g.nq * g.d / 2;
+    s.act = D * B * g.I / 2;
     return s;
 }
 
@@ -339,7 +376,8 @@ static std::string check_config(const amk_config &c, int batch) {
     if (c.weight_dtype != AMK_WEIGHT_BF16 && c.weight_dtype != AMK_WEIGHT_INT8) return "unknown weight dtype";
     if (c.tied_embeddings && c.weight_dtype == AMK_WEIGHT_INT8) return "tied embeddings need bf16 weights";
     if (!(c.rms_eps >= 0.0f) || !(c.rope_theta > 0.0f)) return "bad rms_eps or rope_theta";
-    if (c.n_layers > 4096 || (int64_t)c.n_layers * (c.n_kv_heads + 4) >= NO_WAIT) return "too many layers";
+    if (c.n_layers > 4096 || (int64_t)c.n_layers * (c.n_kv_heads * (c.max_batch + 1) + 4) >= NO_WAIT)
+        return "too many layers";
     return "";
 }
 
@@ -376,14 +414,8 @@ amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_c
     int maxC = std::max(1, std::min(64, (4 * n_sm) / std::max(1, g.B * g.nkv)));
     for (int ks : ks_choices) {
         if (o.ksplit && ks != o.ksplit) continue;
-        SmemModel sm = smem_model(g, ks, n_sm);
         for (int slot : slot_choices) {
             if (o.slot_bytes && slot != o.slot_bytes) continue;
-            int avail = smem_per_cta - sm.fixed;
-            int ns = avail / slot;
-            if (o.n_slots) ns = std::min(ns, o.n_slots);
-            ns = std::min(ns, MAX_SLOTS);
-            if (ns < 2) continue;
             bool fits = true;
             for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN, OP_LMH})
                 if ((int64_t)(g.K(op) / ksplit_for(g, op, ks)) * g.web(op) > slot) fits = false;
@@ -391,6 +423,11 @@ amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_c
             if (!fits) continue;
             for (int C = 1; C <= maxC; ++C) {
                 if (o.att_chunks && C != o.att_chunks) continue;
+                SmemModel sm = smem_model(g, ks, slot, C, n_sm);
+                int ns = (smem_per_cta - sm.fixed) / slot;
+                if (o.n_slots) ns = std::min(ns, o.n_slots);
+                ns = std::min(ns, MAX_SLOTS);
+                if (ns < 2) continue;
                 Knobs k;
                 k.C = C;
                 k.slot_bytes = slot;
@@ -422,10 +459,11 @@ amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_c
     P->k = best;
     Builder bld{g, best, n_sm, P, 0};
     bld.run();
-    SmemModel sm = smem_model(g, best.ksplit, n_sm);
+    SmemModel sm = smem_model(g, best.ksplit, best.slot_bytes, best.C, n_sm);
     P->act_bytes = sm.act;
     P->result_bytes = sm.result;
     P->scale_bytes = sm.scales;
+    P->fac_bytes = sm.fac;
     P->smem_bytes = sm.fixed + best.n_slots * best.slot_bytes;
     P->modeled_us = best_cost;
     P->candidates = cands;
@@ -435,7 +473,7 @@ amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_c
     wb += (int64_t)g.rows(OP_LMH) * g.row_bytes(OP_LMH);
     P->weight_bytes = wb;
     ScratchSizes ss = scratch_sizes(*P);
-    P->scratch_bytes = 4 * (ss.x_in + ss.x_mid + ss.qkv + ss.part) + 2 * ss.act;
+    P->scratch_bytes = 8 * (ss.x_in + ss.x_mid + ss.qkv + ss.part + ss.aout + ss.act);
 
     /* ---- validate ---- */
     std::string why;
@@ -599,7 +637,8 @@ bool plan_validate(const amk_plan &p, std::string *msg) {
     auto overlap = [](const Access *x, const Access *y) {
         return x->b0 < y->b1 && y->b0 < x->b1 && x->e0 < y->e1 && y->e0 < x->e1;
     };
-    static const char *bufname[BUF_COUNT] = {"x_in", "x_mid", "qkv", "attn_partials", "swiglu_act", "kv_slot", "logits"};
+    static const char *bufname[BUF_COUNT] = {"x_in",       "x_mid",      "qkv",     "attn_partials",
+                                             "attn_output", "swiglu_act", "kv_slot", "logits"};
     auto where = [&](int t) { return fmt("cta %d task %d", sm_of[t], idx_of[t]); };
     for (auto &gk : groups) {
         const char *bn = bufname[gk.first.first];

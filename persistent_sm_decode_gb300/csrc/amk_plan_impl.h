@@ -14,7 +14,7 @@ namespace amk {
 
 /* Activation buffers whose accesses the validator tracks.  A buffer has
  * `depth` slots; the data of layer l lives in slot l % depth ("version" l). */
-enum : uint8_t { BUF_XIN = 0, BUF_XMID, BUF_QKV, BUF_PART, BUF_ACT, BUF_KVNEW, BUF_LOGITS, BUF_COUNT };
+enum : uint8_t { BUF_XIN = 0, BUF_XMID, BUF_QKV, BUF_PART, BUF_AOUT, BUF_ACT, BUF_KVNEW, BUF_LOGITS, BUF_COUNT };
 
 /* One read or write of a rectangle [b0, b1) x [e0, e1) of (buffer, slot). */
 struct Access {
@@ -63,7 +63,7 @@ struct amk_plan {
     std::vector<std::vector<amk::Task>> sm_tasks;
     std::vector<std::vector<std::vector<amk::Access>>> acc; /* parallel to sm_tasks */
     int n_counters = 0, n_levels = 0;
-    int act_bytes = 0, result_bytes = 0, scale_bytes = 0, smem_bytes = 0;
+    int act_bytes = 0, result_bytes = 0, scale_bytes = 0, fac_bytes = 0, smem_bytes = 0;
     int64_t weight_bytes = 0, scratch_bytes = 0;
     double modeled_us = 0, search_ms = 0;
     int candidates = 0;
@@ -77,7 +77,7 @@ amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_c
 bool plan_validate(const amk_plan &p, std::string *msg);
 /* Element counts of the scratch buffers described in Params. */
 struct ScratchSizes {
-    int64_t x_in, x_mid, qkv, part, act; /* elements */
+    int64_t x_in, x_mid, qkv, part, aout, act; /* 8-byte epoch-tagged words */
 };
 ScratchSizes scratch_sizes(const amk_plan &p);
 }  // namespace amk

@@ -41,6 +41,7 @@ class Result:
         self.argmax_agree = 0
         self.floor = 0.0          # same ratio for the fp32-accumulation build of the definition
         self.steps = 0
+        self.records = []         # (step, row, margin, gpu agrees, fp32-build max|dlogit| or None)
 
     def __repr__(self):
         return ("Result(worst=%.3g, floor=%.3g, max_abs=%.3g, argmax %d/%d, steps=%d)"
@@ -82,17 +83,21 @@ def teacher_forced(wl, model=None, kv=None, steps=None, options=None, batch=None
             bound = REL_TOL * np.abs(ref[i]).max() + ABS_TOL
             res.worst = max(res.worst, float(d.max() / bound))
             res.max_abs = max(res.max_abs, float(d.max()))
+        fdev = [None] * len(rows)
         if o32 is not None:
             f = o32.step(tokens[rows], pos[rows])
             for i in range(len(rows)):
                 bound = REL_TOL * np.abs(ref[i]).max() + ABS_TOL
-                res.floor = max(res.floor, float(np.abs(f[i] - ref[i]).max() / bound))
+                fdev[i] = float(np.abs(f[i] - ref[i]).max())
+                res.floor = max(res.floor, fdev[i] / bound)
         ref_tok, margin = oracle.greedy(ref)
         gpu_tok = np.argmax(got, axis=1).astype(np.int32)
         for i, b in enumerate(rows):
+            agree = bool(gpu_tok[b] == ref_tok[i])
+            res.records.append((s, b, float(margin[i]), agree, fdev[i]))
             if margin[i] > MARGIN:
                 res.checked_argmax += 1
-                res.argmax_agree += int(gpu_tok[b] == ref_tok[i])
+                res.argmax_agree += int(agree)
         nxt = gpu_tok.copy()
         for i, b in enumerate(rows):
             nxt[b] = ref_tok[i]
@@ -104,13 +109,18 @@ def teacher_forced(wl, model=None, kv=None, steps=None, options=None, batch=None
         # carry the same error bound as the logits; rounding them to bf16 adds
         # at most one bf16 ulp (2^-7 of the magnitude) on top.  The seeded
         # prefix must be untouched, bit for bit.
+        # With floor=True (deep stacks) a slot may also differ by up to twice
+        # what the fp32-accumulation build's cache differs from the oracle's.
         gk, gv = kv_from_device(kv_dev)
         for i, b in enumerate(rows):
-            for (ga, oa) in ((gk, orc.kc), (gv, orc.vc)):
+            for (ga, oa, fa) in ((gk, orc.kc, o32.kc if o32 else None), (gv, orc.vc, o32.vc if o32 else None)):
                 for p in range(int(pos0[b]), int(pos[b])):
                     x = synth.bf16_bits_to_f32(ga[:, b, :, p]).astype(np.float64)
                     y = synth.bf16_bits_to_f32(oa[:, i, :, p]).astype(np.float64)
                     bound = (REL_TOL + 2.0 ** -7) * np.abs(y).max() + ABS_TOL
+                    if fa is not None:
+                        f = synth.bf16_bits_to_f32(fa[:, i, :, p]).astype(np.float64)
+                        bound = max(bound, 2.0 * np.abs(f - y).max())
                     assert np.abs(x - y).max() <= bound, \
                         "KV slot %d of sequence %d: max diff %.3g > %.3g" % (p, b, np.abs(x - y).max(), bound)
                 x0 = ga[:, b, :, : int(pos0[b])]
@@ -129,9 +139,12 @@ def assert_end_to_end(res: Result):
     """Deep random-init stacks amplify single bf16 rounding flips (a plain fp32
     implementation of the definition already exceeds the logit bound): the
     GPU must meet the bound, or stay within twice the fp32-accumulation
-    build's deviation; greedy tokens agree at >= 95% of the clear-margin steps."""
+    build's deviation on the same run.  Its greedy token must equal the
+    oracle's wherever the oracle's top-2 margin exceeds both 1e-2 and twice
+    what fp32 rounding alone moved the logits at that step."""
     assert res.worst <= max(1.0, 2.0 * res.floor), res
-    assert res.argmax_agree >= 0.95 * res.checked_argmax, res
+    bad = [r for r in res.records if not r[3] and r[2] > max(MARGIN, 2.0 * (r[4] or 0.0))]
+    assert not bad, (res, bad[:5])
 
 
 class LayerResult:

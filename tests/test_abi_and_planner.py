@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(amk):
     for h in ("amk.h", "amk_plan.h"):
         src = open(os.path.join(ROOT, "include", h)).read()
         names |= set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(amk_\w+)\s*\(", src, re.M))
-    assert len(names) == 17 and {"amk_create", "amk_decode_step", "amk_destroy", "amk_plan_build"} <= names, names
+    assert len(names) == 18 and {"amk_create", "amk_decode_step", "amk_destroy", "amk_plan_build"} <= names, names
     for n in sorted(names):
         assert hasattr(lib, n), "libamk.so does not export %s" % n
 
@@ -54,7 +54,7 @@ def test_plans_validate_for_every_workload(amk, name):
     wl = synth.workload(name)
     p = amk.Plan(_cfg(amk, wl), wl.batch, 152)
     info = p.info()
-    assert info["n_levels"] == 5 * wl.n_layers + 1
+    assert info["n_levels"] == 6 * wl.n_layers + 1
     assert info["smem_bytes"] <= 232448
     assert p.validate()[0] == amk.OK
     assert info["weight_bytes"] == wl.weight_bytes() - (2 * wl.n_layers + 1) * wl.hidden * 2
@@ -81,6 +81,11 @@ def _coverage(wl, plan, B):
                 assert key not in att
                 att.add(key)
                 continue
+            if t["op"] == "MRG":
+                key = ("MRG", t["layer"], t["b"], t["g"])
+                assert key not in seen
+                seen[key] = 1
+                continue
             base = 0
             if t["op"] == "QKV":
                 base = [0, nq * d, (nq + nkv) * d][t["mat"]]
@@ -94,6 +99,7 @@ def _coverage(wl, plan, B):
             for r in range(n):
                 assert (op, l, r) in seen, "row not covered: %s layer %d row %d" % (op, l, r)
     assert len(att) == wl.n_layers * B * nkv * C
+    assert all(("MRG", l, b, g) in seen for l in range(wl.n_layers) for b in range(B) for g in range(nkv))
 
 
 def test_rejects_bad_configs(amk):
@@ -180,8 +186,12 @@ def brute_force_unsafe(wl, plan, B, depth):
                 hi = lo + (G * d if lo == g * G * d else d)
                 acc.append((k, "qkv", l, 0, b, b + 1, lo, hi))
             acc.append((k, "part", l, 1, b, b + 1, (g * C + c) * G, (g * C + c + 1) * G))
+        elif op == "MRG":
+            b, g = t["b"], t["g"]
+            acc.append((k, "part", l, 0, b, b + 1, g * C * G, (g + 1) * C * G))
+            acc.append((k, "aout", l, 1, b, b + 1, g * G * d, (g + 1) * G * d))
         elif op == "OPR":
-            acc.append((k, "part", l, 0, 0, B, 0, nkv * C * G))
+            acc.append((k, "aout", l, 0, 0, B, 0, nq * d))
             if l > 0:
                 acc.append((k, "xin", l, 0, 0, B, t["r0"], t["r1"]))
             acc.append((k, "xmid", l, 1, 0, B, t["r0"], t["r1"]))
