@@ -144,6 +144,29 @@ amk_status amk_decode_step(amk_handle *h, int32_t batch, const int32_t *tokens,
                            const int32_t *positions, void *kv_cache, float *logits,
                            amk_stream_t stream);
 
+/* A decode step that allocates nothing, for callers that cannot allocate
+ * device memory (an external allocator owns the device, or allocation is
+ * forbidden after start-up).  The method's pages have no counterpart: it is a
+ * deployment variant of amk_decode_step.  Instead of a handle, every call
+ * takes the configuration and the weights (as in amk_create, with default
+ * schedule options) and keeps the schedule, RoPE table, error word and
+ * activation scratch in one static device array of 16 MiB per device.
+ *   - The first call on a device, with that device current, looks up the
+ *     array's address (cudaGetSymbolAddress) and clears it; make that first
+ *     call before any stream capture.  A call whose configuration or weight
+ *     pointers differ from the previous call's re-plans and re-uploads.
+ *   - A configuration whose state does not fit in 16 MiB is refused with
+ *     AMK_ERR_UNSUPPORTED (the needed size is printed to stderr).
+ *   - tokens, positions, kv_cache, logits and stream are as in
+ *     amk_decode_step.  The call waits for the step to finish and returns
+ *     AMK_ERR_TIMEOUT or AMK_ERR_INVALID_ARG for a device-side failure.
+ *   - All calls share the array: calls are serialised by a process-wide lock;
+ *     calls that overlapped on the GPU would race. */
+amk_status amk_decode_step_noalloc(const amk_config *config, const amk_weights *weights,
+                                   int32_t batch, const int32_t *tokens,
+                                   const int32_t *positions, void *kv_cache,
+                                   float *logits, amk_stream_t stream);
+
 /* Synchronises the stream of the last step and reads the device error word.
  * Returns AMK_ERR_TIMEOUT if any wait of any step since the last call gave up
  * (then the handle's counters are reset, so the next step runs normally). */

@@ -95,6 +95,8 @@ def lib():
             L.amk_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights),
                                      ctypes.POINTER(ScheduleOptions), ctypes.POINTER(vp)]
             L.amk_decode_step.argtypes = [vp, i32, vp, vp, vp, vp, vp]
+            L.amk_decode_step_noalloc.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), i32, vp, vp,
+                                                  vp, vp, vp]
             L.amk_sync_status.argtypes = [vp]
             L.amk_destroy.argtypes = [vp]
             L.amk_last_error.argtypes = [vp, ctypes.POINTER(ErrorInfo)]
@@ -113,7 +115,7 @@ def lib():
             L.amk_plan_last_message.restype = ctypes.c_char_p
             L.amk_plan_destroy.argtypes = [vp]
             L.amk_plan_destroy.restype = None
-            for f in ("amk_create", "amk_decode_step", "amk_sync_status", "amk_destroy", "amk_last_error",
+            for f in ("amk_create", "amk_decode_step", "amk_decode_step_noalloc", "amk_sync_status", "amk_destroy", "amk_last_error",
                       "amk_get_plan_info", "amk_debug_drop_signal", "amk_debug_read_residuals", "amk_debug_read_trace", "amk_plan_build", "amk_plan_validate",
                       "amk_plan_get_info", "amk_plan_get_task", "amk_plan_mutate"):
                 getattr(L, f).restype = ctypes.c_int
@@ -292,3 +294,20 @@ class DecodeEngine:
             self.close()
         except Exception:
             pass
+
+
+def decode_step_noalloc(cfg: Config, embed, final_norm, layers: Sequence[Dict], tokens, positions, kv_cache,
+                        logits, lm_head=None, s_lm=None, stream=None, batch: Optional[int] = None) -> int:
+    """One decode step through amk_decode_step_noalloc, which keeps all of its
+    device state in a static array and allocates nothing (for callers that
+    cannot allocate device memory).  Arguments as for DecodeEngine and
+    DecodeEngine.step; waits for the step and returns the amk status."""
+    arr = (LayerWeights * cfg.n_layers)()
+    for l, d in enumerate(layers):
+        for k in _LAYER_KEYS + _SCALE_KEYS:
+            setattr(arr[l], k, _ptr(d.get(k)))
+    w = Weights(_ptr(embed), _ptr(final_norm), _ptr(lm_head), _ptr(s_lm), arr)
+    B = int(tokens.numel()) if batch is None else int(batch)
+    s = None if stream is None else (stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    return lib().amk_decode_step_noalloc(ctypes.byref(cfg), ctypes.byref(w), B, _ptr(tokens), _ptr(positions),
+                                         _ptr(kv_cache), _ptr(logits), s)

@@ -16,7 +16,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libamk.so")
 
-SOURCES = ["amk_kernel.cu", "amk_api.cpp", "amk_plan.cpp"]
+SOURCES = ["amk_kernel.cu", "amk_api.cpp", "amk_plan.cpp", "amk_noalloc.cu"]
 HEADERS = ["amk_internal.h", "amk_launch.h", "amk_plan_impl.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
