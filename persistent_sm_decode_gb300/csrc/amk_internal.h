@@ -110,23 +110,48 @@ struct Params {
     unsigned long long *trace; /* NULL, or [n_tasks][16] timings */
 };
 
-/* Batch-1 GEMV: a consumer warp keeps the activations of its K segment in
- * registers for a whole task; a segment holds at most this many elements. */
-constexpr int SEGMAX_BF16 = 2048;
-constexpr int SEGMAX_INT8 = 1024;
+/* Batch-1 GEMV.  A row of a task's K slice is cut into S segments; consumer
+ * warp w owns segment w % S and keeps that segment's activations in
+ * registers for the whole task: J 16-byte chunks per lane (chunk c of the
+ * segment sits in lane c % 32, slot c / 32).  Warps w / S = 0 .. 8/S - 1
+ * share out the rows of every tile.  S is the largest power of two up to 8
+ * that cuts K into whole chunks and still gives every lane a chunk; J is
+ * rounded up to a supported value (the loops are unrolled per J). */
+constexpr int JMAX_BF16 = 6;
+constexpr int JMAX_INT8 = 2;
 
-/* K segments per row for a GEMV task: batch 1 -> enough segments that each
- * fits in registers; larger batches read activations from shared memory and
- * use 8 / rows_per_stage segments when a tile has fewer than 8 rows. */
+/* K segments per row: batch 1 as above; larger batches read activations from
+ * shared memory and use 8 / rows_per_stage segments when a tile has fewer
+ * than 8 rows. */
 AMK_HD inline int gemv_segments(int batch_max, int Kc, bool int8, int rows_per_stage) {
     if (batch_max == 1) {
-        const int segmax = int8 ? SEGMAX_INT8 : SEGMAX_BF16;
-        int S = 1;
-        while (S < NCW && Kc > S * segmax) S *= 2;
-        return S;
+        const int epc = int8 ? 16 : 8;
+        int fallback = 1;
+        for (int S = NCW; S >= 1; S >>= 1) {
+            if (Kc % (S * epc) != 0) continue;
+            if (fallback == 1) fallback = S;
+            if (Kc / S >= 32 * epc) return S;
+        }
+        return fallback;
     }
     return rows_per_stage < NCW ? NCW / rows_per_stage : 1;
 }
+
+/* chunks per lane J of a batch-1 segment (0: the slice is too long) */
+AMK_HD inline int gemv_lane_chunks(int Kc, int S, bool int8) {
+    const int epc = int8 ? 16 : 8;
+    const int j = (Kc / S / epc + 31) / 32;
+    const int J = j <= 1 ? 1 : j <= 2 ? 2 : j <= 3 ? 3 : j <= 4 ? 4 : j <= 6 ? 6 : 0;
+    return J > (int8 ? JMAX_INT8 : JMAX_BF16) ? 0 : J;
+}
+
+/* Attention: positions per warp block; q heads per kv head rounded up to a
+ * power of two; chunk partials one merge thread can hold. */
+constexpr int ATT_BP = 16;
+constexpr int MRG_MAX_CPT = 2;
+AMK_HD inline int att_gp(int G) { return G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8; }
+/* most context chunks the merge supports: (threads / (d/4)) * MRG_MAX_CPT */
+AMK_HD inline int att_max_chunks(int d) { return (NCW * 32 / (d / 4)) * MRG_MAX_CPT; }
 
 /* shared-memory layout (bytes), common to host sizing and device carving */
 constexpr int SMEM_BARRIERS = 2 * MAX_SLOTS * 8;

@@ -118,14 +118,16 @@ __device__ __forceinline__ uint64_t ld_ll1(const uint64_t *p) {
 __device__ __forceinline__ uint32_t ll_flag(uint64_t w) { return (uint32_t)(w >> 32); }
 __device__ __forceinline__ float ll_f(uint64_t w) { return __uint_as_float((uint32_t)w); }
 
-/* consumer-warps-only barrier; returns the OR of `pred` over all consumers,
- * so that every consumer takes the same abort decision */
+/* Consumer-warps-only barrier; returns the OR of `pred` over all consumers,
+ * so that every consumer takes the same abort decision.  The non-.aligned
+ * forms count threads, not warps: a warp that arrives diverged (after
+ * per-lane waits) is still counted correctly. */
 __device__ __forceinline__ bool cbar_or(bool pred) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, %2, p;\n\t"
+        "barrier.red.or.pred q, 1, %2, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
         : "r"((uint32_t)pred), "n"(NCW * 32)
@@ -133,7 +135,7 @@ __device__ __forceinline__ bool cbar_or(bool pred) {
     return r != 0;
 }
 
-__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory"); }
+__device__ __forceinline__ void cbar() { asm volatile("barrier.sync 1, %0;" ::"n"(NCW * 32) : "memory"); }
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -212,6 +214,16 @@ __device__ bool wait_phase(const Params &p, Smem &s, uint64_t *bar, uint32_t par
             }
         }
     }
+}
+
+/* Warp-uniform gate of one ring stage: false (for every lane) if any lane has
+ * seen the abort flag or gave up waiting for the slot.  Lanes must agree:
+ * a tile ends in full-warp shuffles, and a lane that skipped it would leave
+ * the others waiting. */
+__device__ __forceinline__ bool stage_ready(const Params &p, Smem &s, uint64_t *bar, uint32_t parity, int task) {
+    bool ok = !__any_sync(0xffffffffu, s.misc->abort != 0);
+    if (ok) ok = wait_phase(p, s, bar, parity, 2, task);
+    return __all_sync(0xffffffffu, ok);
 }
 
 /* Which activation buffer a poll waits on (reported in the error word). */
@@ -414,14 +426,6 @@ __device__ void loader(const Params &p, Smem &s, int tbeg, int tend) {
 
 /* ----------------------------------------------------------- prologues */
 
-constexpr int MAXG = 4; /* float4 of x (and of the gain) per consumer thread kept in registers: H <= 4096 */
-
-/* batch 1 with the whole row in one K slice: x and the gain stay in registers */
-template <int NB>
-__device__ __forceinline__ bool norm_keeps_x(const Params &p, int k0, int k1) {
-    return NB == 1 && p.H / 4 <= MAXG * NCW * 32 && k0 == 0 && k1 == p.H;
-}
-
 /* four consecutive x values: the token's embedding row (layer 0) or epoch-
  * tagged residual words (waited for) */
 __device__ __forceinline__ float4 load_x4(const Params &p, Smem &s, const uint64_t *xs, const uint16_t *emb, int i4,
@@ -437,33 +441,22 @@ __device__ __forceinline__ float4 load_x4(const Params &p, Smem &s, const uint64
     return make_float4(ll_f(a.x), ll_f(a.y), ll_f(b.x), ll_f(b.y));
 }
 
-/* RMSNorm prologue: act[b][k - k0] = bf16(x[b][k] * r_b * gain[k]) for k in
- * [k0, k1), stored as fp32 (the bf16 value exactly).  r_b is computed once per
- * task (need_r) from the whole of x[b].  Reading x waits for its producers. */
-template <int NB>
+/* RMSNorm prologue into shared memory (batches above 1, or a K split):
+ * act[b][k - k0] = bf16(x[b][k] * r_b * gain[k]) for k in [k0, k1), stored as
+ * fp32 (the bf16 value exactly).  r_b is computed once per task (need_r) from
+ * the whole of x[b].  Reading x waits for its producers. */
 __device__ void norm_prologue(const Params &p, Smem &s, const uint64_t *xbase, bool from_embed, const uint16_t *gain,
-                              int k0, int k1, bool need_r, const uint2 *gpre, uint32_t f, int task, int which, int ctid,
-                              int warp, int lane) {
+                              int k0, int k1, bool need_r, uint32_t f, int task, int which, int ctid, int warp,
+                              int lane) {
     const int H = p.H, H4 = H / 4;
-    const bool keep = norm_keeps_x<NB>(p, k0, k1);
-    float4 xr[MAXG];
     if (need_r) {
         for (int b = 0; b < p.batch; ++b) {
             const uint64_t *xs = from_embed ? nullptr : xbase + (size_t)b * H;
             const uint16_t *emb = from_embed ? p.embed + (size_t)__ldg(p.tokens + b) * H : nullptr;
             float ss = 0.f;
-            if (keep) {
-#pragma unroll
-                for (int g = 0; g < MAXG; ++g) {
-                    const int i4 = ctid + g * NCW * 32;
-                    xr[g] = i4 < H4 ? load_x4(p, s, xs, emb, i4, f, task, which) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    ss += xr[g].x * xr[g].x + xr[g].y * xr[g].y + xr[g].z * xr[g].z + xr[g].w * xr[g].w;
-                }
-            } else {
-                for (int i4 = ctid; i4 < H4; i4 += NCW * 32) {
-                    float4 v = load_x4(p, s, xs, emb, i4, f, task, which);
-                    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-                }
+            for (int i4 = ctid; i4 < H4; i4 += NCW * 32) {
+                float4 v = load_x4(p, s, xs, emb, i4, f, task, which);
+                ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
             }
             ss = warp_sum(ss);
             if (lane == 0) s.misc->red[b][warp] = ss;
@@ -474,24 +467,6 @@ __device__ void norm_prologue(const Params &p, Smem &s, const uint64_t *xbase, b
 #pragma unroll
             for (int w = 0; w < NCW; ++w) ss += s.misc->red[ctid][w];
             s.misc->rnorm[ctid] = rsqrtf(ss / (float)H + p.eps);
-        }
-        if (keep) {
-            /* every thread derives r itself: no second barrier */
-            float ss = 0.f;
-#pragma unroll
-            for (int w = 0; w < NCW; ++w) ss += s.misc->red[0][w];
-            const float r = rsqrtf(ss / (float)H + p.eps);
-            float4 *dst = reinterpret_cast<float4 *>(s.act);
-#pragma unroll
-            for (int g = 0; g < MAXG; ++g) {
-                const int i4 = ctid + g * NCW * 32;
-                if (i4 < H4) {
-                    const uint2 gw = gpre[g];
-                    dst[i4] = make_float4(round_bf(xr[g].x * r * bf_lo(gw.x)), round_bf(xr[g].y * r * bf_hi(gw.x)),
-                                          round_bf(xr[g].z * r * bf_lo(gw.y)), round_bf(xr[g].w * r * bf_hi(gw.y)));
-                }
-            }
-            return;
         }
         cbar();
     }
@@ -566,62 +541,6 @@ __device__ __forceinline__ float dot_chunk(const uint4 &w, const float *h) {
     return s0 + s1;
 }
 
-/* Batch-1 tile with the activations in registers: warp w owns K segment
- * w % S (chunks [c0, c1)) and rows w / S, w / S + 8 / S, ...; hv holds this
- * lane's chunks c0 + lane + 32 j of the activation slice.  All of a row's
- * 16-byte shared loads are issued first, then the products go into eight
- * independent accumulators (short dependency chains). */
-template <bool I8>
-__device__ __forceinline__ void gemv_tile_b1(const uint8_t *tile, int nrows, int S, int Kc, const float4 (*hv)[I8 ? 4 : 2],
-                                             int c0, int c1, float *res, bool first, int warp, int lane) {
-    constexpr int EPC = I8 ? 16 : 8;
-    constexpr int MAXJ = (I8 ? SEGMAX_INT8 : SEGMAX_BF16) / (32 * EPC);
-    const int RG = NCW / S, seg = warp % S;
-    const size_t rowb = (size_t)Kc * (I8 ? 1 : 2);
-    for (int rr = warp / S; rr < nrows; rr += RG) {
-        const uint4 *w = reinterpret_cast<const uint4 *>(tile + rr * rowb);
-        uint4 wv[MAXJ];
-#pragma unroll
-        for (int j = 0; j < MAXJ; ++j) {
-            const int c = c0 + lane + 32 * j;
-            wv[j] = c < c1 ? w[c] : make_uint4(0u, 0u, 0u, 0u);
-        }
-        float a[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) a[e] = 0.f;
-#pragma unroll
-        for (int j = 0; j < MAXJ; ++j) {
-            if constexpr (I8) {
-                const uint32_t x[4] = {wv[j].x ^ 0x80808080u, wv[j].y ^ 0x80808080u, wv[j].z ^ 0x80808080u,
-                                       wv[j].w ^ 0x80808080u};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 h = hv[j][q];
-                    a[2 * q] = fmaf(i8_to_f(x[q], 0), h.x, a[2 * q]);
-                    a[2 * q + 1] = fmaf(i8_to_f(x[q], 1), h.y, a[2 * q + 1]);
-                    a[2 * q] = fmaf(i8_to_f(x[q], 2), h.z, a[2 * q]);
-                    a[2 * q + 1] = fmaf(i8_to_f(x[q], 3), h.w, a[2 * q + 1]);
-                }
-            } else {
-                const float4 x = hv[j][0], y = hv[j][1];
-                a[0] = fmaf(bf_lo(wv[j].x), x.x, a[0]);
-                a[1] = fmaf(bf_hi(wv[j].x), x.y, a[1]);
-                a[2] = fmaf(bf_lo(wv[j].y), x.z, a[2]);
-                a[3] = fmaf(bf_hi(wv[j].y), x.w, a[3]);
-                a[4] = fmaf(bf_lo(wv[j].z), y.x, a[4]);
-                a[5] = fmaf(bf_hi(wv[j].z), y.y, a[5]);
-                a[6] = fmaf(bf_lo(wv[j].w), y.z, a[6]);
-                a[7] = fmaf(bf_hi(wv[j].w), y.w, a[7]);
-            }
-        }
-        const float v = warp_sum(((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7])));
-        if (lane == 0) {
-            float *r = res + (size_t)rr * S + seg;
-            *r = first ? v : *r + v;
-        }
-    }
-}
-
 /* Batched tile: activations act[b][0..Kc) in shared memory.  With S > 1
  * segments per row warp w takes row w / S, K segment w % S; with S == 1 warp
  * w takes rows w, w + 8, ...  Partial sums go to res[(row * S + seg) * Bmax + b]
@@ -659,88 +578,237 @@ __device__ void gemv_tile(const uint8_t *tile, int nrows, int S, int Kc, const f
     }
 }
 
-/* residual value x[b][row] of a layer's input: the embedding row at layer 0 */
-__device__ __forceinline__ float x_in_value(const Params &p, Smem &s, int l, int b, int row, int task) {
-    if (l == 0) return bf2f(__ldg(p.embed + (size_t)__ldg(p.tokens + b) * p.H + row));
-    return ll_wait1(p, s, p.x_in + ((size_t)(l % p.depth) * p.Bmax + b) * p.H + row, ver(p, l), task, WB_XIN);
+/* ------------------------------------------- batch-1 GEMV, activations in registers */
+
+/* Sums of R values over the 32 lanes of a warp at once (R = 1, 2, 4, 8):
+ * each butterfly step halves the values a lane holds, sending one half to
+ * its partner.  Afterwards lane l holds the full sum of value l / (32 / R). */
+template <int N, int O, int R>
+__device__ __forceinline__ void xstep(float (&v)[R], int lane) {
+    const bool up = (lane & O) != 0;
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+        const float send = up ? v[i] : v[i + N / 2];
+        const float keep = up ? v[i + N / 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+    }
 }
 
-template <bool I8, int NB>
-__device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring &rg, const uint2 *gpre, int ctid,
-                          int warp, int lane) {
-    const GemvGeo g = gemv_geo(p, t);
-    const int NS = p.n_slots;
-    const int l = t.layer, slot = l % p.depth;
-    const int S = t.seg;
-    for (int kp = 0; kp < g.ks; ++kp) {
-        const int k0 = kp * g.Kc, k1 = k0 + g.Kc;
-        if (t.op == OP_QKV) {
-            const bool emb = l == 0;
-            norm_prologue<NB>(p, s, emb ? nullptr : p.x_in + (size_t)slot * p.Bmax * p.H, emb, p.layers[l].attn_norm, k0,
-                              k1, kp == 0, gpre, ver(p, l), ti, WB_XIN, ctid, warp, lane);
-        } else if (t.op == OP_GUP) {
-            norm_prologue<NB>(p, s, p.x_mid + (size_t)slot * p.Bmax * p.H, false, p.layers[l].mlp_norm, k0, k1, kp == 0,
-                              gpre, ver(p, l), ti, WB_XMID, ctid, warp, lane);
-        } else if (t.op == OP_LMH) {
-            norm_prologue<NB>(p, s, p.x_in + (size_t)(p.L % p.depth) * p.Bmax * p.H, false, p.final_norm, k0, k1,
-                              kp == 0, gpre, ver(p, p.L), ti, WB_XIN, ctid, warp, lane);
-        } else if (t.op == OP_OPR) {
-            copy_prologue(p, s, p.aout + (size_t)slot * p.Bmax * p.nq * p.d / 2, p.nq * p.d, k0, k1, ver(p, l), ti,
-                          WB_AOUT, ctid);
-        } else {
-            copy_prologue(p, s, p.act + (size_t)slot * p.Bmax * p.I / 2, p.I, k0, k1, ver(p, l), ti, WB_ACT, ctid);
-        }
-        if (cbar_or(s.misc->abort != 0)) return false;
-        if (p.trace && kp == 0 && ctid == 0) s.misc->t_pro = now_ns();
-        /* batch 1: this warp's K segment of the activations into registers */
-        constexpr int EPC = I8 ? 16 : 8;
-        constexpr int MAXJ = (I8 ? SEGMAX_INT8 : SEGMAX_BF16) / (32 * EPC);
-        float4 hv[NB == 1 ? MAXJ : 1][I8 ? 4 : 2];
-        const int nch = g.Kc / EPC, seg = warp % S;
-        const int c0 = seg * nch / S, c1 = (seg + 1) * nch / S;
-        if constexpr (NB == 1) {
-            const float4 *a4 = reinterpret_cast<const float4 *>(s.act);
+/* Sums of R values over groups of LP lanes at once (R = 1, 2, 4, 8; LP a
+ * power of two >= R): each butterfly step halves the values a lane holds,
+ * sending one half to its partner.  Afterwards lane l holds the full group
+ * sum of value (l % LP) / (LP / R). */
+template <int R, int LP>
+__device__ __forceinline__ float xsum_g(float (&v)[R], int lane) {
+    static_assert(R == 1 || R == 2 || R == 4 || R == 8, "xsum width");
+    static_assert(LP >= R && LP <= 32, "xsum group");
+    if constexpr (R >= 2) xstep<R, LP / 2>(v, lane);
+    if constexpr (R >= 4) xstep<R / 2, LP / 4>(v, lane);
+    if constexpr (R >= 8) xstep<R / 4, LP / 8>(v, lane);
+    float t = v[0];
 #pragma unroll
-            for (int j = 0; j < MAXJ; ++j) {
-                const int c = c0 + lane + 32 * j;
-#pragma unroll
-                for (int q = 0; q < EPC / 4; ++q)
-                    hv[j][q] = c < c1 ? a4[(size_t)c * (EPC / 4) + q] : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-        for (int rb = 0; rb < g.nrb; ++rb) {
-            const int ra = t.r0 + rb * g.R, re = min(t.r1, ra + g.R);
-            for (int m = 0; m < g.nmat; ++m, rg.advance(NS)) {
-                const int sl = rg.slot;
-                if (s.misc->abort) continue;
-                const unsigned long long tw0 = p.trace ? now_ns() : 0;
-                if (!wait_phase(p, s, &s.full[sl], rg.pass & 1u, 2, ti)) continue;
-                const unsigned long long tw1 = p.trace ? now_ns() : 0;
-                if (p.trace && kp == 0 && rb == 0 && m == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
-                float *res = s.res + ((size_t)m * g.nrows + (ra - t.r0)) * S * p.Bmax;
-                const uint8_t *tile = s.ring + (size_t)sl * p.slot_bytes;
-                if constexpr (NB == 1)
-                    gemv_tile_b1<I8>(tile, re - ra, S, g.Kc, hv, c0, c1, res, kp == 0, warp, lane);
-                else
-                    gemv_tile<I8, NB>(tile, re - ra, S, g.Kc, reinterpret_cast<const float *>(s.act), p.batch, res,
-                                      p.Bmax, kp == 0, warp, lane);
-                if (p.trace && warp == 0 && lane == 0) {
-                    s.misc->t_wait_full += tw1 - tw0;
-                    s.misc->t_tiles += now_ns() - tw1;
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s.empty[sl]);
-            }
-        }
-        if (cbar_or(s.misc->abort != 0)) return false;
-    }
+    for (int o = LP / (2 * R); o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    return t;
+}
 
-    /* epilogue: publish the task's rows as epoch-tagged words; a task marked
-     * TF_SKIP_SIGNAL publishes them with a stale epoch (timeout tests) */
+template <int R>
+__device__ __forceinline__ float xsum(float (&v)[R], int lane) {
+    return xsum_g<R, 32>(v, lane);
+}
+
+/* one 16-byte weight chunk (8 bf16 or 16 int8) against activations in registers */
+template <bool I8>
+__device__ __forceinline__ float dot_reg(const uint4 &w, const float4 (&h)[I8 ? 4 : 2]) {
+    float s0 = 0.f, s1 = 0.f;
+    if constexpr (I8) {
+        const uint32_t x[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            s0 = fmaf(i8_to_f(x[q], 0), h[q].x, s0);
+            s1 = fmaf(i8_to_f(x[q], 1), h[q].y, s1);
+            s0 = fmaf(i8_to_f(x[q], 2), h[q].z, s0);
+            s1 = fmaf(i8_to_f(x[q], 3), h[q].w, s1);
+        }
+    } else {
+        s0 = fmaf(bf_lo(w.x), h[0].x, s0);
+        s1 = fmaf(bf_hi(w.x), h[0].y, s1);
+        s0 = fmaf(bf_lo(w.y), h[0].z, s0);
+        s1 = fmaf(bf_hi(w.y), h[0].w, s1);
+        s0 = fmaf(bf_lo(w.z), h[1].x, s0);
+        s1 = fmaf(bf_hi(w.z), h[1].y, s1);
+        s0 = fmaf(bf_lo(w.w), h[1].z, s0);
+        s1 = fmaf(bf_hi(w.w), h[1].w, s1);
+    }
+    return s0 + s1;
+}
+
+/* rows handled together by one warp: at most 8 chunk loads in flight per lane */
+template <int J>
+struct RowsPerGroup {
+    static constexpr int value = J >= 6 ? 1 : J >= 3 ? 2 : J == 2 ? 4 : 8;
+};
+
+/* One ring tile of a batch-1 task.  This warp takes rows rgp, rgp + RG, ...
+ * of the tile, RPG of them at a time: every chunk load of the group is issued
+ * first, then each row's products are summed over the lane's chunks, and one
+ * transposing reduction gives all RPG row sums at once.  res[row * S + seg]
+ * receives the segment's partial sum. */
+template <bool I8, int J>
+__device__ __forceinline__ void gemv_stage_b1(const uint8_t *tile, int nrows, int RG, int rgp, int rowc, int cs,
+                                              int nch, const float4 (&hv)[J][I8 ? 4 : 2], float *res, int S, int seg,
+                                              int lane) {
+    constexpr int RPG = RowsPerGroup<J>::value;
+    const uint4 *W = reinterpret_cast<const uint4 *>(tile) + cs;
+    for (int r0 = rgp; r0 < nrows; r0 += RG * RPG) {
+        uint4 wv[RPG][J];
+#pragma unroll
+        for (int i = 0; i < RPG; ++i) {
+            const int rr = r0 + i * RG;
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const int c = lane + 32 * j;
+                wv[i][j] = (rr < nrows && c < nch) ? W[(size_t)rr * rowc + c] : make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        float v[RPG];
+#pragma unroll
+        for (int i = 0; i < RPG; ++i) {
+            float a = 0.f;
+#pragma unroll
+            for (int j = 0; j < J; ++j) a += dot_reg<I8>(wv[i][j], hv[j]);
+            v[i] = a;
+        }
+        const float y = xsum<RPG>(v, lane);
+        const int rr = r0 + (lane / (32 / RPG)) * RG;
+        if ((lane & (32 / RPG - 1)) == 0 && rr < nrows) res[(size_t)rr * S + seg] = y;
+    }
+}
+
+/* RMSNorm of sequence 0 straight into this warp's activation registers:
+ * hv[j] = bf16(x * r * gain) over chunk cs + lane + 32 j of the segment.  The
+ * warps that own distinct segments (warp < S) add up the sum of squares. */
+template <bool I8, int J>
+__device__ __forceinline__ void norm_regs(const Params &p, Smem &s, const uint64_t *xs, const uint16_t *emb,
+                                          const uint16_t *gain, int cs, int nch, int S, float4 (&hv)[J][I8 ? 4 : 2],
+                                          uint32_t f, int task, int which, int warp, int lane) {
+    constexpr int EPC = I8 ? 16 : 8, Q = EPC / 4;
+    uint2 gw[J][Q];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int c = lane + 32 * j;
+#pragma unroll
+        for (int q = 0; q < Q; ++q)
+            gw[j][q] = c < nch ? __ldg(reinterpret_cast<const uint2 *>(gain) + (size_t)(cs + c) * Q + q) : make_uint2(0u, 0u);
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int c = lane + 32 * j;
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            hv[j][q] = c < nch ? load_x4(p, s, xs, emb, (cs + c) * Q + q, f, task, which) : make_float4(0.f, 0.f, 0.f, 0.f);
+            ss += hv[j][q].x * hv[j][q].x + hv[j][q].y * hv[j][q].y + hv[j][q].z * hv[j][q].z + hv[j][q].w * hv[j][q].w;
+        }
+    }
+    __syncwarp();
+    ss = warp_sum(ss);
+    if (lane == 0 && warp < S) s.misc->red[0][warp] = ss;
+    cbar();
+    float tot = 0.f;
+    for (int w = 0; w < S; ++w) tot += s.misc->red[0][w];
+    const float r = rsqrtf(tot / (float)p.H + p.eps);
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            const float4 x = hv[j][q];
+            const uint2 g = gw[j][q];
+            hv[j][q] = make_float4(round_bf(x.x * r * bf_lo(g.x)), round_bf(x.y * r * bf_hi(g.x)),
+                                   round_bf(x.z * r * bf_lo(g.y)), round_bf(x.w * r * bf_hi(g.y)));
+        }
+}
+
+/* bf16 activations (two per epoch-tagged word) of sequence 0 into this warp's
+ * registers: every load is issued before the first wait */
+template <bool I8, int J>
+__device__ __forceinline__ void copy_regs(const Params &p, Smem &s, const uint64_t *src, int cs, int nch,
+                                          float4 (&hv)[J][I8 ? 4 : 2], uint32_t f, int task, int which, int lane) {
+    constexpr int EPC = I8 ? 16 : 8, Q = EPC / 4;
+    ulonglong2 w[J][Q];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int c = lane + 32 * j;
+#pragma unroll
+        for (int q = 0; q < Q; ++q)
+            w[j][q] = c < nch ? ld_ll2(src + ((size_t)(cs + c) * EPC + 4 * q) / 2) : ulonglong2{0ull, 0ull};
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int c = lane + 32 * j;
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            if (c < nch) {
+                ulonglong2 v = w[j][q];
+                if (!ll_ok(f, v)) ll_settle(p, s, src + ((size_t)(cs + c) * EPC + 4 * q) / 2, v, f, task, which);
+                const uint32_t a = (uint32_t)v.x, b = (uint32_t)v.y;
+                hv[j][q] = make_float4(bf_lo(a), bf_hi(a), bf_lo(b), bf_hi(b));
+            } else {
+                hv[j][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    }
+    __syncwarp();
+}
+
+/* Residual inputs of a task's epilogue (O projection: x_in of the layer, or
+ * the embedding row at layer 0; down projection: x_mid), one per epilogue
+ * item, read at task start; their producers ran levels earlier, so the words
+ * are normally current and the epilogue does not wait on L2. */
+struct ResidPre {
+    uint64_t w[2];
+};
+
+__device__ __forceinline__ void resid_prefetch(const Params &p, const Task &t, int ctid, ResidPre &rp) {
+    rp.w[0] = rp.w[1] = 0ull;
+    if (t.op != OP_OPR && t.op != OP_DWN) return;
+    const int n = t.r1 - t.r0, B = p.batch, l = t.layer, slot = l % p.depth;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int i = ctid + k * NCW * 32;
+        if (i >= n * B) break;
+        const int row = t.r0 + i / B, b = i % B;
+        if (t.op == OP_OPR && l == 0)
+            rp.w[k] = (uint64_t)__float_as_uint(bf2f(__ldg(p.embed + (size_t)__ldg(p.tokens + b) * p.H + row))) |
+                      ((uint64_t)ver(p, 0) << 32);
+        else if (t.op == OP_OPR)
+            rp.w[k] = ld_ll1(p.x_in + ((size_t)slot * p.Bmax + b) * p.H + row);
+        else
+            rp.w[k] = ld_ll1(p.x_mid + ((size_t)slot * p.Bmax + b) * p.H + row);
+    }
+}
+
+/* the prefetched residual of epilogue item k, or a wait for it */
+__device__ __forceinline__ float resid_value(const Params &p, Smem &s, const Task &t, int ti, const ResidPre &rp, int k,
+                                             int b, int row) {
+    const int l = t.layer, slot = l % p.depth;
+    if (k < 2 && ll_flag(rp.w[k]) == ver(p, l)) return ll_f(rp.w[k]);
+    if (t.op == OP_OPR) {
+        if (l == 0) return bf2f(__ldg(p.embed + (size_t)__ldg(p.tokens + b) * p.H + row));
+        return ll_wait1(p, s, p.x_in + ((size_t)slot * p.Bmax + b) * p.H + row, ver(p, l), ti, WB_XIN);
+    }
+    return ll_wait1(p, s, p.x_mid + ((size_t)slot * p.Bmax + b) * p.H + row, ver(p, l), ti, WB_XMID);
+}
+
+/* Epilogue: publish the task's rows as epoch-tagged words (a task marked
+ * TF_SKIP_SIGNAL publishes them with a stale flag: timeout tests).  Partial
+ * sums of the S segments are added in a fixed order. */
+template <bool I8>
+__device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, int S, const ResidPre &rp, int ctid) {
     if (p.trace && ctid == 0) s.misc->t_stages = now_ns();
+    const int l = t.layer, slot = l % p.depth;
     const uint32_t stale = (t.flags & TF_SKIP_SIGNAL) ? (uint32_t)(p.L + 1) : 0u;
     const uint32_t ep = ver(p, l) - stale, ep_next = ver(p, l + 1) - stale;
-    const int n = g.nrows, B = p.batch;
+    const int n = t.r1 - t.r0, B = p.batch;
     auto y_of = [&](int m, int rr, int b) {
         float y = 0.f;
         for (int sg = 0; sg < S; ++sg) y += s.res[(((size_t)m * n + rr) * S + sg) * p.Bmax + b];
@@ -759,7 +827,8 @@ __device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring 
             st_ll(p.act + (((size_t)slot * p.Bmax + b) * p.I + t.r0 + rr) / 2, pack_bf2(a2[0], a2[1]), ep);
         }
     } else {
-        for (int i = ctid; i < n * B; i += NCW * 32) {
+        int k = 0;
+        for (int i = ctid; i < n * B; i += NCW * 32, ++k) {
             const int rr = i / B, b = i % B, row = t.r0 + rr;
             const float y0 = y_of(0, rr, b);
             switch (t.op) {
@@ -769,13 +838,12 @@ __device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring 
                 break;
             }
             case OP_OPR: {
-                const float xr = x_in_value(p, s, l, b, row, ti);
+                const float xr = resid_value(p, s, t, ti, rp, k, b, row);
                 st_ll(p.x_mid + ((size_t)slot * p.Bmax + b) * p.H + row, __float_as_uint(xr + y0), ep);
                 break;
             }
             case OP_DWN: {
-                const float xm =
-                    ll_wait1(p, s, p.x_mid + ((size_t)slot * p.Bmax + b) * p.H + row, ver(p, l), ti, WB_XMID);
+                const float xm = resid_value(p, s, t, ti, rp, k, b, row);
                 st_ll(p.x_in + ((size_t)((l + 1) % p.depth) * p.Bmax + b) * p.H + row, __float_as_uint(xm + y0),
                       ep_next);
                 break;
@@ -790,106 +858,242 @@ __device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring 
     return ok;
 }
 
+/* Batch-1 task without a K split: prologue into registers, tiles, epilogue. */
+template <bool I8, int J>
+__device__ bool gemv_task_b1(const Params &p, Smem &s, const Task &t, int ti, Ring &rg, const ResidPre &rp, int ctid,
+                             int warp, int lane) {
+    constexpr int EPC = I8 ? 16 : 8;
+    const GemvGeo g = gemv_geo(p, t);
+    const int NS = p.n_slots, l = t.layer, slot = l % p.depth;
+    const int S = t.seg, RG = NCW / S, seg = warp % S, rgp = warp / S;
+    const int nch = g.K / S / EPC, cs = seg * nch, rowc = g.K / EPC;
+    float4 hv[J][I8 ? 4 : 2];
+    if (t.op == OP_QKV) {
+        const bool emb = l == 0;
+        norm_regs<I8, J>(p, s, emb ? nullptr : p.x_in + (size_t)slot * p.Bmax * p.H,
+                         emb ? p.embed + (size_t)__ldg(p.tokens) * p.H : nullptr, p.layers[l].attn_norm, cs, nch, S,
+                         hv, ver(p, l), ti, WB_XIN, warp, lane);
+    } else if (t.op == OP_GUP) {
+        norm_regs<I8, J>(p, s, p.x_mid + (size_t)slot * p.Bmax * p.H, nullptr, p.layers[l].mlp_norm, cs, nch, S, hv,
+                         ver(p, l), ti, WB_XMID, warp, lane);
+    } else if (t.op == OP_LMH) {
+        norm_regs<I8, J>(p, s, p.x_in + (size_t)(p.L % p.depth) * p.Bmax * p.H, nullptr, p.final_norm, cs, nch, S, hv,
+                         ver(p, p.L), ti, WB_XIN, warp, lane);
+    } else if (t.op == OP_OPR) {
+        copy_regs<I8, J>(p, s, p.aout + (size_t)slot * p.Bmax * p.nq * p.d / 2, cs, nch, hv, ver(p, l), ti, WB_AOUT,
+                         lane);
+    } else {
+        copy_regs<I8, J>(p, s, p.act + (size_t)slot * p.Bmax * p.I / 2, cs, nch, hv, ver(p, l), ti, WB_ACT, lane);
+    }
+    if (p.trace && ctid == 0) s.misc->t_pro = now_ns();
+    for (int rb = 0; rb < g.nrb; ++rb) {
+        const int ra = t.r0 + rb * g.R, re = min(t.r1, ra + g.R);
+        for (int m = 0; m < g.nmat; ++m, rg.advance(NS)) {
+            const int sl = rg.slot;
+            const unsigned long long tw0 = p.trace ? now_ns() : 0;
+            if (!stage_ready(p, s, &s.full[sl], rg.pass & 1u, ti)) continue;
+            const unsigned long long tw1 = p.trace ? now_ns() : 0;
+            if (p.trace && rb == 0 && m == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
+            float *res = s.res + ((size_t)m * g.nrows + (ra - t.r0)) * S;
+            gemv_stage_b1<I8, J>(s.ring + (size_t)sl * p.slot_bytes, re - ra, RG, rgp, rowc, cs, nch, hv, res, S, seg,
+                                 lane);
+            if (p.trace && warp == 0 && lane == 0) {
+                s.misc->t_wait_full += tw1 - tw0;
+                s.misc->t_tiles += now_ns() - tw1;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.empty[sl]);
+        }
+    }
+    if (cbar_or(s.misc->abort != 0)) return false;
+    return gemv_epilogue<I8>(p, s, t, ti, S, rp, ctid);
+}
+
+template <bool I8, int NB>
+__device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring &rg, const ResidPre &rp, int ctid,
+                          int warp, int lane) {
+    const GemvGeo g = gemv_geo(p, t);
+    if constexpr (NB == 1) {
+        if (g.ks == 1) {
+            const int J = gemv_lane_chunks(g.K, t.seg, I8);
+            if (J == 1) return gemv_task_b1<I8, 1>(p, s, t, ti, rg, rp, ctid, warp, lane);
+            if (J == 2) return gemv_task_b1<I8, 2>(p, s, t, ti, rg, rp, ctid, warp, lane);
+            if constexpr (!I8) {
+                if (J == 3) return gemv_task_b1<I8, 3>(p, s, t, ti, rg, rp, ctid, warp, lane);
+                if (J == 4) return gemv_task_b1<I8, 4>(p, s, t, ti, rg, rp, ctid, warp, lane);
+                if (J == 6) return gemv_task_b1<I8, 6>(p, s, t, ti, rg, rp, ctid, warp, lane);
+            }
+            return false;
+        }
+    }
+    /* activations of the K slice in shared memory */
+    const int NS = p.n_slots;
+    const int l = t.layer, slot = l % p.depth;
+    const int S = t.seg;
+    for (int kp = 0; kp < g.ks; ++kp) {
+        const int k0 = kp * g.Kc, k1 = k0 + g.Kc;
+        if (t.op == OP_QKV) {
+            const bool emb = l == 0;
+            norm_prologue(p, s, emb ? nullptr : p.x_in + (size_t)slot * p.Bmax * p.H, emb, p.layers[l].attn_norm, k0, k1,
+                          kp == 0, ver(p, l), ti, WB_XIN, ctid, warp, lane);
+        } else if (t.op == OP_GUP) {
+            norm_prologue(p, s, p.x_mid + (size_t)slot * p.Bmax * p.H, false, p.layers[l].mlp_norm, k0, k1, kp == 0,
+                          ver(p, l), ti, WB_XMID, ctid, warp, lane);
+        } else if (t.op == OP_LMH) {
+            norm_prologue(p, s, p.x_in + (size_t)(p.L % p.depth) * p.Bmax * p.H, false, p.final_norm, k0, k1, kp == 0,
+                          ver(p, p.L), ti, WB_XIN, ctid, warp, lane);
+        } else if (t.op == OP_OPR) {
+            copy_prologue(p, s, p.aout + (size_t)slot * p.Bmax * p.nq * p.d / 2, p.nq * p.d, k0, k1, ver(p, l), ti,
+                          WB_AOUT, ctid);
+        } else {
+            copy_prologue(p, s, p.act + (size_t)slot * p.Bmax * p.I / 2, p.I, k0, k1, ver(p, l), ti, WB_ACT, ctid);
+        }
+        if (cbar_or(s.misc->abort != 0)) return false;
+        if (p.trace && kp == 0 && ctid == 0) s.misc->t_pro = now_ns();
+        for (int rb = 0; rb < g.nrb; ++rb) {
+            const int ra = t.r0 + rb * g.R, re = min(t.r1, ra + g.R);
+            for (int m = 0; m < g.nmat; ++m, rg.advance(NS)) {
+                const int sl = rg.slot;
+                const unsigned long long tw0 = p.trace ? now_ns() : 0;
+                if (!stage_ready(p, s, &s.full[sl], rg.pass & 1u, ti)) continue;
+                const unsigned long long tw1 = p.trace ? now_ns() : 0;
+                if (p.trace && kp == 0 && rb == 0 && m == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
+                float *res = s.res + ((size_t)m * g.nrows + (ra - t.r0)) * S * p.Bmax;
+                gemv_tile<I8, NB>(s.ring + (size_t)sl * p.slot_bytes, re - ra, S, g.Kc,
+                                  reinterpret_cast<const float *>(s.act), p.batch, res, p.Bmax, kp == 0, warp, lane);
+                if (p.trace && warp == 0 && lane == 0) {
+                    s.misc->t_wait_full += tw1 - tw0;
+                    s.misc->t_tiles += now_ns() - tw1;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.empty[sl]);
+            }
+        }
+        if (cbar_or(s.misc->abort != 0)) return false;
+    }
+    return gemv_epilogue<I8>(p, s, t, ti, S, rp, ctid);
+}
+
 /* ----------------------------------------------------------- attention */
 
+/* Shared memory of an attention task, carved from the activation region. */
 struct AttSmem {
-    float *q;        /* [G][d], pre-scaled by log2(e)/sqrt(d) */
+    float *q;        /* [GP][d]: rotated q of the group's heads, pre-scaled by log2(e)/sqrt(d) */
     uint16_t *knew;  /* [d] bf16(rope(k)) of position p */
     uint16_t *vnew;  /* [d] */
-    float *wst;      /* [NCW][d + PART_PAD]: per-warp (o, m, l) */
-    float *sbuf;     /* [NCW][32]: per-warp scores, then probabilities, of a block */
+    float *wst;      /* [NCW][GP][d + PART_PAD]: per-warp (o, m, l) of each head */
+    float *sbuf;     /* [NCW][ATT_BP][GP]: per-warp scores, then probabilities, of a block */
 };
 
-__device__ __forceinline__ AttSmem att_smem(const Params &p, Smem &s) {
+__device__ __forceinline__ AttSmem att_smem(const Params &p, Smem &s, int GP) {
     AttSmem a;
     uint8_t *base = s.act;
     a.q = reinterpret_cast<float *>(base);
-    base += align_up(p.G * p.d * 4, 16);
+    base += align_up(GP * p.d * 4, 16);
     a.knew = reinterpret_cast<uint16_t *>(base);
     a.vnew = a.knew + p.d;
     base += align_up(2 * p.d * 2, 16);
     a.wst = reinterpret_cast<float *>(base);
-    a.sbuf = a.wst + NCW * (p.d + PART_PAD);
+    a.sbuf = a.wst + NCW * GP * (p.d + PART_PAD);
     return a;
 }
 
-/* Online-softmax state of one warp, which owns one head and a subset of the
- * positions.  LP = d / 8 lanes share a position when scoring (8 elements
- * each); for the P.V product every lane owns d / 32 output elements. */
-template <int LP>
+/* Online-softmax state of one warp over all GP (= G rounded up to a power of
+ * two) heads of a kv group.  Scoring: LP = d / 4 lanes share a position,
+ * each holding four elements of K and the matching four q values of every
+ * head.  P.V: every lane owns EL = d / 32 output elements of every head.  m
+ * and l belong to head lane % GP (replicated over its lanes). */
+template <int LP, int GP>
 struct AttState {
-    float q[8];
-    float o[LP / 4];
-    float m;  /* running max, warp-uniform (log2 units) */
-    float l;  /* this lane's share of the running sum */
+    float q[GP][4];
+    float o[GP][LP / 8];
+    float m, l;
 };
 
-/* positions j0 .. j0 + nb - 1 (nb <= 32) of a K/V tile in shared memory */
-template <int LP>
-__device__ __forceinline__ void att_block(AttState<LP> &st, const uint16_t *Kt, const uint16_t *Vt, int j0, int nb,
-                                          int d, float *sb, int lane) {
-    constexpr int PW = 32 / LP, EL = LP / 4;
-    const int pg = lane / LP, ch = lane % LP;
-#pragma unroll
-    for (int it = 0; it < LP; ++it) {
+/* positions j0 .. j0 + nb - 1 (nb <= ATT_BP) of a K/V tile in shared memory */
+template <int LP, int GP>
+__device__ __forceinline__ void att_block(AttState<LP, GP> &st, const uint16_t *Kt, const uint16_t *Vt, int j0,
+                                          int nb, int d, float *sb, int lane) {
+    constexpr int PW = 32 / LP, EL = LP / 8, LPH = 32 / GP;
+    const int pg = lane / LP, ch = lane % LP, li = lane % LP;
+    /* scores of every head for PW positions at a time */
+#pragma unroll 2
+    for (int it = 0; it < ATT_BP / PW; ++it) {
         const int jj = it * PW + pg;
-        float sc = -INFINITY;
+        float sc[GP];
         if (jj < nb) {
-            const uint4 kv = reinterpret_cast<const uint4 *>(Kt + (size_t)(j0 + jj) * d)[ch];
-            const float s0 = st.q[0] * bf_lo(kv.x) + st.q[1] * bf_hi(kv.x) + st.q[2] * bf_lo(kv.y) + st.q[3] * bf_hi(kv.y);
-            const float s1 = st.q[4] * bf_lo(kv.z) + st.q[5] * bf_hi(kv.z) + st.q[6] * bf_lo(kv.w) + st.q[7] * bf_hi(kv.w);
-            sc = s0 + s1;
-        }
+            const uint2 kv = reinterpret_cast<const uint2 *>(Kt + (size_t)(j0 + jj) * d)[ch];
+            const float k0 = bf_lo(kv.x), k1 = bf_hi(kv.x), k2 = bf_lo(kv.y), k3 = bf_hi(kv.y);
 #pragma unroll
-        for (int o = LP / 2; o > 0; o >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o);
-        if (ch == 0) sb[jj] = sc;
+            for (int h = 0; h < GP; ++h)
+                sc[h] = fmaf(st.q[h][0], k0, st.q[h][1] * k1) + fmaf(st.q[h][2], k2, st.q[h][3] * k3);
+        } else {
+#pragma unroll
+            for (int h = 0; h < GP; ++h) sc[h] = 0.f;
+        }
+        const float t = xsum_g<GP, LP>(sc, lane);
+        if (li % (LP / GP) == 0 && jj < nb) sb[jj * GP + li / (LP / GP)] = t;
     }
     __syncwarp();
-    const float si = sb[lane];
-    float mb = si;
+    /* online softmax, head lane % GP over positions lane / GP + LPH k */
+    const int hh = lane % GP, k0 = lane / GP;
+    float mb = -INFINITY;
+    for (int jj = k0; jj < nb; jj += LPH) mb = fmaxf(mb, sb[jj * GP + hh]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+    for (int o = GP; o < 32; o <<= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
     const float mnew = fmaxf(st.m, mb);
     const float alpha = exp2f(st.m - mnew);
-    const float pi = lane < nb ? exp2f(si - mnew) : 0.f;
-    st.l = st.l * alpha + pi;
+    float ps = 0.f;
+    for (int jj = k0; jj < nb; jj += LPH) {
+        const float pv = exp2f(sb[jj * GP + hh] - mnew);
+        sb[jj * GP + hh] = pv;
+        ps += pv;
+    }
+#pragma unroll
+    for (int o = GP; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+    st.l = st.l * alpha + ps;
     st.m = mnew;
 #pragma unroll
-    for (int e = 0; e < EL; ++e) st.o[e] *= alpha;
+    for (int h = 0; h < GP; ++h) {
+        const float ah = __shfl_sync(0xffffffffu, alpha, h);
+#pragma unroll
+        for (int e = 0; e < EL; ++e) st.o[h][e] *= ah;
+    }
     __syncwarp();
-    sb[lane] = pi;
-    __syncwarp();
+    /* P.V */
     const uint16_t *vcol = Vt + (size_t)j0 * d + lane * EL;
     for (int i = 0; i < nb; ++i) {
-        const float w = sb[i];
+        float v[EL];
         if constexpr (EL == 2) {
-            const uint32_t v = *reinterpret_cast<const uint32_t *>(vcol + (size_t)i * d);
-            st.o[0] = fmaf(w, bf_lo(v), st.o[0]);
-            st.o[1] = fmaf(w, bf_hi(v), st.o[1]);
+            const uint32_t w = *reinterpret_cast<const uint32_t *>(vcol + (size_t)i * d);
+            v[0] = bf_lo(w);
+            v[1] = bf_hi(w);
         } else {
-            const uint2 v = *reinterpret_cast<const uint2 *>(vcol + (size_t)i * d);
-            st.o[0] = fmaf(w, bf_lo(v.x), st.o[0]);
-            st.o[1] = fmaf(w, bf_hi(v.x), st.o[1]);
-            st.o[2] = fmaf(w, bf_lo(v.y), st.o[2]);
-            st.o[3] = fmaf(w, bf_hi(v.y), st.o[3]);
+            const uint2 w = *reinterpret_cast<const uint2 *>(vcol + (size_t)i * d);
+            v[0] = bf_lo(w.x);
+            v[1] = bf_hi(w.x);
+            v[2] = bf_lo(w.y);
+            v[3] = bf_hi(w.y);
+        }
+        const float *pr = sb + i * GP;
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+            const float ph = pr[h];
+#pragma unroll
+            for (int e = 0; e < EL; ++e) st.o[h][e] = fmaf(ph, v[e], st.o[h][e]);
         }
     }
     __syncwarp();
 }
 
-template <int LP>
-__device__ __forceinline__ void att_tile(AttState<LP> &st, const uint16_t *Kt, const uint16_t *Vt, int nt, int d,
-                                         int sub, int wph, float *sb, int lane) {
-    for (int j0 = sub * 32; j0 < nt; j0 += wph * 32) att_block<LP>(st, Kt, Vt, j0, min(32, nt - j0), d, sb, lane);
-}
-
-template <int LP>
+template <int LP, int GP>
 __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, Ring &rg, int ctid, int warp, int lane) {
+    constexpr int EL = LP / 8;
     const int d = p.d, G = p.G, NS = p.n_slots;
     const int l = t.layer, slot = l % p.depth, b = t.b, grp = t.g;
     const AttGeo ag = att_geo(p, t);
     const bool active_seq = b < p.batch;
-    AttSmem as = att_smem(p, s);
+    AttSmem as = att_smem(p, s, GP);
 
     /* prologue: wait for q, k, v of this kv head, rotate q and the new k,
      * round k and v to bf16 */
@@ -928,32 +1132,34 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
         }
     }
 
-    const int wph = NCW / G;
-    const bool wactive = warp < wph * G;
-    const int h = warp % G, sub = warp / G;
-    const int ch = lane % LP;
-    constexpr int EL = LP / 4;
-    float *sb = as.sbuf + warp * 32;
-    AttState<LP> st;
+    AttState<LP, GP> st;
     st.m = -INFINITY;
     st.l = 0.f;
+    {
+        const int ch = lane % LP;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) st.q[e] = wactive ? as.q[h * d + ch * 8 + e] : 0.f;
+        for (int h = 0; h < GP; ++h)
 #pragma unroll
-    for (int e = 0; e < EL; ++e) st.o[e] = 0.f;
+            for (int e = 0; e < 4; ++e) st.q[h][e] = h < G ? as.q[h * d + ch * 4 + e] : 0.f;
+#pragma unroll
+        for (int h = 0; h < GP; ++h)
+#pragma unroll
+            for (int e = 0; e < EL; ++e) st.o[h][e] = 0.f;
+    }
+    float *sb = as.sbuf + warp * ATT_BP * GP;
 
     for (int k = 0; k < ag.ntile; ++k, rg.advance(NS)) {
         const int sl = rg.slot;
-        if (s.misc->abort) continue;
         const unsigned long long tw0 = p.trace ? now_ns() : 0;
-        if (!wait_phase(p, s, &s.full[sl], rg.pass & 1u, 2, ti)) continue;
+        if (!stage_ready(p, s, &s.full[sl], rg.pass & 1u, ti)) continue;
         const unsigned long long tw1 = p.trace ? now_ns() : 0;
         if (p.trace && k == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
         const int t0 = ag.s0 + k * t.rows_per_stage;
         const int nt = min(ag.e, t0 + (int)t.rows_per_stage) - t0;
         const uint16_t *Kt = reinterpret_cast<const uint16_t *>(s.ring + (size_t)sl * p.slot_bytes);
         const uint16_t *Vt = Kt + (size_t)t.rows_per_stage * d;
-        if (wactive) att_tile<LP>(st, Kt, Vt, nt, d, sub, wph, sb, lane);
+        for (int j0 = warp * ATT_BP; j0 < nt; j0 += NCW * ATT_BP)
+            att_block<LP, GP>(st, Kt, Vt, j0, min(ATT_BP, nt - j0), d, sb, lane);
         if (p.trace && warp == 0 && lane == 0) {
             s.misc->t_wait_full += tw1 - tw0;
             s.misc->t_tiles += now_ns() - tw1;
@@ -961,99 +1167,140 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.empty[sl]);
     }
-    if (active_seq && (t.flags & TF_NEW_TOKEN) && wactive) att_tile<LP>(st, as.knew, as.vnew, 1, d, sub, wph, sb, lane);
+    /* the new position, from shared memory, on the last warp */
+    if (active_seq && (t.flags & TF_NEW_TOKEN) && warp == NCW - 1) att_block<LP, GP>(st, as.knew, as.vnew, 0, 1, d, sb, lane);
 
-    /* the warp's state: l summed over lanes, o spread EL elements per lane */
-    st.l = warp_sum(st.l);
-    if (wactive) {
-        float *w = as.wst + (size_t)warp * (d + PART_PAD);
+    /* the warp's state: o of every head, m and l of head lane (lane < GP) */
+    {
+        float *w = as.wst + (size_t)warp * GP * (d + PART_PAD);
 #pragma unroll
-        for (int e = 0; e < EL; ++e) w[lane * EL + e] = st.o[e];
-        if (lane == 0) {
-            w[d] = st.m;
-            w[d + 1] = st.l;
+        for (int h = 0; h < GP; ++h)
+#pragma unroll
+            for (int e = 0; e < EL; ++e) w[(size_t)h * (d + PART_PAD) + lane * EL + e] = st.o[h][e];
+        if (lane < GP) {
+            w[(size_t)lane * (d + PART_PAD) + d] = st.m;
+            w[(size_t)lane * (d + PART_PAD) + d + 1] = st.l;
         }
     }
     if (cbar_or(s.misc->abort != 0)) return false;
 
-    /* merge the warps of each head; publish the chunk's partial (o unnormalised, m, l) */
+    /* merge the warps of each head; publish the chunk's partial (o unnormalised, m, l),
+     * head-major: part[b][kv head][head][chunk] */
     if (active_seq) {
         const uint32_t ep = ver(p, l) - ((t.flags & TF_SKIP_SIGNAL) ? (uint32_t)(p.L + 1) : 0u);
-        uint64_t *part = p.part + ((((size_t)slot * p.Bmax + b) * p.nkv + grp) * p.C + t.r0) * G * (d + PART_PAD);
+        uint64_t *part = p.part + (((size_t)slot * p.Bmax + b) * p.nkv + grp) * G * p.C * (d + PART_PAD);
         for (int i = ctid; i < G * (d + 2); i += NCW * 32) {
             const int hh = i / (d + 2), e = i % (d + 2);
             float M = -INFINITY;
-            for (int w2 = 0; w2 < wph; ++w2) M = fmaxf(M, as.wst[(size_t)(w2 * G + hh) * (d + PART_PAD) + d]);
+            for (int w2 = 0; w2 < NCW; ++w2) M = fmaxf(M, as.wst[((size_t)w2 * GP + hh) * (d + PART_PAD) + d]);
             float v = 0.f;
             if (e == d) {
                 v = M;
             } else if (M != -INFINITY) {
-                for (int w2 = 0; w2 < wph; ++w2) {
-                    const float *w = as.wst + (size_t)(w2 * G + hh) * (d + PART_PAD);
+                for (int w2 = 0; w2 < NCW; ++w2) {
+                    const float *w = as.wst + ((size_t)w2 * GP + hh) * (d + PART_PAD);
                     const float mw = w[d];
                     if (mw == -INFINITY) continue;
                     v += exp2f(mw - M) * (e == d + 1 ? w[d + 1] : w[e]);
                 }
             }
-            st_ll(part + (size_t)hh * (d + PART_PAD) + e, __float_as_uint(v), ep);
+            st_ll(part + ((size_t)hh * p.C + t.r0) * (d + PART_PAD) + e, __float_as_uint(v), ep);
         }
     }
     return !cbar_or(s.misc->abort != 0);
 }
 
-/* Merge the C chunk partials of one (sequence, kv head) into bf16 attention
- * outputs of its G heads: o = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c
- * (the log-sum-exp combination of split softmax), in chunk order. */
+template <int LP>
+__device__ bool att_task(const Params &p, Smem &s, const Task &t, int ti, Ring &rg, int ctid, int warp, int lane) {
+    const int GP = att_gp(p.G);
+    if (GP == 1) return att_task_impl<LP, 1>(p, s, t, ti, rg, ctid, warp, lane);
+    if (GP == 2) return att_task_impl<LP, 2>(p, s, t, ti, rg, ctid, warp, lane);
+    if (GP == 4) return att_task_impl<LP, 4>(p, s, t, ti, rg, ctid, warp, lane);
+    return att_task_impl<LP, 8>(p, s, t, ti, rg, ctid, warp, lane);
+}
+
+/* Merge the C chunk partials of one query head of one sequence into its bf16
+ * attention output: o = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c (the
+ * log-sum-exp combination of split softmax).  Every partial word is loaded
+ * before the first wait; thread t takes four output elements (t % (d/4)) of
+ * the chunks c = t / (d/4) (mod NCL); the NCL sums of each element are added
+ * in a fixed order. */
 __device__ bool mrg_task(const Params &p, Smem &s, const Task &t, int ti, int ctid) {
-    const int d = p.d, G = p.G, C = t.r1, slot = t.layer % p.depth, b = t.b, grp = t.g;
+    const int d = p.d, G = p.G, C = t.r1, slot = t.layer % p.depth, b = t.b, h = t.g;
+    const int grp = h / G, hh = h % G;
+    const int Q4 = d / 4, NCL = NCW * 32 / Q4, e4 = ctid % Q4, cl = ctid / Q4;
+    constexpr int MAXCPT = MRG_MAX_CPT;
+    float *num = s.fac;                  /* [NCL][d] */
+    float *den = s.fac + NCL * d;        /* [NCL] */
+    float *mx = den + NCL;               /* [NCL] */
     if (b < p.batch) {
         const uint32_t f = ver(p, t.layer);
-        const uint32_t ep = f - ((t.flags & TF_SKIP_SIGNAL) ? (uint32_t)(p.L + 1) : 0u);
-        const uint64_t *base = p.part + (((size_t)slot * p.Bmax + b) * p.nkv + grp) * C * G * (d + PART_PAD);
-        float *ml = s.fac;         /* [G][C] m, then factors */
-        float *lv = s.fac + G * C; /* [G][C] l */
-        for (int i = ctid; i < G * C; i += NCW * 32) {
-            const int h = i / C, c = i % C;
-            const uint64_t *pc = base + ((size_t)c * G + h) * (d + PART_PAD) + d;
-            ulonglong2 v = ld_ll2(pc);
-            if (!ll_ok(f, v)) ll_settle(p, s, pc, v, f, ti, WB_PART);
-            ml[i] = ll_f(v.x);
-            lv[i] = ll_f(v.y);
-        }
-        if (cbar_or(s.misc->abort != 0)) return false;
-        if (ctid < G) {
-            float M = -INFINITY;
-            for (int c = 0; c < C; ++c) M = fmaxf(M, ml[ctid * C + c]);
-            float den = 0.f;
-            for (int c = 0; c < C; ++c) {
-                const float mc = ml[ctid * C + c];
-                const float f = mc == -INFINITY ? 0.f : exp2f(mc - M);
-                ml[ctid * C + c] = f;
-                den += f * lv[ctid * C + c];
+        const uint64_t *base = p.part + ((((size_t)slot * p.Bmax + b) * p.nkv + grp) * G + hh) * C * (d + PART_PAD);
+        ulonglong2 ml[MAXCPT], o0[MAXCPT], o1[MAXCPT];
+#pragma unroll
+        for (int k = 0; k < MAXCPT; ++k) {
+            const int c = cl + k * NCL;
+            if (c < C) {
+                const uint64_t *r = base + (size_t)c * (d + PART_PAD);
+                ml[k] = ld_ll2(r + d);
+                o0[k] = ld_ll2(r + 4 * e4);
+                o1[k] = ld_ll2(r + 4 * e4 + 2);
             }
-            const float inv = 1.f / den;
-            for (int c = 0; c < C; ++c) ml[ctid * C + c] *= inv;
         }
+        float mloc = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < MAXCPT; ++k) {
+            const int c = cl + k * NCL;
+            if (c < C) {
+                const uint64_t *r = base + (size_t)c * (d + PART_PAD);
+                ulonglong2 v = ml[k];
+                if (!ll_ok(f, v)) ll_settle(p, s, r + d, v, f, ti, WB_PART);
+                ml[k] = v;
+                v = o0[k];
+                if (!ll_ok(f, v)) ll_settle(p, s, r + 4 * e4, v, f, ti, WB_PART);
+                o0[k] = v;
+                v = o1[k];
+                if (!ll_ok(f, v)) ll_settle(p, s, r + 4 * e4 + 2, v, f, ti, WB_PART);
+                o1[k] = v;
+                mloc = fmaxf(mloc, ll_f(ml[k].x));
+            }
+        }
+        if (e4 == 0) mx[cl] = mloc;
         cbar();
-        uint64_t *out = p.aout + (((size_t)slot * p.Bmax + b) * p.nq * d + (size_t)grp * G * d) / 2;
-        const int q4 = d / 4;
-        for (int i = ctid; i < G * q4; i += NCW * 32) {
-            const int h = i / q4, e4 = i % q4;
-            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-            for (int c = 0; c < C; ++c) {
-                const float w = ml[h * C + c];
-                const uint64_t *src = base + ((size_t)c * G + h) * (d + PART_PAD) + 4 * e4;
-                ulonglong2 u = ld_ll2(src), v = ld_ll2(src + 2);
-                if (!ll_ok(f, u)) ll_settle(p, s, src, u, f, ti, WB_PART);
-                if (!ll_ok(f, v)) ll_settle(p, s, src + 2, v, f, ti, WB_PART);
-                o.x = fmaf(w, ll_f(u.x), o.x);
-                o.y = fmaf(w, ll_f(u.y), o.y);
-                o.z = fmaf(w, ll_f(v.x), o.z);
-                o.w = fmaf(w, ll_f(v.y), o.w);
+        float M = -INFINITY;
+        for (int i = 0; i < NCL; ++i) M = fmaxf(M, mx[i]);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f}, dl = 0.f;
+#pragma unroll
+        for (int k = 0; k < MAXCPT; ++k) {
+            const int c = cl + k * NCL;
+            if (c < C) {
+                const float mc = ll_f(ml[k].x);
+                const float w = mc == -INFINITY ? 0.f : exp2f(mc - M);
+                dl = fmaf(w, ll_f(ml[k].y), dl);
+                acc[0] = fmaf(w, ll_f(o0[k].x), acc[0]);
+                acc[1] = fmaf(w, ll_f(o0[k].y), acc[1]);
+                acc[2] = fmaf(w, ll_f(o1[k].x), acc[2]);
+                acc[3] = fmaf(w, ll_f(o1[k].y), acc[3]);
             }
-            st_ll(out + ((size_t)h * d + 4 * e4) / 2, pack_bf2(o.x, o.y), ep);
-            st_ll(out + ((size_t)h * d + 4 * e4) / 2 + 1, pack_bf2(o.z, o.w), ep);
+        }
+        *reinterpret_cast<float4 *>(num + (size_t)cl * d + 4 * e4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        if (e4 == 0) den[cl] = dl;
+        cbar();
+        if (ctid < Q4) {
+            float o[4] = {0.f, 0.f, 0.f, 0.f}, dd = 0.f;
+            for (int i = 0; i < NCL; ++i) {
+                const float4 v = *reinterpret_cast<const float4 *>(num + (size_t)i * d + 4 * ctid);
+                o[0] += v.x;
+                o[1] += v.y;
+                o[2] += v.z;
+                o[3] += v.w;
+                dd += den[i];
+            }
+            const float inv = 1.f / dd;
+            const uint32_t ep = f - ((t.flags & TF_SKIP_SIGNAL) ? (uint32_t)(p.L + 1) : 0u);
+            uint64_t *out = p.aout + (((size_t)slot * p.Bmax + b) * p.nq * d + (size_t)h * d + 4 * ctid) / 2;
+            st_ll(out, pack_bf2(o[0] * inv, o[1] * inv), ep);
+            st_ll(out + 1, pack_bf2(o[2] * inv, o[3] * inv), ep);
         }
     }
     return !cbar_or(s.misc->abort != 0);
@@ -1101,6 +1348,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p)
 
     if (warp == NCW) {
         if (lane == 0) loader(p, s, tbeg, tend);
+        __syncwarp();
     } else {
         const int ctid = tid;
         Ring rg{0, 0, 0};
@@ -1115,17 +1363,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p)
                     s.sc[i] = __ldg(op_scales(p, t, m) + t.r0 + rr);
                 }
             }
-            uint2 gpre[MAXG];
-            if (NB == 1 && (t.op == OP_QKV || t.op == OP_GUP || t.op == OP_LMH) && t.ksplit == 1) {
-                const uint16_t *gain = t.op == OP_QKV   ? p.layers[t.layer].attn_norm
-                                       : t.op == OP_GUP ? p.layers[t.layer].mlp_norm
-                                                        : p.final_norm;
-#pragma unroll
-                for (int g = 0; g < MAXG; ++g) {
-                    const int i4 = ctid + g * NCW * 32;
-                    gpre[g] = i4 < p.H / 4 ? __ldg(reinterpret_cast<const uint2 *>(gain) + i4) : make_uint2(0, 0);
-                }
-            }
+            ResidPre rp;
+            resid_prefetch(p, t, ctid, rp);
             unsigned long long *tr = p.trace ? p.trace + 16 * (size_t)ti : nullptr;
             if (tr && ctid == 0) {
                 tr[0] = tr[1] = now_ns();
@@ -1136,12 +1375,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p)
             }
             bool ok;
             if (t.op == OP_ATT)
-                ok = p.d == 64 ? att_task_impl<8>(p, s, t, ti, rg, ctid, warp, lane)
-                               : att_task_impl<16>(p, s, t, ti, rg, ctid, warp, lane);
+                ok = p.d == 64 ? att_task<16>(p, s, t, ti, rg, ctid, warp, lane)
+                               : att_task<32>(p, s, t, ti, rg, ctid, warp, lane);
             else if (t.op == OP_MRG)
                 ok = mrg_task(p, s, t, ti, ctid);
             else
-                ok = gemv_task<I8, NB>(p, s, t, ti, rg, gpre, ctid, warp, lane);
+                ok = gemv_task<I8, NB>(p, s, t, ti, rg, rp, ctid, warp, lane);
             if (!ok) break;
             if (tr && ctid == 0) {
                 tr[2] = s.misc->t_first;

@@ -51,6 +51,8 @@ constexpr double L2_SM_BPS = 1.5e11;   /* one CTA reading activations from L2 */
 constexpr double T_SYNC = 2.0e-6;      /* producer signal -> consumer sees it -> inputs loaded */
 constexpr double T_TASK = 0.3e-6;      /* per-task fixed cost (barriers, epilogue, signal) */
 constexpr double T_COPY = 0.33e-6;     /* one bulk copy through a CTA's ring (measured floor per slot) */
+constexpr double T_ATT_MAC = 8e-12;    /* attention: one (position, head, element) of scores plus P.V per CTA */
+constexpr double T_MERGE = 0.5e-6;     /* merge of one query head: barriers, factors, store */
 
 std::string fmt(const char *f, ...) __attribute__((format(printf, 1, 2)));
 std::string fmt(const char *f, ...) {
@@ -68,11 +70,54 @@ struct SmemModel {
     int act, result, scales, fac, fixed;
 };
 
+/* attention task: q of the group, the new k and v, per-warp (o, m, l) of every
+ * head, per-warp block scores */
 int att_smem_need(const Geo &g) {
-    return align_up(g.G * g.d * 4, 16) + align_up(2 * g.d * 2, 16) + NCW * (g.d + PART_PAD) * 4 + NCW * 32 * 4 + 256;
+    const int GP = att_gp(g.G);
+    return align_up(GP * g.d * 4, 16) + align_up(2 * g.d * 2, 16) + NCW * GP * (g.d + PART_PAD) * 4 +
+           NCW * ATT_BP * GP * 4 + 256;
+}
+
+/* merge task: per-lane-group sums of o and l, and chunk maxima */
+int mrg_smem_need(const Geo &g) {
+    const int ncl = NCW * 32 / (g.d / 4);
+    return ncl * (g.d + 2) * 4;
+}
+
+/* CTAs per QKV matrix: proportional to its rows (largest remainder), at least
+ * one each, so that no CTA's range straddles two matrices (n_sm >= 3) */
+std::vector<int> qkv_ctas(const Geo &g, int n_sm) {
+    const int64_t rows[3] = {(int64_t)g.nq * g.d, (int64_t)g.nkv * g.d, (int64_t)g.nkv * g.d};
+    const int64_t tot = rows[0] + rows[1] + rows[2];
+    std::vector<int> cnt(3);
+    std::vector<std::pair<int64_t, int>> rem;
+    int used = 0;
+    for (int m = 0; m < 3; ++m) {
+        cnt[m] = std::max<int>(1, (int)(rows[m] * n_sm / tot));
+        used += cnt[m];
+        rem.push_back({rows[m] * n_sm % tot, m});
+    }
+    std::sort(rem.begin(), rem.end(),
+              [](const std::pair<int64_t, int> &x, const std::pair<int64_t, int> &y) {
+                  return x.first > y.first || (x.first == y.first && x.second < y.second);
+              });
+    for (int i = 0; used < n_sm; i = (i + 1) % 3, ++used) cnt[rem[i].second]++;
+    while (used > n_sm) {
+        int m = (int)(std::max_element(cnt.begin(), cnt.end()) - cnt.begin());
+        cnt[m]--;
+        used--;
+    }
+    return cnt;
 }
 
 int max_task_rows(const Geo &g, int op, int n_sm) {
+    if (op == OP_QKV && n_sm >= 3) {
+        const std::vector<int> cnt = qkv_ctas(g, n_sm);
+        const int len[3] = {g.nq * g.d, g.nkv * g.d, g.nkv * g.d};
+        int r = 0;
+        for (int m = 0; m < 3; ++m) r = std::max(r, ceil_div(len[m], cnt[m]));
+        return std::min(r, MAX_TASK_ROWS);
+    }
     return std::min(ceil_div(g.rows(op), n_sm), MAX_TASK_ROWS);
 }
 
@@ -90,14 +135,16 @@ SmemModel smem_model(const Geo &g, int ks, int slot, int C, int n_sm) {
     m.act = att_smem_need(g);
     for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN, OP_LMH}) {
         int kc = g.K(op) / ksplit_for(g, op, ks);
-        m.act = std::max(m.act, g.B * kc * 4);
+        /* batch 1 without a K split keeps activations in registers */
+        if (g.B > 1 || ksplit_for(g, op, ks) > 1) m.act = std::max(m.act, g.B * kc * 4);
         int R = rows_per_slot(g, op, ks, slot);
         int S = gemv_segments(g.B, kc, g.web(op) == 1, R);
         int rows = max_task_rows(g, op, n_sm) + 1;  /* +1: a QKV matrix boundary can split a block */
         m.result = std::max(m.result, rows * g.nmat(op) * S * g.B * 4);
         if (g.scaled(op)) m.scales = std::max(m.scales, rows * g.nmat(op) * 4);
     }
-    m.fac = g.B * g.nq * C * 4;
+    (void)C;
+    m.fac = mrg_smem_need(g);
     m.act = align_up(m.act, 128);
     m.result = align_up(m.result, 128);
     m.scales = align_up(m.scales, 128);
@@ -126,14 +173,18 @@ double model_cost_us(const Geo &g, const Knobs &k, int n_sm) {
         t += g.L * (bytes / (per_sm * std::max(fill, 1e-3)) + stall(pro) + T_TASK * ks);
     }
     {
-        /* attention chunks, then the merge of each (sequence, kv head) */
+        /* attention chunks (K/V streamed, scores and P.V for every head of the
+         * group), then one merge per (sequence, query head) */
         int T = g.B * g.nkv * k.C;
-        double task_bytes = (double)g.Smax / k.C * g.d * 4;
         int per = ceil_div(T, n_sm), active = std::min(T, n_sm);
+        double pos = (double)g.Smax / k.C;
+        double task_bytes = pos * g.d * 4;
         double bw = std::min(std::min(SM_BPS_MAX, HBM_BPS / active), k.slot_bytes / T_COPY);
+        double compute = pos * g.d * att_gp(g.G) * T_ATT_MAC + std::ceil(pos / k.att_tile) * T_TASK;
         double pro = (double)(g.G + 2) * g.d * 4 / L2_SM_BPS;
-        double merge = (double)k.C * g.G * (g.d + PART_PAD) * 4 / L2_SM_BPS;
-        t += g.L * (per * task_bytes / bw + stall(pro) + T_TASK * per + T_SYNC + merge);
+        int per_m = ceil_div(g.B * g.nq, n_sm);
+        double merge = T_SYNC + per_m * (T_MERGE + (double)k.C * (g.d + 2) * 8 / L2_SM_BPS);
+        t += g.L * (per * std::max(task_bytes / bw, compute) + stall(pro) + T_TASK * per + merge);
     }
     {
         double bytes = (double)ceil_div(g.V, n_sm) * g.row_bytes(OP_LMH);
@@ -189,12 +240,28 @@ struct Builder {
      * most MAX_TASK_ROWS rows (and, for QKV, at matrix and signal-count limits). */
     void gemv_level(int op, int l) {
         int rows = g.rows(op);
-        int ks = ksplit_for(g, op, k.ksplit);
         /* gate/up tasks start on even rows: two SwiGLU outputs share a word */
         const int unit = op == OP_GUP ? 2 : 1;
-        for (int s = 0; s < n_sm; ++s) {
-            int a = unit * (int)((int64_t)s * (rows / unit) / n_sm);
-            int e = unit * (int)((int64_t)(s + 1) * (rows / unit) / n_sm);
+        if (op == OP_QKV && n_sm >= 3) {
+            const std::vector<int> cnt = qkv_ctas(g, n_sm);
+            const int lo[3] = {0, g.nq * g.d, (g.nq + g.nkv) * g.d};
+            const int len[3] = {g.nq * g.d, g.nkv * g.d, g.nkv * g.d};
+            int sm = 0;
+            for (int m = 0; m < 3; ++m)
+                for (int j = 0; j < cnt[m]; ++j, ++sm)
+                    gemv_range(op, l, sm, lo[m] + (int)((int64_t)j * len[m] / cnt[m]),
+                               lo[m] + (int)((int64_t)(j + 1) * len[m] / cnt[m]));
+            return;
+        }
+        for (int s = 0; s < n_sm; ++s)
+            gemv_range(op, l, s, unit * (int)((int64_t)s * (rows / unit) / n_sm),
+                       unit * (int)((int64_t)(s + 1) * (rows / unit) / n_sm));
+    }
+
+    /* tasks for rows [a, e) of `op` on CTA s */
+    void gemv_range(int op, int l, int s, int a, int e) {
+        int ks = ksplit_for(g, op, k.ksplit);
+        {
             while (a < e) {
                 int b = std::min(e, a + MAX_TASK_ROWS);
                 Task t = base(op, l);
@@ -275,23 +342,30 @@ struct Builder {
             ac.push_back(acc(BUF_QKV, false, l, b, b + 1, (int64_t)grp * g.G * g.d, (int64_t)(grp + 1) * g.G * g.d));
             ac.push_back(acc(BUF_QKV, false, l, b, b + 1, qd + (int64_t)grp * g.d, qd + (int64_t)(grp + 1) * g.d));
             ac.push_back(acc(BUF_QKV, false, l, b, b + 1, qd + kd + (int64_t)grp * g.d, qd + kd + (int64_t)(grp + 1) * g.d));
-            int64_t pr = ((int64_t)grp * k.C + c) * g.G;
-            ac.push_back(acc(BUF_PART, true, l, b, b + 1, pr, pr + g.G));
+            /* partials are head-major: [kv head][q head of the group][chunk] */
+            for (int hh = 0; hh < g.G; ++hh) {
+                int64_t e = ((int64_t)grp * g.G + hh) * k.C + c;
+                ac.push_back(acc(BUF_PART, true, l, b, b + 1, e, e + 1));
+            }
             if (x.flags & TF_NEW_TOKEN) ac.push_back(acc(BUF_KVNEW, true, l, b, b + 1, grp, grp + 1));
             add(sm, x, std::move(ac));
-            if (c == k.C - 1) {
-                /* the merge of this (sequence, kv head) follows its last chunk on the same CTA */
-                Task m = base(OP_MRG, l);
-                m.r1 = k.C;
-                m.b = (uint16_t)b;
-                m.g = (uint16_t)grp;
-                m.wait_id = (uint16_t)cid_chunk(l, b, grp);
-                m.sig[m.nsig++] = (uint16_t)cid_att(l);
-                std::vector<Access> am;
-                am.push_back(acc(BUF_PART, false, l, b, b + 1, (int64_t)grp * k.C * g.G, (int64_t)(grp + 1) * k.C * g.G));
-                am.push_back(acc(BUF_AOUT, true, l, b, b + 1, (int64_t)grp * g.G * g.d, (int64_t)(grp + 1) * g.G * g.d));
-                add(sm, m, std::move(am));
-            }
+        }
+        /* one merge per (sequence, query head), spread over the CTAs, after
+         * every attention task of the layer in each CTA's program order */
+        int M = g.B * g.nq;
+        for (int i = 0; i < M; ++i) {
+            int b = i / g.nq, h = i % g.nq, grp = h / g.G;
+            int sm = (int)((int64_t)i * n_sm / M);
+            Task m = base(OP_MRG, l);
+            m.r1 = k.C;
+            m.b = (uint16_t)b;
+            m.g = (uint16_t)h;
+            m.wait_id = (uint16_t)cid_chunk(l, b, grp);
+            m.sig[m.nsig++] = (uint16_t)cid_att(l);
+            std::vector<Access> am;
+            am.push_back(acc(BUF_PART, false, l, b, b + 1, (int64_t)h * k.C, (int64_t)(h + 1) * k.C));
+            am.push_back(acc(BUF_AOUT, true, l, b, b + 1, (int64_t)h * g.d, (int64_t)(h + 1) * g.d));
+            add(sm, m, std::move(am));
         }
     }
 
@@ -411,14 +485,18 @@ amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_c
     Knobs best;
     double best_cost = 1e300;
     int cands = 0;
-    int maxC = std::max(1, std::min(64, (4 * n_sm) / std::max(1, g.B * g.nkv)));
+    int maxC = std::max(1, std::min(att_max_chunks(g.d), (2 * n_sm) / std::max(1, g.B * g.nkv)));
     for (int ks : ks_choices) {
         if (o.ksplit && ks != o.ksplit) continue;
         for (int slot : slot_choices) {
             if (o.slot_bytes && slot != o.slot_bytes) continue;
             bool fits = true;
-            for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN, OP_LMH})
-                if ((int64_t)(g.K(op) / ksplit_for(g, op, ks)) * g.web(op) > slot) fits = false;
+            for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN, OP_LMH}) {
+                const int kc = g.K(op) / ksplit_for(g, op, ks);
+                if ((int64_t)kc * g.web(op) > slot) fits = false;
+                if (g.B == 1 && gemv_lane_chunks(kc, gemv_segments(1, kc, g.web(op) == 1, 1), g.web(op) == 1) == 0)
+                    fits = false;
+            }
             if (g.d * 4 > slot) fits = false;
             if (!fits) continue;
             for (int C = 1; C <= maxC; ++C) {
@@ -474,6 +552,19 @@ amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_c
     P->weight_bytes = wb;
     ScratchSizes ss = scratch_sizes(*P);
     P->scratch_bytes = 8 * (ss.x_in + ss.x_mid + ss.qkv + ss.part + ss.aout + ss.act);
+
+    /* every GEMV task's partial sums must fit the result buffer */
+    for (int sm_i = 0; sm_i < n_sm; ++sm_i)
+        for (const Task &t : P->sm_tasks[sm_i]) {
+            if (t.op == OP_ATT || t.op == OP_MRG) continue;
+            const int64_t need = (int64_t)(t.r1 - t.r0) * g.nmat(t.op) * t.seg * g.B * 4;
+            if (need > P->result_bytes) {
+                *msg = fmt("task rows %d exceed the result buffer (%lld > %d bytes)", t.r1 - t.r0, (long long)need,
+                           P->result_bytes);
+                amk_plan_destroy(P);
+                return AMK_ERR_SCHEDULE;
+            }
+        }
 
     /* ---- validate ---- */
     std::string why;

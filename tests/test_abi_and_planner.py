@@ -99,7 +99,7 @@ def _coverage(wl, plan, B):
             for r in range(n):
                 assert (op, l, r) in seen, "row not covered: %s layer %d row %d" % (op, l, r)
     assert len(att) == wl.n_layers * B * nkv * C
-    assert all(("MRG", l, b, g) in seen for l in range(wl.n_layers) for b in range(B) for g in range(nkv))
+    assert all(("MRG", l, b, h) in seen for l in range(wl.n_layers) for b in range(B) for h in range(nq))
 
 
 def test_rejects_bad_configs(amk):
@@ -185,11 +185,15 @@ def brute_force_unsafe(wl, plan, B, depth):
             for lo in (g * G * d, qd + g * d, qd + kd + g * d):
                 hi = lo + (G * d if lo == g * G * d else d)
                 acc.append((k, "qkv", l, 0, b, b + 1, lo, hi))
-            acc.append((k, "part", l, 1, b, b + 1, (g * C + c) * G, (g * C + c + 1) * G))
+            # partials are head-major: [kv head][q head of the group][chunk]
+            for hh in range(G):
+                e = (g * G + hh) * C + c
+                acc.append((k, "part", l, 1, b, b + 1, e, e + 1))
         elif op == "MRG":
-            b, g = t["b"], t["g"]
-            acc.append((k, "part", l, 0, b, b + 1, g * C * G, (g + 1) * C * G))
-            acc.append((k, "aout", l, 1, b, b + 1, g * G * d, (g + 1) * G * d))
+            # one merge per query head h of sequence b
+            b, h = t["b"], t["g"]
+            acc.append((k, "part", l, 0, b, b + 1, h * C, (h + 1) * C))
+            acc.append((k, "aout", l, 1, b, b + 1, h * d, (h + 1) * d))
         elif op == "OPR":
             acc.append((k, "aout", l, 0, 0, B, 0, nq * d))
             if l > 0:
