@@ -78,6 +78,7 @@ struct Params {
     const int32_t *task_start; /* [n_sm + 1] */
     int C, depth, slot_bytes, n_slots, att_tile;
     int act_bytes, result_bytes, scale_bytes, fac_bytes;
+    int work_bytes; /* the per-task region: GEMV sums + scales + activations, or attention state, or merge sums */
     int l2_prefetch_bytes;
     /* weights */
     const LayerPtrs *layers;

@@ -174,6 +174,7 @@ struct Misc {
 struct Smem {
     uint64_t *full, *empty;
     Misc *misc;
+    uint8_t *work;
     float *res;
     float *sc;
     float *fac;
@@ -616,28 +617,56 @@ __device__ __forceinline__ float xsum(float (&v)[R], int lane) {
     return xsum_g<R, 32>(v, lane);
 }
 
+/* Activations matching one 16-byte weight chunk, in registers: eight bf16
+ * values packed in pairs (element order of the weights) for bf16 weights,
+ * sixteen fp32 values for int8 weights. */
+template <bool I8>
+struct ActChunk {
+    uint32_t w[4];
+};
+template <>
+struct ActChunk<true> {
+    float4 v[4];
+};
+
+/* a += w * h over one pair of bf16 values (low or high halves): the
+ * mixed-precision FMA takes both operands as bf16, forms their product
+ * exactly in fp32 and rounds once, as fmaf on the widened values would */
+__device__ __forceinline__ void fma_bf16_lo(float &a, uint32_t w, uint32_t h) {
+    asm("{\n\t.reg .b16 w0, w1, h0, h1;\n\tmov.b32 {w0, w1}, %1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, w0, h0, %0;\n\t}"
+        : "+f"(a)
+        : "r"(w), "r"(h));
+}
+__device__ __forceinline__ void fma_bf16_hi(float &a, uint32_t w, uint32_t h) {
+    asm("{\n\t.reg .b16 w0, w1, h0, h1;\n\tmov.b32 {w0, w1}, %1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, w1, h1, %0;\n\t}"
+        : "+f"(a)
+        : "r"(w), "r"(h));
+}
+
 /* one 16-byte weight chunk (8 bf16 or 16 int8) against activations in registers */
 template <bool I8>
-__device__ __forceinline__ float dot_reg(const uint4 &w, const float4 (&h)[I8 ? 4 : 2]) {
+__device__ __forceinline__ float dot_reg(const uint4 &w, const ActChunk<I8> &h) {
     float s0 = 0.f, s1 = 0.f;
     if constexpr (I8) {
         const uint32_t x[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            s0 = fmaf(i8_to_f(x[q], 0), h[q].x, s0);
-            s1 = fmaf(i8_to_f(x[q], 1), h[q].y, s1);
-            s0 = fmaf(i8_to_f(x[q], 2), h[q].z, s0);
-            s1 = fmaf(i8_to_f(x[q], 3), h[q].w, s1);
+            s0 = fmaf(i8_to_f(x[q], 0), h.v[q].x, s0);
+            s1 = fmaf(i8_to_f(x[q], 1), h.v[q].y, s1);
+            s0 = fmaf(i8_to_f(x[q], 2), h.v[q].z, s0);
+            s1 = fmaf(i8_to_f(x[q], 3), h.v[q].w, s1);
         }
     } else {
-        s0 = fmaf(bf_lo(w.x), h[0].x, s0);
-        s1 = fmaf(bf_hi(w.x), h[0].y, s1);
-        s0 = fmaf(bf_lo(w.y), h[0].z, s0);
-        s1 = fmaf(bf_hi(w.y), h[0].w, s1);
-        s0 = fmaf(bf_lo(w.z), h[1].x, s0);
-        s1 = fmaf(bf_hi(w.z), h[1].y, s1);
-        s0 = fmaf(bf_lo(w.w), h[1].z, s0);
-        s1 = fmaf(bf_hi(w.w), h[1].w, s1);
+        fma_bf16_lo(s0, w.x, h.w[0]);
+        fma_bf16_hi(s1, w.x, h.w[0]);
+        fma_bf16_lo(s0, w.y, h.w[1]);
+        fma_bf16_hi(s1, w.y, h.w[1]);
+        fma_bf16_lo(s0, w.z, h.w[2]);
+        fma_bf16_hi(s1, w.z, h.w[2]);
+        fma_bf16_lo(s0, w.w, h.w[3]);
+        fma_bf16_hi(s1, w.w, h.w[3]);
     }
     return s0 + s1;
 }
@@ -655,7 +684,7 @@ struct RowsPerGroup {
  * receives the segment's partial sum. */
 template <bool I8, int J>
 __device__ __forceinline__ void gemv_stage_b1(const uint8_t *tile, int nrows, int RG, int rgp, int rowc, int cs,
-                                              int nch, const float4 (&hv)[J][I8 ? 4 : 2], float *res, int S, int seg,
+                                              int nch, const ActChunk<I8> (&hv)[J], float *res, int S, int seg,
                                               int lane) {
     constexpr int RPG = RowsPerGroup<J>::value;
     const uint4 *W = reinterpret_cast<const uint4 *>(tile) + cs;
@@ -689,10 +718,11 @@ __device__ __forceinline__ void gemv_stage_b1(const uint8_t *tile, int nrows, in
  * warps that own distinct segments (warp < S) add up the sum of squares. */
 template <bool I8, int J>
 __device__ __forceinline__ void norm_regs(const Params &p, Smem &s, const uint64_t *xs, const uint16_t *emb,
-                                          const uint16_t *gain, int cs, int nch, int S, float4 (&hv)[J][I8 ? 4 : 2],
+                                          const uint16_t *gain, int cs, int nch, int S, ActChunk<I8> (&hv)[J],
                                           uint32_t f, int task, int which, int warp, int lane) {
     constexpr int EPC = I8 ? 16 : 8, Q = EPC / 4;
     uint2 gw[J][Q];
+    float4 x[J][Q];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         const int c = lane + 32 * j;
@@ -706,8 +736,8 @@ __device__ __forceinline__ void norm_regs(const Params &p, Smem &s, const uint64
         const int c = lane + 32 * j;
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
-            hv[j][q] = c < nch ? load_x4(p, s, xs, emb, (cs + c) * Q + q, f, task, which) : make_float4(0.f, 0.f, 0.f, 0.f);
-            ss += hv[j][q].x * hv[j][q].x + hv[j][q].y * hv[j][q].y + hv[j][q].z * hv[j][q].z + hv[j][q].w * hv[j][q].w;
+            x[j][q] = c < nch ? load_x4(p, s, xs, emb, (cs + c) * Q + q, f, task, which) : make_float4(0.f, 0.f, 0.f, 0.f);
+            ss += x[j][q].x * x[j][q].x + x[j][q].y * x[j][q].y + x[j][q].z * x[j][q].z + x[j][q].w * x[j][q].w;
         }
     }
     __syncwarp();
@@ -721,10 +751,17 @@ __device__ __forceinline__ void norm_regs(const Params &p, Smem &s, const uint64
     for (int j = 0; j < J; ++j)
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
-            const float4 x = hv[j][q];
+            const float4 v = x[j][q];
             const uint2 g = gw[j][q];
-            hv[j][q] = make_float4(round_bf(x.x * r * bf_lo(g.x)), round_bf(x.y * r * bf_hi(g.x)),
-                                   round_bf(x.z * r * bf_lo(g.y)), round_bf(x.w * r * bf_hi(g.y)));
+            const float4 h = make_float4(round_bf(v.x * r * bf_lo(g.x)), round_bf(v.y * r * bf_hi(g.x)),
+                                         round_bf(v.z * r * bf_lo(g.y)), round_bf(v.w * r * bf_hi(g.y)));
+            if constexpr (I8) {
+                hv[j].v[q] = h;
+            } else {
+                /* the values are exactly bf16: keep their upper halves, two per word */
+                hv[j].w[2 * q] = (__float_as_uint(h.x) >> 16) | (__float_as_uint(h.y) & 0xffff0000u);
+                hv[j].w[2 * q + 1] = (__float_as_uint(h.z) >> 16) | (__float_as_uint(h.w) & 0xffff0000u);
+            }
         }
 }
 
@@ -732,7 +769,7 @@ __device__ __forceinline__ void norm_regs(const Params &p, Smem &s, const uint64
  * registers: every load is issued before the first wait */
 template <bool I8, int J>
 __device__ __forceinline__ void copy_regs(const Params &p, Smem &s, const uint64_t *src, int cs, int nch,
-                                          float4 (&hv)[J][I8 ? 4 : 2], uint32_t f, int task, int which, int lane) {
+                                          ActChunk<I8> (&hv)[J], uint32_t f, int task, int which, int lane) {
     constexpr int EPC = I8 ? 16 : 8, Q = EPC / 4;
     ulonglong2 w[J][Q];
 #pragma unroll
@@ -747,13 +784,18 @@ __device__ __forceinline__ void copy_regs(const Params &p, Smem &s, const uint64
         const int c = lane + 32 * j;
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
+            uint32_t a = 0u, b = 0u;
             if (c < nch) {
                 ulonglong2 v = w[j][q];
                 if (!ll_ok(f, v)) ll_settle(p, s, src + ((size_t)(cs + c) * EPC + 4 * q) / 2, v, f, task, which);
-                const uint32_t a = (uint32_t)v.x, b = (uint32_t)v.y;
-                hv[j][q] = make_float4(bf_lo(a), bf_hi(a), bf_lo(b), bf_hi(b));
+                a = (uint32_t)v.x;
+                b = (uint32_t)v.y;
+            }
+            if constexpr (I8) {
+                hv[j].v[q] = make_float4(bf_lo(a), bf_hi(a), bf_lo(b), bf_hi(b));
             } else {
-                hv[j][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                hv[j].w[2 * q] = a;
+                hv[j].w[2 * q + 1] = b;
             }
         }
     }
@@ -867,7 +909,7 @@ __device__ bool gemv_task_b1(const Params &p, Smem &s, const Task &t, int ti, Ri
     const int NS = p.n_slots, l = t.layer, slot = l % p.depth;
     const int S = t.seg, RG = NCW / S, seg = warp % S, rgp = warp / S;
     const int nch = g.K / S / EPC, cs = seg * nch, rowc = g.K / EPC;
-    float4 hv[J][I8 ? 4 : 2];
+    ActChunk<I8> hv[J];
     if (t.op == OP_QKV) {
         const bool emb = l == 0;
         norm_regs<I8, J>(p, s, emb ? nullptr : p.x_in + (size_t)slot * p.Bmax * p.H,
@@ -987,7 +1029,7 @@ struct AttSmem {
 
 __device__ __forceinline__ AttSmem att_smem(const Params &p, Smem &s, int GP) {
     AttSmem a;
-    uint8_t *base = s.act;
+    uint8_t *base = s.work;
     a.q = reinterpret_cast<float *>(base);
     base += align_up(GP * p.d * 4, 16);
     a.knew = reinterpret_cast<uint16_t *>(base);
@@ -1315,11 +1357,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p)
     s.full = reinterpret_cast<uint64_t *>(smem);
     s.empty = s.full + MAX_SLOTS;
     s.misc = reinterpret_cast<Misc *>(smem + SMEM_BARRIERS);
-    s.res = reinterpret_cast<float *>(smem + SMEM_BARRIERS + SMEM_MISC);
-    s.sc = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(s.res) + p.result_bytes);
-    s.fac = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(s.sc) + p.scale_bytes);
-    s.act = reinterpret_cast<uint8_t *>(s.fac) + p.fac_bytes;
-    s.ring = s.act + p.act_bytes;
+    /* one region per task: GEMV [sums | scales | activations], attention
+     * state, or merge sums (tasks of a CTA never overlap) */
+    s.work = smem + SMEM_BARRIERS + SMEM_MISC;
+    s.res = reinterpret_cast<float *>(s.work);
+    s.sc = reinterpret_cast<float *>(s.work + p.result_bytes);
+    s.act = s.work + p.result_bytes + p.scale_bytes;
+    s.fac = reinterpret_cast<float *>(s.work);
+    s.ring = s.work + p.work_bytes;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tbeg = p.task_start[blockIdx.x], tend = p.task_start[blockIdx.x + 1];

@@ -217,6 +217,7 @@ amk_status upload(DeviceState &ds, const amk_config *c, const amk_weights *w, in
     p.result_bytes = P.result_bytes;
     p.scale_bytes = P.scale_bytes;
     p.fac_bytes = P.fac_bytes;
+    p.work_bytes = P.work_bytes;
     p.l2_prefetch_bytes = P.k.l2_prefetch_kb > 0 ? P.k.l2_prefetch_kb * 1024 : 0;
     p.layers = (const LayerPtrs *)(ds.base + o_layers);
     p.embed = (const uint16_t *)w->embed;

@@ -53,6 +53,8 @@ constexpr double T_TASK = 0.3e-6;      /* per-task fixed cost (barriers, epilogu
 constexpr double T_COPY = 0.33e-6;     /* one bulk copy through a CTA's ring (measured floor per slot) */
 constexpr double T_ATT_MAC = 8e-12;    /* attention: one (position, head, element) of scores plus P.V per CTA */
 constexpr double T_MERGE = 0.5e-6;     /* merge of one query head: barriers, factors, store */
+constexpr double T_STAGE = 0.12e-6;    /* consumer cost per ring stage: slot wait, votes, release */
+constexpr double C_BPS = 1.5e11;       /* consumer GEMV rate of one CTA on staged weights (bytes/s) */
 
 std::string fmt(const char *f, ...) __attribute__((format(printf, 1, 2)));
 std::string fmt(const char *f, ...) {
@@ -67,7 +69,7 @@ std::string fmt(const char *f, ...) {
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
 struct SmemModel {
-    int act, result, scales, fac, fixed;
+    int act, result, scales, fac, work, fixed;
 };
 
 /* attention task: q of the group, the new k and v, per-warp (o, m, l) of every
@@ -126,17 +128,18 @@ int rows_per_slot(const Geo &g, int op, int ks, int slot) {
     return std::max(1, std::min(256, slot / (kc * g.web(op))));
 }
 
-/* Shared memory besides the ring: fp32 activation slice [B][K/ks], GEMV
- * partial sums [rows][segments][B] (a tile of R < 8 rows is split into 8/R
- * K segments so every consumer warp works), int8 row scales, attention merge
- * factors [B][n_heads][C]. */
+/* Shared memory besides the ring.  One region serves whichever task runs:
+ * a GEMV task's partial sums [rows][segments][B], int8 row scales and (batch
+ * above 1 or a K split) its fp32 activation slice [B][K/ks]; an attention
+ * task's q, new k/v and per-warp state; a merge task's sums.  A tile of R < 8
+ * rows at batch above 1 is split into 8/R K segments so every warp works. */
 SmemModel smem_model(const Geo &g, int ks, int slot, int C, int n_sm) {
     SmemModel m{};
-    m.act = att_smem_need(g);
+    int gemv_act = 0;
     for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN, OP_LMH}) {
         int kc = g.K(op) / ksplit_for(g, op, ks);
         /* batch 1 without a K split keeps activations in registers */
-        if (g.B > 1 || ksplit_for(g, op, ks) > 1) m.act = std::max(m.act, g.B * kc * 4);
+        if (g.B > 1 || ksplit_for(g, op, ks) > 1) gemv_act = std::max(gemv_act, g.B * kc * 4);
         int R = rows_per_slot(g, op, ks, slot);
         int S = gemv_segments(g.B, kc, g.web(op) == 1, R);
         int rows = max_task_rows(g, op, n_sm) + 1;  /* +1: a QKV matrix boundary can split a block */
@@ -144,34 +147,39 @@ SmemModel smem_model(const Geo &g, int ks, int slot, int C, int n_sm) {
         if (g.scaled(op)) m.scales = std::max(m.scales, rows * g.nmat(op) * 4);
     }
     (void)C;
-    m.fac = mrg_smem_need(g);
-    m.act = align_up(m.act, 128);
+    m.act = align_up(gemv_act, 128);
     m.result = align_up(m.result, 128);
     m.scales = align_up(m.scales, 128);
-    m.fac = align_up(m.fac, 128);
-    m.fixed = SMEM_BARRIERS + SMEM_MISC + m.act + m.result + m.scales + m.fac;
+    m.fac = align_up(mrg_smem_need(g), 128);
+    m.work = align_up(std::max(std::max(m.result + m.scales + m.act, att_smem_need(g)), m.fac), 128);
+    m.fixed = SMEM_BARRIERS + SMEM_MISC + m.work;
     return m;
 }
 
 double model_cost_us(const Geo &g, const Knobs &k, int n_sm) {
     /* a CTA streams at most one ring slot per T_COPY, and its share of HBM */
     const double per_sm = std::min(HBM_BPS / n_sm, k.slot_bytes / T_COPY);
-    const double ring_hide = (double)k.n_slots * k.slot_bytes / per_sm;
+    const double ring = (double)k.n_slots * k.slot_bytes;
+    const double ring_hide = ring / per_sm;
     auto stall = [&](double pro) { return std::max(0.0, T_SYNC + pro - ring_hide); };
-    double t = 0;
-    for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN}) {
+    /* one GEMV level: the loader has filled the ring while the level waited for
+     * its inputs; the rest streams at the CTA's share of HBM, while consumers
+     * pay a fixed cost per ring stage plus their arithmetic rate */
+    auto gemv = [&](int op, double rows) {
         int ks = ksplit_for(g, op, k.ksplit);
         int R = rows_per_slot(g, op, k.ksplit, k.slot_bytes);
-        double rows = ceil_div(g.rows(op), n_sm);
         double stages = std::ceil(rows / R) * ks * g.nmat(op);
         double bytes = rows * g.nmat(op) * g.row_bytes(op);
-        double fill = bytes / (stages * k.slot_bytes); /* slot fraction actually used */
+        double stream = std::max(0.0, bytes - ring) / per_sm;
+        double consume = stages * T_STAGE + bytes / C_BPS;
         double pro;
         if (op == OP_OPR) pro = (double)g.B * g.nq * g.d * 2 / L2_SM_BPS;
         else if (op == OP_DWN) pro = (double)g.B * g.I * 2 / L2_SM_BPS;
         else pro = (double)g.B * g.H * 4 / L2_SM_BPS;
-        t += g.L * (bytes / (per_sm * std::max(fill, 1e-3)) + stall(pro) + T_TASK * ks);
-    }
+        return T_SYNC + pro + std::max(stream, consume) + T_TASK * ks;
+    };
+    double t = 0;
+    for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN}) t += g.L * gemv(op, std::ceil((double)g.rows(op) / n_sm));
     {
         /* attention chunks (K/V streamed, scores and P.V for every head of the
          * group), then one merge per (sequence, query head) */
@@ -186,10 +194,7 @@ double model_cost_us(const Geo &g, const Knobs &k, int n_sm) {
         double merge = T_SYNC + per_m * (T_MERGE + (double)k.C * (g.d + 2) * 8 / L2_SM_BPS);
         t += g.L * (per * std::max(task_bytes / bw, compute) + stall(pro) + T_TASK * per + merge);
     }
-    {
-        double bytes = (double)ceil_div(g.V, n_sm) * g.row_bytes(OP_LMH);
-        t += bytes / per_sm + stall((double)g.B * g.H * 4 / L2_SM_BPS) + T_TASK;
-    }
+    t += gemv(OP_LMH, std::ceil((double)g.V / n_sm));
     return t * 1e6;
 }
 
@@ -542,6 +547,7 @@ amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_c
     P->result_bytes = sm.result;
     P->scale_bytes = sm.scales;
     P->fac_bytes = sm.fac;
+    P->work_bytes = sm.work;
     P->smem_bytes = sm.fixed + best.n_slots * best.slot_bytes;
     P->modeled_us = best_cost;
     P->candidates = cands;

@@ -63,7 +63,7 @@ struct amk_plan {
     std::vector<std::vector<amk::Task>> sm_tasks;
     std::vector<std::vector<std::vector<amk::Access>>> acc; /* parallel to sm_tasks */
     int n_counters = 0, n_levels = 0;
-    int act_bytes = 0, result_bytes = 0, scale_bytes = 0, fac_bytes = 0, smem_bytes = 0;
+    int act_bytes = 0, result_bytes = 0, scale_bytes = 0, fac_bytes = 0, work_bytes = 0, smem_bytes = 0;
     int64_t weight_bytes = 0, scratch_bytes = 0;
     double modeled_us = 0, search_ms = 0;
     int candidates = 0;
