@@ -114,7 +114,8 @@ typedef struct amk_schedule_options {
     int32_t n_slots;         /* ring depth (pipeline stages) */
     int32_t ksplit;          /* K-dimension split of GEMV tiles (1, 2, 4) */
     int32_t scratch_depth;   /* layers of activation scratch kept before reuse (>= 1) */
-    int32_t l2_prefetch_kb;  /* bytes the loader prefetches into L2 ahead of the ring, KB; -1 none */
+    int32_t l2_prefetch_kb;  /* KB each CTA's loader prefetches into L2 ahead of its ring fills, only while
+                                the ring is full; 0 or -1: none (the default; it measured slower) */
     int32_t trace;           /* 1: record per-task timestamps of every step (amk_debug_read_trace) */
     int64_t wait_timeout_ns; /* bound on every device-side wait; 0: 1 s */
 } amk_schedule_options;

@@ -359,19 +359,113 @@ struct Ring {
 
 /* ----------------------------------------------------------- loader */
 
+/* L2 prefetch ahead of the ring.  The ring holds a few stages; while the
+ * loader waits for a free slot, HBM would idle.  The loader therefore walks a
+ * second cursor over the same byte sequence and issues bulk L2 prefetches
+ * for the tiles the ring will take next, up to l2_prefetch_bytes ahead of
+ * what it has filled, so that later fills come from L2. */
+__device__ __forceinline__ void l2_prefetch(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+/* The idx-th contiguous byte range a task streams, in fill order: a GEMV
+ * task's row block of one matrix per stage (whole rows when K is split), an
+ * attention tile's K then V.  False past the last range. */
+__device__ bool task_range(const Params &p, const Task &t, int idx, const uint8_t *&ptr, uint32_t &bytes) {
+    if (t.op == OP_MRG) return false;
+    if (t.op == OP_ATT) {
+        const AttGeo a = att_geo(p, t);
+        const int k = idx / 2;
+        if (k >= a.ntile) return false;
+        const int t0 = a.s0 + k * t.rows_per_stage, t1 = min(a.e, t0 + (int)t.rows_per_stage);
+        const size_t row = (((size_t)t.layer * p.Bmax + t.b) * p.nkv + t.g) * (size_t)p.Smax + t0;
+        ptr = (const uint8_t *)((idx & 1 ? p.vc : p.kc) + row * p.d);
+        bytes = (uint32_t)(t1 - t0) * p.d * 2;
+        return true;
+    }
+    const GemvGeo g = gemv_geo(p, t);
+    const size_t rowb = (size_t)g.K * ((t.op == OP_LMH ? p.lm_int8 : p.wint8) ? 1 : 2);
+    if (g.ks > 1) {
+        if (idx >= g.nmat) return false;
+        ptr = op_weights(p, t, idx) + (size_t)t.r0 * rowb;
+        bytes = (uint32_t)((size_t)g.nrows * rowb);
+        return true;
+    }
+    const int rb = idx / g.nmat, m = idx % g.nmat;
+    if (rb >= g.nrb) return false;
+    const int ra = t.r0 + rb * g.R, re = min(t.r1, ra + g.R);
+    ptr = op_weights(p, t, m) + (size_t)ra * rowb;
+    bytes = (uint32_t)((size_t)(re - ra) * rowb);
+    return true;
+}
+
+struct Prefetch {
+    int ti, r;               /* task and range of the cursor */
+    uint32_t off;            /* offset in the range */
+    unsigned long long pos;  /* bytes the cursor has passed (prefetched or skipped) */
+    unsigned long long fill; /* bytes the ring has been given so far */
+    int cached;              /* task index held in t */
+    Task t;
+};
+
+/* move the prefetch cursor towards `ahead` bytes past the fill position, at
+ * most four prefetches per call so that the loader returns to its ring
+ * promptly; ranges the ring has already taken are skipped, not prefetched */
+__device__ void prefetch_ahead(const Params &p, Prefetch &pf, int tend) {
+    const unsigned long long goal = pf.fill + (unsigned long long)p.l2_prefetch_bytes;
+    for (int issued = 0; pf.pos < goal && pf.ti < tend && issued < 4;) {
+        if (pf.cached != pf.ti) {
+            load_task(p.tasks + pf.ti, pf.t);
+            pf.cached = pf.ti;
+        }
+        const uint8_t *ptr;
+        uint32_t bytes;
+        if (!task_range(p, pf.t, pf.r, ptr, bytes)) {
+            ++pf.ti;
+            pf.r = 0;
+            pf.off = 0;
+            continue;
+        }
+        uint32_t step = min(bytes - pf.off, 65536u);
+        if (pf.pos < pf.fill) {
+            step = (uint32_t)min((unsigned long long)step, pf.fill - pf.pos);
+        } else {
+            l2_prefetch(ptr + pf.off, step);
+            ++issued;
+        }
+        pf.off += step;
+        pf.pos += step;
+        if (pf.off >= bytes) {
+            ++pf.r;
+            pf.off = 0;
+        }
+    }
+}
+
 /* claim the next slot (bounded wait for its release) and arm its full barrier */
-__device__ __forceinline__ uint8_t *loader_claim(const Params &p, Smem &s, Ring &r, uint32_t bytes, int ti) {
+__device__ __forceinline__ uint8_t *loader_claim(const Params &p, Smem &s, Ring &r, uint32_t bytes, int ti,
+                                                 Prefetch &pf, int tend) {
     const unsigned long long t0 = p.trace ? now_ns() : 0;
+    /* prefetch only while the ring is full: fills of the current level come first */
+    if (p.l2_prefetch_bytes > 0 && r.pass > 0 && !mbar_test(&s.empty[r.slot], (r.pass - 1u) & 1u))
+        prefetch_ahead(p, pf, tend);
     if (r.pass > 0 && !wait_phase(p, s, &s.empty[r.slot], (r.pass - 1u) & 1u, 3, ti)) return nullptr;
     if (p.trace) p.trace[16 * (size_t)ti + 9] += now_ns() - t0;
     if (s.misc->abort) return nullptr;
     mbar_arrive_expect_tx(&s.full[r.slot], bytes);
+    pf.fill += bytes;
     return s.ring + (size_t)r.slot * p.slot_bytes;
 }
 
 __device__ void loader(const Params &p, Smem &s, int tbeg, int tend) {
     const int NS = p.n_slots;
     Ring r{0, 0, 0};
+    Prefetch pf;
+    pf.ti = tbeg;
+    pf.r = 0;
+    pf.off = 0u;
+    pf.pos = pf.fill = 0ull;
+    pf.cached = -1;
     for (int ti = tbeg; ti < tend; ++ti) {
         Task t;
         load_task(p.tasks + ti, t);
@@ -385,7 +479,7 @@ __device__ void loader(const Params &p, Smem &s, int tbeg, int tend) {
             for (int t0 = a.s0; t0 < a.e; t0 += t.rows_per_stage) {
                 const int t1 = min(a.e, t0 + (int)t.rows_per_stage);
                 const uint32_t bytes = (uint32_t)(t1 - t0) * p.d * 2;
-                uint8_t *dst = loader_claim(p, s, r, 2 * bytes, ti);
+                uint8_t *dst = loader_claim(p, s, r, 2 * bytes, ti, pf, tend);
                 if (!dst) {
                     s.misc->issued = (int)r.count;
                     return;
@@ -405,7 +499,7 @@ __device__ void loader(const Params &p, Smem &s, int tbeg, int tend) {
                 const int re = min(t.r1, ra + g.R);
                 const uint32_t bytes = (uint32_t)((re - ra) * segb);
                 for (int m = 0; m < g.nmat; ++m) {
-                    uint8_t *dst = loader_claim(p, s, r, bytes, ti);
+                    uint8_t *dst = loader_claim(p, s, r, bytes, ti, pf, tend);
                     if (!dst) {
                         s.misc->issued = (int)r.count;
                         return;
