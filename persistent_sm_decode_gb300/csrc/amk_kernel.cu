@@ -99,19 +99,21 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p) {
 
 /* epoch-tagged words: one 8-byte store publishes payload and flag together;
  * a two-word load returns each 8-byte element whole */
+/* one 8-byte store or load of each word is single-copy atomic; gpu scope is
+ * enough, since every producer and consumer runs on this device */
 __device__ __forceinline__ void st_ll(uint64_t *p, uint32_t payload, uint32_t epoch) {
-    asm volatile("st.volatile.global.u64 [%0], %1;" ::"l"(p), "l"(((uint64_t)epoch << 32) | payload) : "memory");
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(((uint64_t)epoch << 32) | payload) : "memory");
 }
 
 __device__ __forceinline__ ulonglong2 ld_ll2(const uint64_t *p) {
     ulonglong2 v;
-    asm volatile("ld.volatile.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
     return v;
 }
 
 __device__ __forceinline__ uint64_t ld_ll1(const uint64_t *p) {
     uint64_t v;
-    asm volatile("ld.volatile.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 
@@ -1154,7 +1156,7 @@ __device__ __forceinline__ void att_block(AttState<LP, GP> &st, const uint16_t *
     const int pg = lane / LP, ch = lane % LP, li = lane % LP;
     /* scores of every head for PW positions at a time */
 #pragma unroll 2
-    for (int it = 0; it < ATT_BP / PW; ++it) {
+    for (int it = 0; it * PW < nb; ++it) {
         const int jj = it * PW + pg;
         float sc[GP];
         if (jj < nb) {
@@ -1198,6 +1200,7 @@ __device__ __forceinline__ void att_block(AttState<LP, GP> &st, const uint16_t *
     __syncwarp();
     /* P.V */
     const uint16_t *vcol = Vt + (size_t)j0 * d + lane * EL;
+#pragma unroll 4
     for (int i = 0; i < nb; ++i) {
         float v[EL];
         if constexpr (EL == 2) {
@@ -1294,8 +1297,10 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
         const int nt = min(ag.e, t0 + (int)t.rows_per_stage) - t0;
         const uint16_t *Kt = reinterpret_cast<const uint16_t *>(s.ring + (size_t)sl * p.slot_bytes);
         const uint16_t *Vt = Kt + (size_t)t.rows_per_stage * d;
-        for (int j0 = warp * ATT_BP; j0 < nt; j0 += NCW * ATT_BP)
-            att_block<LP, GP>(st, Kt, Vt, j0, min(ATT_BP, nt - j0), d, sb, lane);
+        constexpr int PW = 32 / LP;
+        const int per = min(ATT_BP, ((nt + NCW - 1) / NCW + PW - 1) / PW * PW);
+        for (int j0 = warp * per; j0 < nt; j0 += NCW * per)
+            att_block<LP, GP>(st, Kt, Vt, j0, min(per, nt - j0), d, sb, lane);
         if (p.trace && warp == 0 && lane == 0) {
             s.misc->t_wait_full += tw1 - tw0;
             s.misc->t_tiles += now_ns() - tw1;
