@@ -640,12 +640,12 @@ __device__ __forceinline__ float dot_chunk(const uint4 &w, const float *h) {
 
 /* Batched tile: activations act[b][0..Kc) in shared memory.  With S > 1
  * segments per row warp w takes row w / S, K segment w % S; with S == 1 warp
- * w takes rows w, w + 8, ...  Partial sums go to res[(row * S + seg) * Bmax + b]
+ * w takes rows w, w + 8, ...  Partial sums go to res[(seg * sstride + row) * Bmax + b]
  * (accumulating over K-split passes); the epilogue adds the S segments in a
  * fixed order, so results do not depend on timing. */
 template <bool I8, int NB>
 __device__ void gemv_tile(const uint8_t *tile, int nrows, int S, int Kc, const float *act, int batch, float *res,
-                          int Bmax, bool first, int warp, int lane) {
+                          int sstride, int Bmax, bool first, int warp, int lane) {
     constexpr int EPC = I8 ? 16 : 8;
     const int nch = Kc / EPC;
     const size_t rowb = (size_t)Kc * (I8 ? 1 : 2);
@@ -667,7 +667,7 @@ __device__ void gemv_tile(const uint8_t *tile, int nrows, int S, int Kc, const f
             if (b < batch) {
                 const float v = warp_sum(a[b]);
                 if (lane == 0) {
-                    float *r = res + ((size_t)rr * S + seg) * Bmax + b;
+                    float *r = res + ((size_t)seg * sstride + rr) * Bmax + b;
                     *r = first ? v : *r + v;
                 }
             }
@@ -776,11 +776,11 @@ struct RowsPerGroup {
 /* One ring tile of a batch-1 task.  This warp takes rows rgp, rgp + RG, ...
  * of the tile, RPG of them at a time: every chunk load of the group is issued
  * first, then each row's products are summed over the lane's chunks, and one
- * transposing reduction gives all RPG row sums at once.  res[row * S + seg]
+ * transposing reduction gives all RPG row sums at once.  res[seg * sstride + row]
  * receives the segment's partial sum. */
 template <bool I8, int J>
 __device__ __forceinline__ void gemv_stage_b1(const uint8_t *tile, int nrows, int RG, int rgp, int rowc, int cs,
-                                              int nch, const ActChunk<I8> (&hv)[J], float *res, int S, int seg,
+                                              int nch, const ActChunk<I8> (&hv)[J], float *res, int sstride, int seg,
                                               int lane) {
     constexpr int RPG = RowsPerGroup<J>::value;
     const uint4 *W = reinterpret_cast<const uint4 *>(tile) + cs;
@@ -805,7 +805,7 @@ __device__ __forceinline__ void gemv_stage_b1(const uint8_t *tile, int nrows, in
         }
         const float y = xsum<RPG>(v, lane);
         const int rr = r0 + (lane / (32 / RPG)) * RG;
-        if ((lane & (32 / RPG - 1)) == 0 && rr < nrows) res[(size_t)rr * S + seg] = y;
+        if ((lane & (32 / RPG - 1)) == 0 && rr < nrows) res[seg * sstride + rr] = y;
     }
 }
 
@@ -929,7 +929,8 @@ __device__ __forceinline__ void resid_prefetch(const Params &p, const Task &t, i
 __device__ __forceinline__ float resid_value(const Params &p, Smem &s, const Task &t, int ti, const ResidPre &rp, int k,
                                              int b, int row) {
     const int l = t.layer, slot = l % p.depth;
-    if (k < 2 && ll_flag(rp.w[k]) == ver(p, l)) return ll_f(rp.w[k]);
+    const uint64_t w = k == 0 ? rp.w[0] : k == 1 ? rp.w[1] : 0ull; /* no dynamic index: rp stays in registers */
+    if (ll_flag(w) == ver(p, l)) return ll_f(w);
     if (t.op == OP_OPR) {
         if (l == 0) return bf2f(__ldg(p.embed + (size_t)__ldg(p.tokens + b) * p.H + row));
         return ll_wait1(p, s, p.x_in + ((size_t)slot * p.Bmax + b) * p.H + row, ver(p, l), ti, WB_XIN);
@@ -947,9 +948,18 @@ __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, i
     const uint32_t stale = (t.flags & TF_SKIP_SIGNAL) ? (uint32_t)(p.L + 1) : 0u;
     const uint32_t ep = ver(p, l) - stale, ep_next = ver(p, l + 1) - stale;
     const int n = t.r1 - t.r0, B = p.batch;
+    /* partial sums are segment-major, res[((seg * nmat + m) * n + row) * Bmax + b]:
+     * consecutive threads read consecutive words; the segments are added in order */
+    const int nmat = t.op == OP_GUP ? 2 : 1;
+    const int sstride = nmat * n * p.Bmax;
     auto y_of = [&](int m, int rr, int b) {
+        const float *r = s.res + ((size_t)m * n + rr) * p.Bmax + b;
+        float v[NCW];
+#pragma unroll
+        for (int sg = 0; sg < NCW; ++sg) v[sg] = sg < S ? r[(size_t)sg * sstride] : 0.f;
         float y = 0.f;
-        for (int sg = 0; sg < S; ++sg) y += s.res[(((size_t)m * n + rr) * S + sg) * p.Bmax + b];
+#pragma unroll
+        for (int sg = 0; sg < NCW; ++sg) y += v[sg];
         return I8 ? y * s.sc[m * n + rr] : y;
     };
     if (t.op == OP_GUP) {
@@ -1032,9 +1042,9 @@ __device__ bool gemv_task_b1(const Params &p, Smem &s, const Task &t, int ti, Ri
             if (!stage_ready(p, s, &s.full[sl], rg.pass & 1u, ti)) continue;
             const unsigned long long tw1 = p.trace ? now_ns() : 0;
             if (p.trace && rb == 0 && m == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
-            float *res = s.res + ((size_t)m * g.nrows + (ra - t.r0)) * S;
-            gemv_stage_b1<I8, J>(s.ring + (size_t)sl * p.slot_bytes, re - ra, RG, rgp, rowc, cs, nch, hv, res, S, seg,
-                                 lane);
+            float *res = s.res + (size_t)m * g.nrows + (ra - t.r0);
+            gemv_stage_b1<I8, J>(s.ring + (size_t)sl * p.slot_bytes, re - ra, RG, rgp, rowc, cs, nch, hv, res,
+                                 g.nmat * g.nrows, seg, lane);
             if (p.trace && warp == 0 && lane == 0) {
                 s.misc->t_wait_full += tw1 - tw0;
                 s.misc->t_tiles += now_ns() - tw1;
@@ -1096,9 +1106,10 @@ __device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring 
                 if (!stage_ready(p, s, &s.full[sl], rg.pass & 1u, ti)) continue;
                 const unsigned long long tw1 = p.trace ? now_ns() : 0;
                 if (p.trace && kp == 0 && rb == 0 && m == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
-                float *res = s.res + ((size_t)m * g.nrows + (ra - t.r0)) * S * p.Bmax;
+                float *res = s.res + ((size_t)m * g.nrows + (ra - t.r0)) * p.Bmax;
                 gemv_tile<I8, NB>(s.ring + (size_t)sl * p.slot_bytes, re - ra, S, g.Kc,
-                                  reinterpret_cast<const float *>(s.act), p.batch, res, p.Bmax, kp == 0, warp, lane);
+                                  reinterpret_cast<const float *>(s.act), p.batch, res, g.nmat * g.nrows, p.Bmax,
+                                  kp == 0, warp, lane);
                 if (p.trace && warp == 0 && lane == 0) {
                     s.misc->t_wait_full += tw1 - tw0;
                     s.misc->t_tiles += now_ns() - tw1;
