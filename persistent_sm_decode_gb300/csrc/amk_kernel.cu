@@ -963,16 +963,27 @@ __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, i
         return I8 ? y * s.sc[m * n + rr] : y;
     };
     if (t.op == OP_GUP) {
-        /* two SwiGLU outputs per word: task rows start at an even row and come in pairs */
-        for (int i = ctid; i < (n / 2) * B; i += NCW * 32) {
-            const int pr = i / B, b = i % B, rr = 2 * pr;
-            float a2[2];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const float gte = y_of(0, rr + q, b), up = y_of(1, rr + q, b);
-                a2[q] = gte / (1.f + __expf(-gte)) * up;
+        /* one SwiGLU output per thread; the thread of the even row packs its
+         * neighbour's value (lane + 1) with its own: task rows start at an
+         * even row and come in pairs, B items per row */
+        const int items = n * B;
+        for (int base = 0; base < items; base += NCW * 32) {
+            /* item index j = (row) * B + b, laid so that rows 2r and 2r+1 of
+             * sequence b sit in lanes that differ by one: j = ((r2 * B + b) * 2 + q) */
+            const int j = base + ctid;
+            float a = 0.f;
+            int pr = 0, b = 0, q = 0;
+            if (j < items) {
+                q = j & 1;
+                b = (j >> 1) % B;
+                pr = (j >> 1) / B;
+                const int rr = 2 * pr + q;
+                const float gte = y_of(0, rr, b), up = y_of(1, rr, b);
+                a = gte / (1.f + __expf(-gte)) * up;
             }
-            st_ll(p.act + (((size_t)slot * p.Bmax + b) * p.I + t.r0 + rr) / 2, pack_bf2(a2[0], a2[1]), ep);
+            const float other = __shfl_down_sync(0xffffffffu, a, 1);
+            if (j < items && q == 0)
+                st_ll(p.act + (((size_t)slot * p.Bmax + b) * p.I + t.r0 + 2 * pr) / 2, pack_bf2(a, other), ep);
         }
     } else {
         int k = 0;
