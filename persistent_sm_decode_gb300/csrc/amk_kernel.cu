@@ -1347,25 +1347,35 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
     }
     if (cbar_or(s.misc->abort != 0)) return false;
 
-    /* merge the warps of each head; publish the chunk's partial (o unnormalised, m, l),
-     * head-major: part[b][kv head][head][chunk] */
+    /* merge the warps of each head.  First the per-(warp, head) factors
+     * 2^(m_w - M) with M the head's maximum over warps, once each, into the
+     * block-score buffer (free after the tiles); then every output element is
+     * a weighted sum over the warps.  Publish the chunk's partial (o
+     * unnormalised, m, l), head-major: part[b][kv head][head][chunk]. */
+    float *fw = as.sbuf;          /* [NCW][GP] factors */
+    float *mh = as.sbuf + NCW * GP; /* [GP] head maxima */
+    if (ctid < NCW * GP) {
+        const int w2 = ctid / GP, hh = ctid % GP;
+        float M = -INFINITY;
+        for (int w3 = 0; w3 < NCW; ++w3) M = fmaxf(M, as.wst[((size_t)w3 * GP + hh) * (d + PART_PAD) + d]);
+        const float mw = as.wst[((size_t)w2 * GP + hh) * (d + PART_PAD) + d];
+        fw[ctid] = (mw == -INFINITY || M == -INFINITY) ? 0.f : exp2f(mw - M);
+        if (w2 == 0) mh[hh] = M;
+    }
+    cbar();
     if (active_seq) {
         const uint32_t ep = ver(p, l) - ((t.flags & TF_SKIP_SIGNAL) ? (uint32_t)(p.L + 1) : 0u);
         uint64_t *part = p.part + (((size_t)slot * p.Bmax + b) * p.nkv + grp) * G * p.C * (d + PART_PAD);
         for (int i = ctid; i < G * (d + 2); i += NCW * 32) {
             const int hh = i / (d + 2), e = i % (d + 2);
-            float M = -INFINITY;
-            for (int w2 = 0; w2 < NCW; ++w2) M = fmaxf(M, as.wst[((size_t)w2 * GP + hh) * (d + PART_PAD) + d]);
             float v = 0.f;
             if (e == d) {
-                v = M;
-            } else if (M != -INFINITY) {
-                for (int w2 = 0; w2 < NCW; ++w2) {
-                    const float *w = as.wst + ((size_t)w2 * GP + hh) * (d + PART_PAD);
-                    const float mw = w[d];
-                    if (mw == -INFINITY) continue;
-                    v += exp2f(mw - M) * (e == d + 1 ? w[d + 1] : w[e]);
-                }
+                v = mh[hh];
+            } else {
+                const int ee = e == d + 1 ? d + 1 : e;
+#pragma unroll
+                for (int w2 = 0; w2 < NCW; ++w2)
+                    v = fmaf(fw[w2 * GP + hh], as.wst[((size_t)w2 * GP + hh) * (d + PART_PAD) + ee], v);
             }
             st_ll(part + ((size_t)hh * p.C + t.r0) * (d + PART_PAD) + e, __float_as_uint(v), ep);
         }
