@@ -1309,6 +1309,8 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
     }
     float *sb = as.sbuf + warp * ATT_BP * GP;
 
+    const bool with_new = active_seq && (t.flags & TF_NEW_TOKEN);
+    bool new_done = false; /* warp-uniform */
     for (int k = 0; k < ag.ntile; ++k, rg.advance(NS)) {
         const int sl = rg.slot;
         const unsigned long long tw0 = p.trace ? now_ns() : 0;
@@ -1317,12 +1319,27 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
         if (p.trace && k == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
         const int t0 = ag.s0 + k * t.rows_per_stage;
         const int nt = min(ag.e, t0 + (int)t.rows_per_stage) - t0;
-        const uint16_t *Kt = reinterpret_cast<const uint16_t *>(s.ring + (size_t)sl * p.slot_bytes);
-        const uint16_t *Vt = Kt + (size_t)t.rows_per_stage * d;
+        uint16_t *Kt = reinterpret_cast<uint16_t *>(s.ring + (size_t)sl * p.slot_bytes);
+        uint16_t *Vt = Kt + (size_t)t.rows_per_stage * d;
+        /* the new position joins the last tile of the last chunk when the slot
+         * has a free row after the cached positions: the warp whose share
+         * covers it copies its K and V into that row first */
+        const bool add_new = with_new && k == ag.ntile - 1 && nt < (int)t.rows_per_stage;
+        const int ntot = nt + (add_new ? 1 : 0);
         constexpr int PW = 32 / LP;
-        const int per = min(ATT_BP, ((nt + NCW - 1) / NCW + PW - 1) / PW * PW);
-        for (int j0 = warp * per; j0 < nt; j0 += NCW * per)
-            att_block<LP, GP>(st, Kt, Vt, j0, min(per, nt - j0), d, sb, lane);
+        const int per = min(ATT_BP, ((ntot + NCW - 1) / NCW + PW - 1) / PW * PW);
+        for (int j0 = warp * per; j0 < ntot; j0 += NCW * per) {
+            const int nb = min(per, ntot - j0);
+            if (add_new && j0 <= nt && nt < j0 + nb) {
+                for (int i = lane; i < d / 8; i += 32) {
+                    reinterpret_cast<uint4 *>(Kt + (size_t)nt * d)[i] = reinterpret_cast<const uint4 *>(as.knew)[i];
+                    reinterpret_cast<uint4 *>(Vt + (size_t)nt * d)[i] = reinterpret_cast<const uint4 *>(as.vnew)[i];
+                }
+                __syncwarp();
+            }
+            att_block<LP, GP>(st, Kt, Vt, j0, nb, d, sb, lane);
+        }
+        if (add_new) new_done = true;
         if (p.trace && warp == 0 && lane == 0) {
             s.misc->t_wait_full += tw1 - tw0;
             s.misc->t_tiles += now_ns() - tw1;
@@ -1330,8 +1347,8 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.empty[sl]);
     }
-    /* the new position, from shared memory, on the last warp */
-    if (active_seq && (t.flags & TF_NEW_TOKEN) && warp == NCW - 1) att_block<LP, GP>(st, as.knew, as.vnew, 0, 1, d, sb, lane);
+    /* otherwise the new position on its own, from shared memory, on the last warp */
+    if (with_new && !new_done && warp == NCW - 1) att_block<LP, GP>(st, as.knew, as.vnew, 0, 1, d, sb, lane);
 
     /* the warp's state: o of every head, m and l of head lane (lane < GP) */
     {
