@@ -162,6 +162,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 struct Misc {
     volatile int abort;
+    volatile int cons_op; /* op of the task the consumers are running (loader's L2 prefetch window) */
     int issued;
     float red[MAXB][NCW];
     float rnorm[MAXB];
@@ -448,8 +449,11 @@ __device__ void prefetch_ahead(const Params &p, Prefetch &pf, int tend) {
 __device__ __forceinline__ uint8_t *loader_claim(const Params &p, Smem &s, Ring &r, uint32_t bytes, int ti,
                                                  Prefetch &pf, int tend) {
     const unsigned long long t0 = p.trace ? now_ns() : 0;
-    /* prefetch only while the ring is full: fills of the current level come first */
-    if (p.l2_prefetch_bytes > 0 && r.pass > 0 && !mbar_test(&s.empty[r.slot], (r.pass - 1u) & 1u))
+    /* prefetch only while the ring is full and the consumers run attention
+     * (a chain of short, latency-bound tasks that leaves HBM idle): fills of a
+     * streaming level come first */
+    if (p.l2_prefetch_bytes > 0 && r.pass > 0 && (s.misc->cons_op == OP_ATT || s.misc->cons_op == OP_MRG) &&
+        !mbar_test(&s.empty[r.slot], (r.pass - 1u) & 1u))
         prefetch_ahead(p, pf, tend);
     if (r.pass > 0 && !wait_phase(p, s, &s.empty[r.slot], (r.pass - 1u) & 1u, 3, ti)) return nullptr;
     if (p.trace) p.trace[16 * (size_t)ti + 9] += now_ns() - t0;
@@ -1519,6 +1523,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p)
 
     if (tid == 0) {
         s.misc->abort = 0;
+        s.misc->cons_op = OP_COUNT;
         s.misc->issued = 0;
         for (int i = 0; i < p.n_slots; ++i) {
             mbar_init(&s.full[i], 1);
@@ -1556,6 +1561,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p)
                     s.sc[i] = __ldg(op_scales(p, t, m) + t.r0 + rr);
                 }
             }
+            if (ctid == 0) s.misc->cons_op = t.op;
             ResidPre rp;
             resid_prefetch(p, t, ctid, rp);
             unsigned long long *tr = p.trace ? p.trace + 16 * (size_t)ti : nullptr;
