@@ -543,9 +543,9 @@ __device__ __forceinline__ float4 load_x4(const Params &p, Smem &s, const uint64
 }
 
 /* RMSNorm prologue into shared memory (batches above 1, or a K split):
- * act[b][k - k0] = bf16(x[b][k] * r_b * gain[k]) for k in [k0, k1), stored as
- * fp32 (the bf16 value exactly).  r_b is computed once per task (need_r) from
- * the whole of x[b].  Reading x waits for its producers. */
+ * act[b][k - k0] = bf16(x[b][k] * r_b * gain[k]) for k in [k0, k1), packed two
+ * per word.  r_b is computed once per task (need_r) from the whole of x[b].
+ * Reading x waits for its producers. */
 __device__ void norm_prologue(const Params &p, Smem &s, const uint64_t *xbase, bool from_embed, const uint16_t *gain,
                               int k0, int k1, bool need_r, uint32_t f, int task, int which, int ctid, int warp,
                               int lane) {
@@ -576,30 +576,30 @@ __device__ void norm_prologue(const Params &p, Smem &s, const uint64_t *xbase, b
         const uint64_t *xs = from_embed ? nullptr : xbase + (size_t)b * H;
         const uint16_t *emb = from_embed ? p.embed + (size_t)__ldg(p.tokens + b) * H : nullptr;
         const float r = s.misc->rnorm[b];
-        float4 *dst = reinterpret_cast<float4 *>(s.act + (size_t)b * kc * 4);
+        uint2 *dst = reinterpret_cast<uint2 *>(s.act + (size_t)b * kc * 2);
         for (int i4 = k0 / 4 + ctid; i4 < k1 / 4; i4 += NCW * 32) {
             float4 v = load_x4(p, s, xs, emb, i4, f, task, which);
             uint2 gw = __ldg(reinterpret_cast<const uint2 *>(gain) + i4);
-            dst[i4 - k0 / 4] = make_float4(round_bf(v.x * r * bf_lo(gw.x)), round_bf(v.y * r * bf_hi(gw.x)),
-                                           round_bf(v.z * r * bf_lo(gw.y)), round_bf(v.w * r * bf_hi(gw.y)));
+            dst[i4 - k0 / 4] = make_uint2(pack_bf2(v.x * r * bf_lo(gw.x), v.y * r * bf_hi(gw.x)),
+                                          pack_bf2(v.z * r * bf_lo(gw.y), v.w * r * bf_hi(gw.y)));
         }
     }
 }
 
 /* O-projection and down-projection prologues: bf16 activations [k0, k1) of
  * rows of `len` elements (attention output, SwiGLU output), held two per
- * epoch-tagged word, as fp32; waits for their producers */
+ * epoch-tagged word, copied as they are (two per word); waits for their
+ * producers */
 __device__ void copy_prologue(const Params &p, Smem &s, const uint64_t *src0, int len, int k0, int k1, uint32_t f,
                               int task, int which, int ctid) {
     const int kc = k1 - k0;
     for (int b = 0; b < p.batch; ++b) {
         const uint64_t *src = src0 + ((size_t)b * len + k0) / 2;
-        float4 *dst = reinterpret_cast<float4 *>(s.act + (size_t)b * kc * 4);
+        uint2 *dst = reinterpret_cast<uint2 *>(s.act + (size_t)b * kc * 2);
         for (int i = ctid; i < kc / 4; i += NCW * 32) {
             ulonglong2 v = ld_ll2(src + 2 * i);
             if (!ll_ok(f, v)) ll_settle(p, s, src + 2 * i, v, f, task, which);
-            const uint32_t a = (uint32_t)v.x, c = (uint32_t)v.y;
-            dst[i] = make_float4(bf_lo(a), bf_hi(a), bf_lo(c), bf_hi(c));
+            dst[i] = make_uint2((uint32_t)v.x, (uint32_t)v.y);
         }
     }
 }
@@ -612,32 +612,48 @@ __device__ __forceinline__ float i8_to_f(uint32_t xflip, int k) {
     return __uint_as_float(__byte_perm(xflip, 0x4B000000u, 0x7540u | (unsigned)k)) - 8388736.0f;
 }
 
-/* Dot product of one 16-byte weight chunk (8 bf16 or 16 int8) with EPC fp32
- * activations at h. */
+/* a += w * h over one pair of bf16 values (low or high halves): the
+ * mixed-precision FMA takes both operands as bf16, forms their product
+ * exactly in fp32 and rounds once, as fmaf on the widened values would */
+__device__ __forceinline__ void fma_bf16_lo(float &a, uint32_t w, uint32_t h) {
+    asm("{\n\t.reg .b16 w0, w1, h0, h1;\n\tmov.b32 {w0, w1}, %1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, w0, h0, %0;\n\t}"
+        : "+f"(a)
+        : "r"(w), "r"(h));
+}
+__device__ __forceinline__ void fma_bf16_hi(float &a, uint32_t w, uint32_t h) {
+    asm("{\n\t.reg .b16 w0, w1, h0, h1;\n\tmov.b32 {w0, w1}, %1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, w1, h1, %0;\n\t}"
+        : "+f"(a)
+        : "r"(w), "r"(h));
+}
+
+/* Dot product of one 16-byte weight chunk (8 bf16 or 16 int8) with EPC
+ * bf16 activations at h, packed two per word in element order. */
 template <bool I8>
-__device__ __forceinline__ float dot_chunk(const uint4 &w, const float *h) {
-    const float4 *h4 = reinterpret_cast<const float4 *>(h);
+__device__ __forceinline__ float dot_chunk(const uint4 &w, const uint32_t *h) {
     float s0 = 0.f, s1 = 0.f;
     if constexpr (I8) {
+        const uint4 ha = reinterpret_cast<const uint4 *>(h)[0], hb = reinterpret_cast<const uint4 *>(h)[1];
+        const uint32_t hw[8] = {ha.x, ha.y, ha.z, ha.w, hb.x, hb.y, hb.z, hb.w};
         const uint32_t x[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float4 a = h4[q];
-            s0 = fmaf(i8_to_f(x[q], 0), a.x, s0);
-            s1 = fmaf(i8_to_f(x[q], 1), a.y, s1);
-            s0 = fmaf(i8_to_f(x[q], 2), a.z, s0);
-            s1 = fmaf(i8_to_f(x[q], 3), a.w, s1);
+            s0 = fmaf(i8_to_f(x[q], 0), bf_lo(hw[2 * q]), s0);
+            s1 = fmaf(i8_to_f(x[q], 1), bf_hi(hw[2 * q]), s1);
+            s0 = fmaf(i8_to_f(x[q], 2), bf_lo(hw[2 * q + 1]), s0);
+            s1 = fmaf(i8_to_f(x[q], 3), bf_hi(hw[2 * q + 1]), s1);
         }
     } else {
-        const float4 a = h4[0], c = h4[1];
-        s0 = fmaf(bf_lo(w.x), a.x, s0);
-        s1 = fmaf(bf_hi(w.x), a.y, s1);
-        s0 = fmaf(bf_lo(w.y), a.z, s0);
-        s1 = fmaf(bf_hi(w.y), a.w, s1);
-        s0 = fmaf(bf_lo(w.z), c.x, s0);
-        s1 = fmaf(bf_hi(w.z), c.y, s1);
-        s0 = fmaf(bf_lo(w.w), c.z, s0);
-        s1 = fmaf(bf_hi(w.w), c.w, s1);
+        const uint4 a = reinterpret_cast<const uint4 *>(h)[0];
+        fma_bf16_lo(s0, w.x, a.x);
+        fma_bf16_hi(s1, w.x, a.x);
+        fma_bf16_lo(s0, w.y, a.y);
+        fma_bf16_hi(s1, w.y, a.y);
+        fma_bf16_lo(s0, w.z, a.z);
+        fma_bf16_hi(s1, w.z, a.z);
+        fma_bf16_lo(s0, w.w, a.w);
+        fma_bf16_hi(s1, w.w, a.w);
     }
     return s0 + s1;
 }
@@ -648,7 +664,7 @@ __device__ __forceinline__ float dot_chunk(const uint4 &w, const float *h) {
  * (accumulating over K-split passes); the epilogue adds the S segments in a
  * fixed order, so results do not depend on timing. */
 template <bool I8, int NB>
-__device__ void gemv_tile(const uint8_t *tile, int nrows, int S, int Kc, const float *act, int batch, float *res,
+__device__ void gemv_tile(const uint8_t *tile, int nrows, int S, int Kc, const uint32_t *act, int batch, float *res,
                           int sstride, int Bmax, bool first, int warp, int lane) {
     constexpr int EPC = I8 ? 16 : 8;
     const int nch = Kc / EPC;
@@ -664,7 +680,7 @@ __device__ void gemv_tile(const uint8_t *tile, int nrows, int S, int Kc, const f
             const uint4 wv = w[c];
 #pragma unroll
             for (int b = 0; b < NB; ++b)
-                if (b < batch) a[b] += dot_chunk<I8>(wv, act + (size_t)b * Kc + (size_t)c * EPC);
+                if (b < batch) a[b] += dot_chunk<I8>(wv, act + ((size_t)b * Kc + (size_t)c * EPC) / 2);
         }
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
@@ -728,22 +744,6 @@ template <>
 struct ActChunk<true> {
     float4 v[4];
 };
-
-/* a += w * h over one pair of bf16 values (low or high halves): the
- * mixed-precision FMA takes both operands as bf16, forms their product
- * exactly in fp32 and rounds once, as fmaf on the widened values would */
-__device__ __forceinline__ void fma_bf16_lo(float &a, uint32_t w, uint32_t h) {
-    asm("{\n\t.reg .b16 w0, w1, h0, h1;\n\tmov.b32 {w0, w1}, %1;\n\tmov.b32 {h0, h1}, %2;\n\t"
-        "fma.rn.f32.bf16 %0, w0, h0, %0;\n\t}"
-        : "+f"(a)
-        : "r"(w), "r"(h));
-}
-__device__ __forceinline__ void fma_bf16_hi(float &a, uint32_t w, uint32_t h) {
-    asm("{\n\t.reg .b16 w0, w1, h0, h1;\n\tmov.b32 {w0, w1}, %1;\n\tmov.b32 {h0, h1}, %2;\n\t"
-        "fma.rn.f32.bf16 %0, w1, h1, %0;\n\t}"
-        : "+f"(a)
-        : "r"(w), "r"(h));
-}
 
 /* one 16-byte weight chunk (8 bf16 or 16 int8) against activations in registers */
 template <bool I8>
@@ -1123,7 +1123,7 @@ __device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring 
                 if (p.trace && kp == 0 && rb == 0 && m == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
                 float *res = s.res + ((size_t)m * g.nrows + (ra - t.r0)) * p.Bmax;
                 gemv_tile<I8, NB>(s.ring + (size_t)sl * p.slot_bytes, re - ra, S, g.Kc,
-                                  reinterpret_cast<const float *>(s.act), p.batch, res, g.nmat * g.nrows, p.Bmax,
+                                  reinterpret_cast<const uint32_t *>(s.act), p.batch, res, g.nmat * g.nrows, p.Bmax,
                                   kp == 0, warp, lane);
                 if (p.trace && warp == 0 && lane == 0) {
                     s.misc->t_wait_full += tw1 - tw0;

@@ -133,8 +133,9 @@ int rows_per_slot(const Geo &g, int op, int ks, int slot) {
 
 /* Shared memory besides the ring.  One region serves whichever task runs:
  * a GEMV task's partial sums [rows][segments][B], int8 row scales and (batch
- * above 1 or a K split) its fp32 activation slice [B][K/ks]; an attention
- * task's q, new k/v and per-warp state; a merge task's sums.  A tile of R < 8
+ * above 1 or a K split) its bf16 activation slice [B][K/ks]; an attention
+ * task's q, new k/v and per-warp state; a merge task's sums.  Activations
+ * in shared memory are bf16, two per word.  A tile of R < 8
  * rows at batch above 1 is split into 8/R K segments so every warp works. */
 SmemModel smem_model(const Geo &g, int ks, int slot, int C, int n_sm) {
     SmemModel m{};
@@ -142,7 +143,7 @@ SmemModel smem_model(const Geo &g, int ks, int slot, int C, int n_sm) {
     for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN, OP_LMH}) {
         int kc = g.K(op) / ksplit_for(g, op, ks);
         /* batch 1 without a K split keeps activations in registers */
-        if (g.B > 1 || ksplit_for(g, op, ks) > 1) gemv_act = std::max(gemv_act, g.B * kc * 4);
+        if (g.B > 1 || ksplit_for(g, op, ks) > 1) gemv_act = std::max(gemv_act, g.B * kc * 2); /* bf16 */
         int R = rows_per_slot(g, op, ks, slot);
         int S = gemv_segments(g.B, kc, g.web(op) == 1, R);
         int rows = max_task_rows(g, op, n_sm) + 1;  /* +1: a QKV matrix boundary can split a block */
