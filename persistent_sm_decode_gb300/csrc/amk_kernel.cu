@@ -745,18 +745,40 @@ struct ActChunk<true> {
     float4 v[4];
 };
 
+/* packed fp32 pairs (sm_100 and later): (a, b) += (c, d); (s0, s1) += (a, b) * (c, d) */
+__device__ __forceinline__ void add_f32x2(float &a, float &b, float c, float d) {
+    asm("{\n\t.reg .b64 x, y;\n\tmov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\t"
+        "add.rn.f32x2 x, x, y;\n\tmov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(a), "+f"(b)
+        : "f"(c), "f"(d));
+}
+__device__ __forceinline__ void fma_f32x2(float &s0, float &s1, float a, float b, float c, float d) {
+    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\tmov.b64 z, {%0, %1};\n\t"
+        "fma.rn.f32x2 z, x, y, z;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "+f"(s0), "+f"(s1)
+        : "f"(a), "f"(b), "f"(c), "f"(d));
+}
+
 /* one 16-byte weight chunk (8 bf16 or 16 int8) against activations in registers */
 template <bool I8>
 __device__ __forceinline__ float dot_reg(const uint4 &w, const ActChunk<I8> &h) {
     float s0 = 0.f, s1 = 0.f;
     if constexpr (I8) {
+        /* int8 -> fp32 as in i8_to_f: the byte-permute places b ^ 0x80 under
+         * the exponent of 2^23, the packed subtraction removes 2^23 + 128 from
+         * two values at once, and one packed FMA takes both products; the
+         * order of the sums is that of the scalar form */
         const uint32_t x[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            s0 = fmaf(i8_to_f(x[q], 0), h.v[q].x, s0);
-            s1 = fmaf(i8_to_f(x[q], 1), h.v[q].y, s1);
-            s0 = fmaf(i8_to_f(x[q], 2), h.v[q].z, s0);
-            s1 = fmaf(i8_to_f(x[q], 3), h.v[q].w, s1);
+            float f0 = __uint_as_float(__byte_perm(x[q], 0x4B000000u, 0x7540u));
+            float f1 = __uint_as_float(__byte_perm(x[q], 0x4B000000u, 0x7541u));
+            float f2 = __uint_as_float(__byte_perm(x[q], 0x4B000000u, 0x7542u));
+            float f3 = __uint_as_float(__byte_perm(x[q], 0x4B000000u, 0x7543u));
+            add_f32x2(f0, f1, -8388736.0f, -8388736.0f);
+            add_f32x2(f2, f3, -8388736.0f, -8388736.0f);
+            fma_f32x2(s0, s1, f0, f1, h.v[q].x, h.v[q].y);
+            fma_f32x2(s0, s1, f2, f3, h.v[q].z, h.v[q].w);
         }
     } else {
         fma_bf16_lo(s0, w.x, h.w[0]);
