@@ -172,6 +172,7 @@ struct Misc {
     unsigned long long t_pro;       /* trace: prologue done */
     unsigned long long t_stages;    /* trace: last tile consumed */
     unsigned long long t_epi;       /* trace: epilogue written */
+    unsigned long long t_x[3];      /* trace: SM cycles from epilogue start to sums formed, stores issued, closing barrier (thread 0) */
 };
 
 struct Smem {
@@ -186,7 +187,7 @@ struct Smem {
 };
 
 /* first error wins; every CTA then stops at its next check */
-__device__ void raise_error(const Params &p, Smem &s, int code, int task, int what, uint32_t seen, uint32_t target) {
+__device__ __noinline__ void raise_error(const Params &p, Smem &s, int code, int task, int what, uint32_t seen, uint32_t target) {
     if (atomicCAS(&p.err[0], 0u, (uint32_t)code) == 0u) {
         p.err[1] = blockIdx.x;
         p.err[2] = (uint32_t)task;
@@ -238,28 +239,6 @@ __device__ __forceinline__ uint32_t ver(const Params &p, int version) { return p
 
 __device__ __forceinline__ bool ll_ok(uint32_t f, const ulonglong2 &v) { return ll_flag(v.x) == f && ll_flag(v.y) == f; }
 
-/* Re-read two tagged words until both carry flag f (the first read was
- * issued by the caller).  False on abort or timeout. */
-__device__ __noinline__ bool ll_settle(const Params &p, Smem &s, const uint64_t *src, ulonglong2 &v, uint32_t f,
-                                       int task, int which) {
-    const uint64_t t0 = now_ns();
-    for (uint32_t n = 0;; ++n) {
-        if (ll_ok(f, v)) return true;
-        if (s.misc->abort) return false;
-        if ((n & 63u) == 63u) {
-            if (ld_relaxed(p.err) != 0u) {
-                s.misc->abort = 1;
-                return false;
-            }
-            if ((long long)(now_ns() - t0) > p.timeout_ns) {
-                raise_error(p, s, 1, task, which, ll_flag(v.x) != f ? ll_flag(v.x) : ll_flag(v.y), f);
-                return false;
-            }
-        }
-        v = ld_ll2(src);
-    }
-}
-
 /* wait for one word with flag f */
 __device__ __noinline__ float ll_wait1(const Params &p, Smem &s, const uint64_t *src, uint32_t f, int task, int which) {
     const uint64_t t0 = now_ns();
@@ -276,6 +255,60 @@ __device__ __noinline__ float ll_wait1(const Params &p, Smem &s, const uint64_t 
                 raise_error(p, s, 1, task, which, ll_flag(w), f);
                 return 0.f;
             }
+        }
+    }
+}
+
+/* Checked every 64 passes of a multi-word wait: stop on another CTA's error,
+ * or raise a timeout that reports the flag `seen` of a word still stale. */
+__device__ __forceinline__ bool poll_slow(const Params &p, Smem &s, uint64_t t0, int task, int which, uint32_t seen,
+                                       uint32_t f) {
+    if (ld_relaxed(p.err) != 0u) {
+        s.misc->abort = 1;
+        return false;
+    }
+    if ((long long)(now_ns() - t0) > p.timeout_ns) {
+        raise_error(p, s, 1, task, which, seen, f);
+        return false;
+    }
+    return true;
+}
+
+/* Wait for N tagged words (W = uint64_t) or word pairs (W = ulonglong2) at
+ * once.  v[i] holds the caller's first read of the word(s) at addr(i); bit i
+ * of `pend` marks it stale (clear for words that are current or not needed).
+ * Every pass re-reads all stale words before it checks any, so a wait costs
+ * one L2 round trip per pass rather than one per word.  On abort or timeout
+ * it returns with words still stale; the caller's next abort check stops the
+ * task. */
+__device__ __forceinline__ uint64_t ll_load(const uint64_t *a, uint64_t) { return ld_ll1(a); }
+__device__ __forceinline__ ulonglong2 ll_load(const uint64_t *a, ulonglong2) { return ld_ll2(a); }
+__device__ __forceinline__ bool ll_cur(uint32_t f, uint64_t w) { return ll_flag(w) == f; }
+__device__ __forceinline__ bool ll_cur(uint32_t f, const ulonglong2 &v) { return ll_ok(f, v); }
+__device__ __forceinline__ uint32_t ll_seen(uint32_t f, uint64_t w) { return ll_flag(w); }
+__device__ __forceinline__ uint32_t ll_seen(uint32_t f, const ulonglong2 &v) {
+    return ll_flag(v.x) != f ? ll_flag(v.x) : ll_flag(v.y);
+}
+
+template <int N, class W, class A>
+__device__ __forceinline__ void settle_all(const Params &p, Smem &s, W (&v)[N], uint32_t pend, A addr, uint32_t f,
+                                           int task, int which) {
+    if (pend == 0u) return;
+    const uint64_t t0 = now_ns();
+    for (uint32_t n = 1;; ++n) {
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (pend >> i & 1u) v[i] = ll_load(addr(i), v[i]);
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if ((pend >> i & 1u) && ll_cur(f, v[i])) pend &= ~(1u << i);
+        if (pend == 0u || s.misc->abort) return;
+        if ((n & 63u) == 0u) {
+            uint32_t seen = 0u;
+#pragma unroll
+            for (int i = N - 1; i >= 0; --i)
+                if (pend >> i & 1u) seen = ll_seen(f, v[i]);
+            if (!poll_slow(p, s, t0, task, which, seen, f)) return;
         }
     }
 }
@@ -527,37 +560,66 @@ __device__ void loader(const Params &p, Smem &s, int tbeg, int tend) {
 
 /* ----------------------------------------------------------- prologues */
 
-/* four consecutive x values: the token's embedding row (layer 0) or epoch-
- * tagged residual words (waited for) */
-__device__ __forceinline__ float4 load_x4(const Params &p, Smem &s, const uint64_t *xs, const uint16_t *emb, int i4,
-                                          uint32_t f, int task, int which) {
+/* U groups of four consecutive x values, group u starting at element
+ * 4 * idx(u) (idx(u) < 0: none, zeros): the token's embedding row (layer 0)
+ * or epoch-tagged residual words, every word read before the first wait */
+template <int U, class I>
+__device__ __forceinline__ void load_x4s(const Params &p, Smem &s, const uint64_t *xs, const uint16_t *emb, I idx,
+                                         float4 (&x)[U], uint32_t f, int task, int which) {
     if (emb) {
-        uint2 w = __ldg(reinterpret_cast<const uint2 *>(emb) + i4);
-        return make_float4(bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i4 = idx(u);
+            const uint2 w = i4 >= 0 ? __ldg(reinterpret_cast<const uint2 *>(emb) + i4) : make_uint2(0u, 0u);
+            x[u] = make_float4(bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
+        }
+        return;
     }
-    const uint64_t *src = xs + 4 * (size_t)i4;
-    ulonglong2 a = ld_ll2(src), b = ld_ll2(src + 2);
-    if (!ll_ok(f, a)) ll_settle(p, s, src, a, f, task, which);
-    if (!ll_ok(f, b)) ll_settle(p, s, src + 2, b, f, task, which);
-    return make_float4(ll_f(a.x), ll_f(a.y), ll_f(b.x), ll_f(b.y));
+    ulonglong2 v[2 * U];
+    uint32_t pend = 0u;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int i4 = idx(u);
+        if (i4 >= 0) {
+            v[2 * u] = ld_ll2(xs + 4 * (size_t)i4);
+            v[2 * u + 1] = ld_ll2(xs + 4 * (size_t)i4 + 2);
+        } else {
+            v[2 * u] = v[2 * u + 1] = ulonglong2{0ull, 0ull};
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        if (idx(u) >= 0) {
+            if (!ll_ok(f, v[2 * u])) pend |= 1u << (2 * u);
+            if (!ll_ok(f, v[2 * u + 1])) pend |= 2u << (2 * u);
+        }
+    settle_all(p, s, v, pend, [=](int i) { return xs + 4 * (size_t)idx(i >> 1) + 2 * (i & 1); }, f, task, which);
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        x[u] = make_float4(ll_f(v[2 * u].x), ll_f(v[2 * u].y), ll_f(v[2 * u + 1].x), ll_f(v[2 * u + 1].y));
 }
 
 /* RMSNorm prologue into shared memory (batches above 1, or a K split):
  * act[b][k - k0] = bf16(x[b][k] * r_b * gain[k]) for k in [k0, k1), packed two
  * per word.  r_b is computed once per task (need_r) from the whole of x[b].
- * Reading x waits for its producers. */
+ * Reading x waits for its producers, XU groups of four per thread at a time. */
+constexpr int XU = 4;
 __device__ void norm_prologue(const Params &p, Smem &s, const uint64_t *xbase, bool from_embed, const uint16_t *gain,
                               int k0, int k1, bool need_r, uint32_t f, int task, int which, int ctid, int warp,
                               int lane) {
     const int H = p.H, H4 = H / 4;
+    constexpr int TS = NCW * 32;
     if (need_r) {
         for (int b = 0; b < p.batch; ++b) {
             const uint64_t *xs = from_embed ? nullptr : xbase + (size_t)b * H;
             const uint16_t *emb = from_embed ? p.embed + (size_t)__ldg(p.tokens + b) * H : nullptr;
             float ss = 0.f;
-            for (int i4 = ctid; i4 < H4; i4 += NCW * 32) {
-                float4 v = load_x4(p, s, xs, emb, i4, f, task, which);
-                ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+            for (int i0 = ctid; i0 < H4; i0 += XU * TS) {
+                float4 x[XU];
+                load_x4s<XU>(p, s, xs, emb, [=](int u) { return i0 + u * TS < H4 ? i0 + u * TS : -1; }, x, f, task,
+                             which);
+#pragma unroll
+                for (int u = 0; u < XU; ++u) ss += x[u].x * x[u].x + x[u].y * x[u].y + x[u].z * x[u].z + x[u].w * x[u].w;
             }
             ss = warp_sum(ss);
             if (lane == 0) s.misc->red[b][warp] = ss;
@@ -571,17 +633,26 @@ __device__ void norm_prologue(const Params &p, Smem &s, const uint64_t *xbase, b
         }
         cbar();
     }
-    const int kc = k1 - k0;
+    const int kc = k1 - k0, a4 = k0 / 4, n4 = kc / 4;
     for (int b = 0; b < p.batch; ++b) {
         const uint64_t *xs = from_embed ? nullptr : xbase + (size_t)b * H;
         const uint16_t *emb = from_embed ? p.embed + (size_t)__ldg(p.tokens + b) * H : nullptr;
         const float r = s.misc->rnorm[b];
         uint2 *dst = reinterpret_cast<uint2 *>(s.act + (size_t)b * kc * 2);
-        for (int i4 = k0 / 4 + ctid; i4 < k1 / 4; i4 += NCW * 32) {
-            float4 v = load_x4(p, s, xs, emb, i4, f, task, which);
-            uint2 gw = __ldg(reinterpret_cast<const uint2 *>(gain) + i4);
-            dst[i4 - k0 / 4] = make_uint2(pack_bf2(v.x * r * bf_lo(gw.x), v.y * r * bf_hi(gw.x)),
-                                          pack_bf2(v.z * r * bf_lo(gw.y), v.w * r * bf_hi(gw.y)));
+        for (int i0 = ctid; i0 < n4; i0 += XU * TS) {
+            float4 x[XU];
+            load_x4s<XU>(p, s, xs, emb, [=](int u) { return i0 + u * TS < n4 ? a4 + i0 + u * TS : -1; }, x, f, task,
+                         which);
+#pragma unroll
+            for (int u = 0; u < XU; ++u) {
+                const int i = i0 + u * TS;
+                if (i < n4) {
+                    const float4 v = x[u];
+                    const uint2 gw = __ldg(reinterpret_cast<const uint2 *>(gain) + a4 + i);
+                    dst[i] = make_uint2(pack_bf2(v.x * r * bf_lo(gw.x), v.y * r * bf_hi(gw.x)),
+                                        pack_bf2(v.z * r * bf_lo(gw.y), v.w * r * bf_hi(gw.y)));
+                }
+            }
         }
     }
 }
@@ -589,17 +660,31 @@ __device__ void norm_prologue(const Params &p, Smem &s, const uint64_t *xbase, b
 /* O-projection and down-projection prologues: bf16 activations [k0, k1) of
  * rows of `len` elements (attention output, SwiGLU output), held two per
  * epoch-tagged word, copied as they are (two per word); waits for their
- * producers */
+ * producers, CU word pairs per thread at a time over all sequences */
+constexpr int CU = 8;
 __device__ void copy_prologue(const Params &p, Smem &s, const uint64_t *src0, int len, int k0, int k1, uint32_t f,
                               int task, int which, int ctid) {
-    const int kc = k1 - k0;
-    for (int b = 0; b < p.batch; ++b) {
-        const uint64_t *src = src0 + ((size_t)b * len + k0) / 2;
-        uint2 *dst = reinterpret_cast<uint2 *>(s.act + (size_t)b * kc * 2);
-        for (int i = ctid; i < kc / 4; i += NCW * 32) {
-            ulonglong2 v = ld_ll2(src + 2 * i);
-            if (!ll_ok(f, v)) ll_settle(p, s, src + 2 * i, v, f, task, which);
-            dst[i] = make_uint2((uint32_t)v.x, (uint32_t)v.y);
+    constexpr int TS = NCW * 32;
+    const int kc = k1 - k0, n4 = kc / 4, tot = p.batch * n4;
+    auto addr = [=](int i) { return src0 + ((size_t)(i / n4) * len + k0) / 2 + 2 * (size_t)(i % n4); };
+    for (int i0 = ctid; i0 < tot; i0 += CU * TS) {
+        ulonglong2 v[CU];
+        uint32_t pend = 0u;
+#pragma unroll
+        for (int u = 0; u < CU; ++u) {
+            const int i = i0 + u * TS;
+            v[u] = i < tot ? ld_ll2(addr(i)) : ulonglong2{0ull, 0ull};
+        }
+#pragma unroll
+        for (int u = 0; u < CU; ++u)
+            if (i0 + u * TS < tot && !ll_ok(f, v[u])) pend |= 1u << u;
+        settle_all(p, s, v, pend, [=](int u) { return addr(i0 + u * TS); }, f, task, which);
+#pragma unroll
+        for (int u = 0; u < CU; ++u) {
+            const int i = i0 + u * TS;
+            if (i < tot)
+                reinterpret_cast<uint2 *>(s.act + (size_t)(i / n4) * kc * 2)[i % n4] =
+                    make_uint2((uint32_t)v[u].x, (uint32_t)v[u].y);
         }
     }
 }
@@ -843,25 +928,44 @@ __device__ __forceinline__ void norm_regs(const Params &p, Smem &s, const uint64
                                           const uint16_t *gain, int cs, int nch, int S, ActChunk<I8> (&hv)[J],
                                           uint32_t f, int task, int which, int warp, int lane) {
     constexpr int EPC = I8 ? 16 : 8, Q = EPC / 4;
+    /* the gains are read before the wait when they fit in registers beside
+     * x (up to four groups of four per lane), else after it */
+    constexpr bool early_gain = J * Q <= 4;
     uint2 gw[J][Q];
     float4 x[J][Q];
+    auto load_gain = [&]() {
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const int c = lane + 32 * j;
+        for (int j = 0; j < J; ++j) {
+            const int c = lane + 32 * j;
 #pragma unroll
-        for (int q = 0; q < Q; ++q)
-            gw[j][q] = c < nch ? __ldg(reinterpret_cast<const uint2 *>(gain) + (size_t)(cs + c) * Q + q) : make_uint2(0u, 0u);
+            for (int q = 0; q < Q; ++q)
+                gw[j][q] = c < nch ? __ldg(reinterpret_cast<const uint2 *>(gain) + (size_t)(cs + c) * Q + q)
+                                   : make_uint2(0u, 0u);
+        }
+    };
+    if constexpr (early_gain) load_gain();
+    /* JG chunks (at most four groups of four values) per wait */
+    constexpr int JG = Q == 2 ? 2 : 1;
+#pragma unroll
+    for (int j0 = 0; j0 < J; j0 += JG) {
+        float4 xf[JG * Q];
+        load_x4s<JG * Q>(
+            p, s, xs, emb,
+            [=](int u) {
+                const int c = lane + 32 * (j0 + u / Q);
+                return j0 + u / Q < J && c < nch ? (cs + c) * Q + u % Q : -1;
+            },
+            xf, f, task, which);
+#pragma unroll
+        for (int u = 0; u < JG * Q; ++u)
+            if (j0 + u / Q < J) x[j0 + u / Q][u % Q] = xf[u];
     }
     float ss = 0.f;
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const int c = lane + 32 * j;
+    for (int j = 0; j < J; ++j)
 #pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            x[j][q] = c < nch ? load_x4(p, s, xs, emb, (cs + c) * Q + q, f, task, which) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < Q; ++q)
             ss += x[j][q].x * x[j][q].x + x[j][q].y * x[j][q].y + x[j][q].z * x[j][q].z + x[j][q].w * x[j][q].w;
-        }
-    }
     __syncwarp();
     ss = warp_sum(ss);
     if (lane == 0 && warp < S) s.misc->red[0][warp] = ss;
@@ -869,6 +973,7 @@ __device__ __forceinline__ void norm_regs(const Params &p, Smem &s, const uint64
     float tot = 0.f;
     for (int w = 0; w < S; ++w) tot += s.misc->red[0][w];
     const float r = rsqrtf(tot / (float)p.H + p.eps);
+    if constexpr (!early_gain) load_gain();
 #pragma unroll
     for (int j = 0; j < J; ++j)
 #pragma unroll
@@ -893,26 +998,20 @@ template <bool I8, int J>
 __device__ __forceinline__ void copy_regs(const Params &p, Smem &s, const uint64_t *src, int cs, int nch,
                                           ActChunk<I8> (&hv)[J], uint32_t f, int task, int which, int lane) {
     constexpr int EPC = I8 ? 16 : 8, Q = EPC / 4;
-    ulonglong2 w[J][Q];
+    auto addr = [=](int u) { return src + ((size_t)(cs + lane + 32 * (u / Q)) * EPC + 4 * (u % Q)) / 2; };
+    ulonglong2 w[J * Q];
+    uint32_t pend = 0u;
+#pragma unroll
+    for (int u = 0; u < J * Q; ++u) w[u] = lane + 32 * (u / Q) < nch ? ld_ll2(addr(u)) : ulonglong2{0ull, 0ull};
+#pragma unroll
+    for (int u = 0; u < J * Q; ++u)
+        if (lane + 32 * (u / Q) < nch && !ll_ok(f, w[u])) pend |= 1u << u;
+    settle_all(p, s, w, pend, addr, f, task, which);
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-        const int c = lane + 32 * j;
-#pragma unroll
-        for (int q = 0; q < Q; ++q)
-            w[j][q] = c < nch ? ld_ll2(src + ((size_t)(cs + c) * EPC + 4 * q) / 2) : ulonglong2{0ull, 0ull};
-    }
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const int c = lane + 32 * j;
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
-            uint32_t a = 0u, b = 0u;
-            if (c < nch) {
-                ulonglong2 v = w[j][q];
-                if (!ll_ok(f, v)) ll_settle(p, s, src + ((size_t)(cs + c) * EPC + 4 * q) / 2, v, f, task, which);
-                a = (uint32_t)v.x;
-                b = (uint32_t)v.y;
-            }
+            const uint32_t a = (uint32_t)w[j * Q + q].x, b = (uint32_t)w[j * Q + q].y;
             if constexpr (I8) {
                 hv[j].v[q] = make_float4(bf_lo(a), bf_hi(a), bf_lo(b), bf_hi(b));
             } else {
@@ -970,6 +1069,7 @@ __device__ __forceinline__ float resid_value(const Params &p, Smem &s, const Tas
 template <bool I8>
 __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, int S, const ResidPre &rp, int ctid) {
     if (p.trace && ctid == 0) s.misc->t_stages = now_ns();
+    const long long c0 = p.trace ? clock64() : 0;
     const int l = t.layer, slot = l % p.depth;
     const uint32_t stale = (t.flags & TF_SKIP_SIGNAL) ? (uint32_t)(p.L + 1) : 0u;
     const uint32_t ep = ver(p, l) - stale, ep_next = ver(p, l + 1) - stale;
@@ -1007,6 +1107,7 @@ __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, i
                 const float gte = y_of(0, rr, b), up = y_of(1, rr, b);
                 a = gte / (1.f + __expf(-gte)) * up;
             }
+            if (p.trace && ctid == 0) s.misc->t_x[0] = clock64() - c0;
             const float other = __shfl_down_sync(0xffffffffu, a, 1);
             if (j < items && q == 0)
                 st_ll(p.act + (((size_t)slot * p.Bmax + b) * p.I + t.r0 + 2 * pr) / 2, pack_bf2(a, other), ep);
@@ -1016,6 +1117,7 @@ __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, i
         for (int i = ctid; i < n * B; i += NCW * 32, ++k) {
             const int rr = i / B, b = i % B, row = t.r0 + rr;
             const float y0 = y_of(0, rr, b);
+            if (p.trace && ctid == 0 && k == 0) s.misc->t_x[0] = clock64() - c0;
             switch (t.op) {
             case OP_QKV: {
                 const int base = t.mat == MAT_Q ? 0 : t.mat == MAT_K ? p.nq * p.d : (p.nq + p.nkv) * p.d;
@@ -1038,7 +1140,9 @@ __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, i
             }
         }
     }
+    if (p.trace && ctid == 0) s.misc->t_x[1] = clock64() - c0;
     const bool ok = !cbar_or(s.misc->abort != 0);
+    if (p.trace && ctid == 0) s.misc->t_x[2] = clock64() - c0;
     if (p.trace && ctid == 0) s.misc->t_epi = now_ns();
     return ok;
 }
@@ -1287,30 +1391,57 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
     if (active_seq) {
         const uint64_t *qkv = p.qkv + ((size_t)slot * p.Bmax + b) * p.qkv_rows;
         const float *rope = p.rope + (size_t)ag.p * d; /* [d/2][2] */
-        const int half = d / 2;
-        for (int i = ctid; i < (G + 2) * half; i += NCW * 32) {
+        const int half = d / 2, tot = (G + 2) * half;
+        const uint32_t f = ver(p, l);
+        /* item i = (h, e): element e of q head h (h < G), of k (h == G) or of
+         * v (h == G + 1), with its partner e + half; AU items per thread are
+         * read before the first wait ((G + 2) d / 2 <= 640 <= AU * 256) */
+        constexpr int AU = 3, TS = NCW * 32;
+        auto src = [=](int i) {
             const int h = i / half, e = i % half;
-            const float c = __ldg(rope + 2 * e), sn = __ldg(rope + 2 * e + 1);
-            const uint64_t *src = h < G ? qkv + (size_t)(grp * G + h) * d
-                                 : h == G ? qkv + (size_t)p.nq * d + grp * d
-                                          : qkv + (size_t)(p.nq + p.nkv) * d + grp * d;
-            const uint32_t f = ver(p, l);
-            uint64_t wa = ld_ll1(src + e), wb = ld_ll1(src + e + half);
-            const float a = ll_flag(wa) == f ? ll_f(wa) : ll_wait1(p, s, src + e, f, ti, WB_QKV);
-            const float bb = ll_flag(wb) == f ? ll_f(wb) : ll_wait1(p, s, src + e + half, f, ti, WB_QKV);
-            if (h < G) {
-                as.q[h * d + e] = (a * c - bb * sn) * p.qk_scale_log2;
-                as.q[h * d + e + half] = (bb * c + a * sn) * p.qk_scale_log2;
-            } else if (h == G) {
-                as.knew[e] = f2bf(a * c - bb * sn);
-                as.knew[e + half] = f2bf(bb * c + a * sn);
-            } else {
-                as.vnew[e] = f2bf(a);
-                as.vnew[e + half] = f2bf(bb);
+            const uint64_t *r = h < G ? qkv + (size_t)(grp * G + h) * d
+                                : h == G ? qkv + (size_t)p.nq * d + grp * d
+                                         : qkv + (size_t)(p.nq + p.nkv) * d + grp * d;
+            return r + e;
+        };
+        for (int i0 = ctid; i0 < tot; i0 += AU * TS) {
+            uint64_t w[2 * AU];
+            uint32_t pend = 0u;
+#pragma unroll
+            for (int u = 0; u < AU; ++u) {
+                const int i = i0 + u * TS;
+                w[2 * u] = i < tot ? ld_ll1(src(i)) : 0ull;
+                w[2 * u + 1] = i < tot ? ld_ll1(src(i) + half) : 0ull;
+            }
+#pragma unroll
+            for (int u = 0; u < AU; ++u)
+                if (i0 + u * TS < tot) {
+                    if (ll_flag(w[2 * u]) != f) pend |= 1u << (2 * u);
+                    if (ll_flag(w[2 * u + 1]) != f) pend |= 2u << (2 * u);
+                }
+            settle_all(p, s, w, pend, [=](int k) { return src(i0 + (k >> 1) * TS) + (k & 1) * half; }, f, ti, WB_QKV);
+#pragma unroll
+            for (int u = 0; u < AU; ++u) {
+                const int i = i0 + u * TS;
+                if (i >= tot) continue;
+                const int h = i / half, e = i % half;
+                const float c = __ldg(rope + 2 * e), sn = __ldg(rope + 2 * e + 1);
+                const float a = ll_f(w[2 * u]), bb = ll_f(w[2 * u + 1]);
+                if (h < G) {
+                    as.q[h * d + e] = (a * c - bb * sn) * p.qk_scale_log2;
+                    as.q[h * d + e + half] = (bb * c + a * sn) * p.qk_scale_log2;
+                } else if (h == G) {
+                    as.knew[e] = f2bf(a * c - bb * sn);
+                    as.knew[e + half] = f2bf(bb * c + a * sn);
+                } else {
+                    as.vnew[e] = f2bf(a);
+                    as.vnew[e + half] = f2bf(bb);
+                }
             }
         }
     }
     if (cbar_or(s.misc->abort != 0)) return false;
+    if (p.trace && ctid == 0) s.misc->t_pro = now_ns();
     if (active_seq && (t.flags & TF_NEW_TOKEN)) {
         const size_t row = ((((size_t)l * p.Bmax + b) * p.nkv + grp) * p.Smax + ag.p) * d;
         for (int i = ctid; i < d; i += NCW * 32) {
@@ -1375,6 +1506,7 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
     }
     /* otherwise the new position on its own, from shared memory, on the last warp */
     if (with_new && !new_done && warp == NCW - 1) att_block<LP, GP>(st, as.knew, as.vnew, 0, 1, d, sb, lane);
+    if (p.trace && ctid == 0) s.misc->t_stages = now_ns();
 
     /* the warp's state: o of every head, m and l of head lane (lane < GP) */
     {
@@ -1423,6 +1555,7 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
             st_ll(part + ((size_t)hh * p.C + t.r0) * (d + PART_PAD) + e, __float_as_uint(v), ep);
         }
     }
+    if (p.trace && ctid == 0) s.misc->t_epi = now_ns();
     return !cbar_or(s.misc->abort != 0);
 }
 
@@ -1452,36 +1585,30 @@ __device__ bool mrg_task(const Params &p, Smem &s, const Task &t, int ti, int ct
     if (b < p.batch) {
         const uint32_t f = ver(p, t.layer);
         const uint64_t *base = p.part + ((((size_t)slot * p.Bmax + b) * p.nkv + grp) * G + hh) * C * (d + PART_PAD);
-        ulonglong2 ml[MAXCPT], o0[MAXCPT], o1[MAXCPT];
+        /* word pairs 3k, 3k+1, 3k+2: (m, l), o[4 e4 ..], o[4 e4 + 2 ..] of chunk cl + k NCL */
+        auto addr = [=](int i) {
+            const uint64_t *r = base + (size_t)(cl + (i / 3) * NCL) * (d + PART_PAD);
+            return i % 3 == 0 ? r + d : r + 4 * e4 + 2 * (i % 3 - 1);
+        };
+        ulonglong2 v[3 * MAXCPT];
+        uint32_t pend = 0u;
 #pragma unroll
-        for (int k = 0; k < MAXCPT; ++k) {
-            const int c = cl + k * NCL;
-            if (c < C) {
-                const uint64_t *r = base + (size_t)c * (d + PART_PAD);
-                ml[k] = ld_ll2(r + d);
-                o0[k] = ld_ll2(r + 4 * e4);
-                o1[k] = ld_ll2(r + 4 * e4 + 2);
-            }
-        }
+        for (int i = 0; i < 3 * MAXCPT; ++i) v[i] = cl + (i / 3) * NCL < C ? ld_ll2(addr(i)) : ulonglong2{0ull, 0ull};
+#pragma unroll
+        for (int i = 0; i < 3 * MAXCPT; ++i)
+            if (cl + (i / 3) * NCL < C && !ll_ok(f, v[i])) pend |= 1u << i;
+        settle_all(p, s, v, pend, addr, f, ti, WB_PART);
+        ulonglong2 ml[MAXCPT], o0[MAXCPT], o1[MAXCPT];
         float mloc = -INFINITY;
 #pragma unroll
         for (int k = 0; k < MAXCPT; ++k) {
-            const int c = cl + k * NCL;
-            if (c < C) {
-                const uint64_t *r = base + (size_t)c * (d + PART_PAD);
-                ulonglong2 v = ml[k];
-                if (!ll_ok(f, v)) ll_settle(p, s, r + d, v, f, ti, WB_PART);
-                ml[k] = v;
-                v = o0[k];
-                if (!ll_ok(f, v)) ll_settle(p, s, r + 4 * e4, v, f, ti, WB_PART);
-                o0[k] = v;
-                v = o1[k];
-                if (!ll_ok(f, v)) ll_settle(p, s, r + 4 * e4 + 2, v, f, ti, WB_PART);
-                o1[k] = v;
-                mloc = fmaxf(mloc, ll_f(ml[k].x));
-            }
+            ml[k] = v[3 * k];
+            o0[k] = v[3 * k + 1];
+            o1[k] = v[3 * k + 2];
+            if (cl + k * NCL < C) mloc = fmaxf(mloc, ll_f(ml[k].x));
         }
         if (e4 == 0) mx[cl] = mloc;
+        if (p.trace && ctid == 0) s.misc->t_pro = now_ns();
         cbar();
         float M = -INFINITY;
         for (int i = 0; i < NCL; ++i) M = fmaxf(M, mx[i]);
@@ -1502,6 +1629,7 @@ __device__ bool mrg_task(const Params &p, Smem &s, const Task &t, int ti, int ct
         *reinterpret_cast<float4 *>(num + (size_t)cl * d + 4 * e4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         if (e4 == 0) den[cl] = dl;
         cbar();
+        if (p.trace && ctid == 0) s.misc->t_stages = now_ns();
         if (ctid < Q4) {
             float o[4] = {0.f, 0.f, 0.f, 0.f}, dd = 0.f;
             for (int i = 0; i < NCL; ++i) {
@@ -1519,6 +1647,7 @@ __device__ bool mrg_task(const Params &p, Smem &s, const Task &t, int ti, int ct
             st_ll(out + 1, pack_bf2(o[2] * inv, o[3] * inv), ep);
         }
     }
+    if (p.trace && ctid == 0) s.misc->t_epi = now_ns();
     return !cbar_or(s.misc->abort != 0);
 }
 
@@ -1593,6 +1722,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p)
                 s.misc->t_wait_full = 0;
                 s.misc->t_tiles = 0;
                 s.misc->t_pro = s.misc->t_stages = s.misc->t_epi = 0;
+                s.misc->t_x[0] = s.misc->t_x[1] = s.misc->t_x[2] = 0;
             }
             bool ok;
             if (t.op == OP_ATT)
@@ -1611,6 +1741,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p)
                 tr[6] = s.misc->t_pro;
                 tr[7] = s.misc->t_stages;
                 tr[8] = s.misc->t_epi;
+                tr[10] = s.misc->t_x[0];
+                tr[11] = s.misc->t_x[1];
+                tr[12] = s.misc->t_x[2];
             }
         }
     }
