@@ -1078,14 +1078,13 @@ __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, i
      * consecutive threads read consecutive words; the segments are added in order */
     const int nmat = t.op == OP_GUP ? 2 : 1;
     const int sstride = nmat * n * p.Bmax;
+    /* (the epilogue runs once per task, from a cold instruction cache: the
+     * segment loop stays rolled) */
     auto y_of = [&](int m, int rr, int b) {
         const float *r = s.res + ((size_t)m * n + rr) * p.Bmax + b;
-        float v[NCW];
-#pragma unroll
-        for (int sg = 0; sg < NCW; ++sg) v[sg] = sg < S ? r[(size_t)sg * sstride] : 0.f;
         float y = 0.f;
-#pragma unroll
-        for (int sg = 0; sg < NCW; ++sg) y += v[sg];
+#pragma unroll 1
+        for (int sg = 0; sg < S; ++sg) y += r[(size_t)sg * sstride];
         return I8 ? y * s.sc[m * n + rr] : y;
     };
     if (t.op == OP_GUP) {
@@ -1305,9 +1304,13 @@ template <int LP, int GP>
 __device__ __forceinline__ void att_block(AttState<LP, GP> &st, const uint16_t *Kt, const uint16_t *Vt, int j0,
                                           int nb, int d, float *sb, int lane) {
     constexpr int PW = 32 / LP, EL = LP / 8, LPH = 32 / GP;
+    /* a task runs this block once or a few times per layer, so its code is
+     * usually not in the instruction cache: with many heads per kv head the
+     * loops stay rolled (less code to fetch); with few, they unroll */
+    constexpr int UR = GP >= 4 ? 1 : 4;
     const int pg = lane / LP, ch = lane % LP, li = lane % LP;
     /* scores of every head for PW positions at a time */
-#pragma unroll 2
+#pragma unroll UR
     for (int it = 0; it * PW < nb; ++it) {
         const int jj = it * PW + pg;
         float sc[GP];
@@ -1328,12 +1331,14 @@ __device__ __forceinline__ void att_block(AttState<LP, GP> &st, const uint16_t *
     /* online softmax, head lane % GP over positions lane / GP + LPH k */
     const int hh = lane % GP, k0 = lane / GP;
     float mb = -INFINITY;
+#pragma unroll 1
     for (int jj = k0; jj < nb; jj += LPH) mb = fmaxf(mb, sb[jj * GP + hh]);
 #pragma unroll
     for (int o = GP; o < 32; o <<= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
     const float mnew = fmaxf(st.m, mb);
     const float alpha = exp2f(st.m - mnew);
     float ps = 0.f;
+#pragma unroll 1
     for (int jj = k0; jj < nb; jj += LPH) {
         const float pv = exp2f(sb[jj * GP + hh] - mnew);
         sb[jj * GP + hh] = pv;
@@ -1352,7 +1357,7 @@ __device__ __forceinline__ void att_block(AttState<LP, GP> &st, const uint16_t *
     __syncwarp();
     /* P.V */
     const uint16_t *vcol = Vt + (size_t)j0 * d + lane * EL;
-#pragma unroll 4
+#pragma unroll UR
     for (int i = 0; i < nb; ++i) {
         float v[EL];
         if constexpr (EL == 2) {
@@ -1548,7 +1553,7 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
                 v = mh[hh];
             } else {
                 const int ee = e == d + 1 ? d + 1 : e;
-#pragma unroll
+#pragma unroll 2
                 for (int w2 = 0; w2 < NCW; ++w2)
                     v = fmaf(fw[w2 * GP + hh], as.wst[((size_t)w2 * GP + hh) * (d + PART_PAD) + ee], v);
             }

@@ -115,7 +115,46 @@ std::vector<int> qkv_ctas(const Geo &g, int n_sm) {
     return cnt;
 }
 
+/* O-projection rows per CTA, as boundaries [n_sm + 1].  The CTAs that merge
+ * attention heads (one merge per (sequence, query head), spread as in
+ * att_level) reach their O-projection task about T_MRG_LAG after the others,
+ * which are already waiting on the merged output with their prologue running;
+ * they take that much less work, at the consumer's in-kernel rate, so that
+ * the level ends at the same time on every CTA. */
+constexpr double T_MRG_LAG = 1.0e-6;
+constexpr double C_BPS_LIVE = 7.5e10; /* consumer rate with ring fills sharing shared memory */
+std::vector<int> opr_split(const Geo &g, int n_sm) {
+    const int rows = g.rows(OP_OPR), M = g.B * g.nq;
+    std::vector<double> w(n_sm, 1.0);
+    if (M < n_sm) {
+        const double lag_rows = T_MRG_LAG * C_BPS_LIVE / (double)g.row_bytes(OP_OPR);
+        /* r_n for the others, r_n - lag for the merging CTAs, total = rows */
+        double rn = ((double)rows + M * lag_rows) / n_sm, rm = rn - lag_rows;
+        if (rm < 0) {
+            rm = 0;
+            rn = (double)rows / (n_sm - M);
+        }
+        for (int i = 0; i < M; ++i) w[(int64_t)i * n_sm / M] = rm / rn;
+    }
+    double tot = 0;
+    for (double x : w) tot += x;
+    std::vector<int> bnd(n_sm + 1, 0);
+    double acc = 0;
+    for (int s = 0; s < n_sm; ++s) {
+        acc += w[s];
+        bnd[s + 1] = std::min(rows, std::max(bnd[s], (int)std::lround(rows * acc / tot)));
+    }
+    bnd[n_sm] = rows;
+    return bnd;
+}
+
 int max_task_rows(const Geo &g, int op, int n_sm) {
+    if (op == OP_OPR) {
+        const std::vector<int> b = opr_split(g, n_sm);
+        int r = 0;
+        for (int s = 0; s < n_sm; ++s) r = std::max(r, b[s + 1] - b[s]);
+        return std::min(r, MAX_TASK_ROWS);
+    }
     if (op == OP_QKV && n_sm >= 3) {
         const std::vector<int> cnt = qkv_ctas(g, n_sm);
         const int len[3] = {g.nq * g.d, g.nkv * g.d, g.nkv * g.d};
@@ -245,8 +284,9 @@ struct Builder {
     }
     int rows_per_stage(int op, int ks) const { return rows_per_slot(g, op, ks, k.slot_bytes); }
 
-    /* Even row split of `op` over CTAs; each CTA's range is cut into tasks of at
-     * most MAX_TASK_ROWS rows (and, for QKV, at matrix and signal-count limits). */
+    /* Even row split of `op` over CTAs (the O projection as opr_split gives);
+     * each CTA's range is cut into tasks of at most MAX_TASK_ROWS rows (and,
+     * for QKV, at matrix and signal-count limits). */
     void gemv_level(int op, int l) {
         int rows = g.rows(op);
         /* gate/up tasks start on even rows: two SwiGLU outputs share a word */
@@ -260,6 +300,12 @@ struct Builder {
                 for (int j = 0; j < cnt[m]; ++j, ++sm)
                     gemv_range(op, l, sm, lo[m] + (int)((int64_t)j * len[m] / cnt[m]),
                                lo[m] + (int)((int64_t)(j + 1) * len[m] / cnt[m]));
+            return;
+        }
+        if (op == OP_OPR) {
+            const std::vector<int> b = opr_split(g, n_sm);
+            for (int s = 0; s < n_sm; ++s)
+                if (b[s + 1] > b[s]) gemv_range(op, l, s, b[s], b[s + 1]);
             return;
         }
         for (int s = 0; s < n_sm; ++s)
