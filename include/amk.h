@@ -118,6 +118,9 @@ typedef struct amk_schedule_options {
                                 the ring is full; 0 or -1: none (the default; it measured slower) */
     int32_t trace;           /* 1: record per-task timestamps of every step (amk_debug_read_trace) */
     int64_t wait_timeout_ns; /* bound on every device-side wait; 0: 1 s */
+    int32_t l2_evict_first;  /* 1 or 0 (the default): ring fills carry an L2 evict-first hint, so that the
+                                once-per-step weight and KV stream does not push code and activation scratch
+                                out of L2; -1: no hint.  Results are identical either way. */
 } amk_schedule_options;
 
 typedef struct amk_handle amk_handle;
@@ -201,7 +204,7 @@ typedef struct amk_plan_info {
     double modeled_us;        /* the search's cost-model estimate for one step */
     double search_ms;         /* host time of DAG build + search + solidify + validate */
     int32_t candidates;       /* schedule points the search evaluated */
-    int32_t reserved;
+    int32_t l2_evict_first;   /* 1 if ring fills carry the L2 evict-first hint */
 } amk_plan_info;
 amk_status amk_get_plan_info(const amk_handle *h, amk_plan_info *info);
 

@@ -47,7 +47,8 @@ class Weights(ctypes.Structure):
 
 class ScheduleOptions(ctypes.Structure):
     _fields_ = [("n_sm", i32), ("att_chunks", i32), ("slot_bytes", i32), ("n_slots", i32), ("ksplit", i32),
-                ("scratch_depth", i32), ("l2_prefetch_kb", i32), ("trace", i32), ("wait_timeout_ns", i64)]
+                ("scratch_depth", i32), ("l2_prefetch_kb", i32), ("trace", i32), ("wait_timeout_ns", i64),
+                ("l2_evict_first", i32)]
 
 
 class ErrorInfo(ctypes.Structure):
@@ -60,10 +61,10 @@ class PlanInfo(ctypes.Structure):
                                    "n_slots", "ksplit", "scratch_depth", "att_tile", "smem_bytes",
                                    "max_tasks_per_sm")] + \
                [("weight_bytes", i64), ("scratch_bytes", i64), ("modeled_us", f64), ("search_ms", f64),
-                ("candidates", i32), ("reserved", i32)]
+                ("candidates", i32), ("l2_evict_first", i32)]
 
     def as_dict(self) -> dict:
-        return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
+        return {k: getattr(self, k) for k, _ in self._fields_}
 
 
 class AmkError(RuntimeError):

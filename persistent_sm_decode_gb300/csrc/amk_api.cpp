@@ -249,6 +249,7 @@ amk_status amk_create(const amk_config *config, const amk_weights *weights, cons
     p.fac_bytes = P.fac_bytes;
     p.work_bytes = P.work_bytes;
     p.l2_prefetch_bytes = P.k.l2_prefetch_kb > 0 ? P.k.l2_prefetch_kb * 1024 : 0;
+    p.evict_first = P.k.evict_first;
     p.layers = h->d_layers;
     p.embed = (const uint16_t *)weights->embed;
     p.final_norm = (const uint16_t *)weights->final_norm;

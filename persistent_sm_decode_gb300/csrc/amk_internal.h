@@ -80,6 +80,8 @@ struct Params {
     int act_bytes, result_bytes, scale_bytes, fac_bytes;
     int work_bytes; /* the per-task region: GEMV sums + scales + activations, or attention state, or merge sums */
     int l2_prefetch_bytes;
+    int evict_first; /* 1: ring fills carry an L2 evict-first hint: weights and the cached prefix are read once
+                        per step, while code, scratch and tables are reused every layer */
     /* weights */
     const LayerPtrs *layers;
     const uint16_t *embed, *final_norm;

@@ -85,6 +85,32 @@ __device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
+/* the same copy with an L2 cache policy (createpolicy) attached */
+__device__ __forceinline__ void bulk_copy_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                               uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+/* L2 policy under which the lines a copy brings in are the first to go */
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+/* fill of one ring slot, with or without the evict-first policy */
+__device__ __forceinline__ void ring_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar, bool hint,
+                                          uint64_t policy) {
+    if (hint)
+        bulk_copy_hint(dst, src, bytes, bar, policy);
+    else
+        bulk_copy(dst, src, bytes, bar);
+}
+
 __device__ __forceinline__ uint64_t now_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -498,6 +524,11 @@ __device__ __forceinline__ uint8_t *loader_claim(const Params &p, Smem &s, Ring 
 
 __device__ void loader(const Params &p, Smem &s, int tbeg, int tend) {
     const int NS = p.n_slots;
+    /* the weight and KV stream passes through L2 once per step; marking it
+     * evict-first keeps the lines that are reused every layer (code, the
+     * activation words, RoPE rows, task records) resident */
+    const bool hint = p.evict_first != 0;
+    const uint64_t pol = hint ? policy_evict_first() : 0ull;
     Ring r{0, 0, 0};
     Prefetch pf;
     pf.ti = tbeg;
@@ -523,8 +554,8 @@ __device__ void loader(const Params &p, Smem &s, int tbeg, int tend) {
                     s.misc->issued = (int)r.count;
                     return;
                 }
-                bulk_copy(dst, kb + (size_t)t0 * p.d * 2, bytes, &s.full[r.slot]);
-                bulk_copy(dst + tb, vb + (size_t)t0 * p.d * 2, bytes, &s.full[r.slot]);
+                ring_copy(dst, kb + (size_t)t0 * p.d * 2, bytes, &s.full[r.slot], hint, pol);
+                ring_copy(dst + tb, vb + (size_t)t0 * p.d * 2, bytes, &s.full[r.slot], hint, pol);
                 r.advance(NS);
             }
             continue;
@@ -544,11 +575,12 @@ __device__ void loader(const Params &p, Smem &s, int tbeg, int tend) {
                         return;
                     }
                     if (g.ks == 1) {
-                        bulk_copy(dst, W[m] + (size_t)ra * rowb, bytes, &s.full[r.slot]);
+                        ring_copy(dst, W[m] + (size_t)ra * rowb, bytes, &s.full[r.slot], hint, pol);
                     } else {
                         const uint8_t *src = W[m] + (size_t)ra * rowb + (size_t)kp * segb;
                         for (int q = 0; q < re - ra; ++q)
-                            bulk_copy(dst + (size_t)q * segb, src + (size_t)q * rowb, (uint32_t)segb, &s.full[r.slot]);
+                            ring_copy(dst + (size_t)q * segb, src + (size_t)q * rowb, (uint32_t)segb, &s.full[r.slot],
+                                      hint, pol);
                     }
                     r.advance(NS);
                 }

@@ -219,6 +219,7 @@ amk_status upload(DeviceState &ds, const amk_config *c, const amk_weights *w, in
     p.fac_bytes = P.fac_bytes;
     p.work_bytes = P.work_bytes;
     p.l2_prefetch_bytes = P.k.l2_prefetch_kb > 0 ? P.k.l2_prefetch_kb * 1024 : 0;
+    p.evict_first = P.k.evict_first;
     p.layers = (const LayerPtrs *)(ds.base + o_layers);
     p.embed = (const uint16_t *)w->embed;
     p.final_norm = (const uint16_t *)w->final_norm;

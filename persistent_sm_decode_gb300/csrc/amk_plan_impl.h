@@ -33,6 +33,7 @@ struct Knobs {
     int depth = 2;          /* scratch slots */
     int att_tile = 64;      /* positions per attention tile */
     int l2_prefetch_kb = 0;
+    int evict_first = 1;    /* ring fills carry an L2 evict-first hint */
 };
 
 /* Model geometry seen by the planner. */

@@ -68,6 +68,17 @@ def test_plans_for_any_cta_count(amk, n_sm):
     _coverage(wl, p, 2)
 
 
+def test_schedule_options_reach_the_planner(amk):
+    # the last options field and the last plan-info field: a layout mismatch
+    # between the binding's structures and include/amk.h shows up here
+    wl = synth.workload("tiny")
+    assert amk.Plan(_cfg(amk, wl), 1, 152).info()["l2_evict_first"] == 1
+    off = amk.Plan(_cfg(amk, wl), 1, 152, options={"l2_evict_first": -1, "wait_timeout_ns": 5})
+    assert off.info()["l2_evict_first"] == 0
+    on = amk.Plan(_cfg(amk, wl), 1, 152, options={"l2_evict_first": 1, "att_chunks": 3})
+    assert on.info()["l2_evict_first"] == 1 and on.info()["att_chunks"] == 3
+
+
 def _coverage(wl, plan, B):
     d, nq, nkv = wl.head_dim, wl.n_heads, wl.n_kv_heads
     rows = {"QKV": (nq + 2 * nkv) * d, "OPR": wl.hidden, "GUP": wl.intermediate, "DWN": wl.hidden, "LMH": wl.vocab}
