@@ -116,7 +116,9 @@ typedef struct amk_schedule_options {
     int32_t scratch_depth;   /* layers of activation scratch kept before reuse (>= 1) */
     int32_t l2_prefetch_kb;  /* KB each CTA's loader prefetches into L2 ahead of its ring fills, only while
                                 the ring is full; 0 or -1: none (the default; it measured slower) */
-    int32_t trace;           /* 1: record per-task timestamps of every step (amk_debug_read_trace) */
+    int32_t trace;           /* 1: record per-task timestamps of every step (amk_debug_read_trace).  Only a
+                                library built with the timing code (AMK_TRACE=1 at build time) accepts it;
+                                the default build returns AMK_ERR_UNSUPPORTED. */
     int64_t wait_timeout_ns; /* bound on every device-side wait; 0: 1 s */
     int32_t l2_evict_first;  /* 1 or 0 (the default): ring fills carry an L2 evict-first hint, so that the
                                 once-per-step weight and KV stream does not push code and activation scratch

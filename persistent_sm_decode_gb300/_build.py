@@ -36,9 +36,18 @@ def _stale(target: str, deps) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+    """AMK_TRACE=1 in the environment builds the tuning variant whose kernel
+    carries the per-task timing code (schedule option ``trace``)."""
     os.makedirs(OBJ, exist_ok=True)
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, h) for h in ("amk.h", "amk_plan.h")]
-    common = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC] + list(extra_flags)
+    flags = list(extra_flags)
+    if os.environ.get("AMK_TRACE", "0") not in ("", "0"):
+        flags.append("-DAMK_TRACE_CODE=1")
+    stamp = os.path.join(OBJ, "flags.txt")
+    prev = open(stamp).read() if os.path.exists(stamp) else None
+    if prev != " ".join(flags):
+        force = True
+    common = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC] + flags
     procs, objs = [], []
     for src in SOURCES:
         path = os.path.join(CSRC, src)
@@ -64,6 +73,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         tmp = LIB + ".%d.tmp" % os.getpid()
         subprocess.check_call([nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static"])
         os.replace(tmp, LIB)
+    with open(stamp, "w") as f:
+        f.write(" ".join(flags))
     return LIB
 
 

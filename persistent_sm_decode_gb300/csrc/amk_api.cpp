@@ -107,6 +107,10 @@ amk_status amk_create(const amk_config *config, const amk_weights *weights, cons
                       amk_handle **out) {
     if (!config || !out) return AMK_ERR_INVALID_ARG;
     *out = nullptr;
+    /* the timing code and the loader's L2 prefetch exist only in builds
+     * that compile them in */
+    if (options && options->trace && !kernel_has_trace()) return AMK_ERR_UNSUPPORTED;
+    if (options && options->l2_prefetch_kb > 0 && !kernel_has_l2_prefetch()) return AMK_ERR_UNSUPPORTED;
     amk_status st = check_weights(*config, weights);
     if (st != AMK_OK) return st;
 

@@ -43,6 +43,23 @@
 #include "amk_internal.h"
 #include "amk_launch.h"
 
+/* Build switches:
+ *  AMK_TRACE_CODE       1 compiles in the per-task timing code that the
+ *                       trace option records (a tuning build).  The default
+ *                       build leaves it out: every task type runs once per
+ *                       layer from a cold instruction cache, and the
+ *                       never-taken timing branches inside the hot loops
+ *                       alone cost about 7 % of a step.
+ *  AMK_L2_PREFETCH_CODE 0 compiles out the loader's L2 prefetch (the
+ *                       l2_prefetch_kb option). */
+#ifndef AMK_TRACE_CODE
+#define AMK_TRACE_CODE 0
+#endif
+#ifndef AMK_L2_PREFETCH_CODE
+#define AMK_L2_PREFETCH_CODE 1
+#endif
+#define TRACE(p) (AMK_TRACE_CODE ? (p).trace : (unsigned long long *)nullptr)
+
 namespace amk {
 
 /* ----------------------------------------------------------- PTX wrappers */
@@ -507,15 +524,17 @@ __device__ void prefetch_ahead(const Params &p, Prefetch &pf, int tend) {
 /* claim the next slot (bounded wait for its release) and arm its full barrier */
 __device__ __forceinline__ uint8_t *loader_claim(const Params &p, Smem &s, Ring &r, uint32_t bytes, int ti,
                                                  Prefetch &pf, int tend) {
-    const unsigned long long t0 = p.trace ? now_ns() : 0;
+    const unsigned long long t0 = TRACE(p) ? now_ns() : 0;
     /* prefetch only while the ring is full and the consumers run attention
      * (a chain of short, latency-bound tasks that leaves HBM idle): fills of a
      * streaming level come first */
+#if AMK_L2_PREFETCH_CODE
     if (p.l2_prefetch_bytes > 0 && r.pass > 0 && (s.misc->cons_op == OP_ATT || s.misc->cons_op == OP_MRG) &&
         !mbar_test(&s.empty[r.slot], (r.pass - 1u) & 1u))
         prefetch_ahead(p, pf, tend);
+#endif
     if (r.pass > 0 && !wait_phase(p, s, &s.empty[r.slot], (r.pass - 1u) & 1u, 3, ti)) return nullptr;
-    if (p.trace) p.trace[16 * (size_t)ti + 9] += now_ns() - t0;
+    if (TRACE(p)) TRACE(p)[16 * (size_t)ti + 9] += now_ns() - t0;
     if (s.misc->abort) return nullptr;
     mbar_arrive_expect_tx(&s.full[r.slot], bytes);
     pf.fill += bytes;
@@ -539,7 +558,7 @@ __device__ void loader(const Params &p, Smem &s, int tbeg, int tend) {
     for (int ti = tbeg; ti < tend; ++ti) {
         Task t;
         load_task(p.tasks + ti, t);
-        if (p.trace) p.trace[16 * (size_t)ti + 9] = 0;
+        if (TRACE(p)) TRACE(p)[16 * (size_t)ti + 9] = 0;
         if (t.op == OP_MRG) continue;
         if (t.op == OP_ATT) {
             const AttGeo a = att_geo(p, t);
@@ -1100,8 +1119,8 @@ __device__ __forceinline__ float resid_value(const Params &p, Smem &s, const Tas
  * sums of the S segments are added in a fixed order. */
 template <bool I8>
 __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, int S, const ResidPre &rp, int ctid) {
-    if (p.trace && ctid == 0) s.misc->t_stages = now_ns();
-    const long long c0 = p.trace ? clock64() : 0;
+    if (TRACE(p) && ctid == 0) s.misc->t_stages = now_ns();
+    const long long c0 = TRACE(p) ? clock64() : 0;
     const int l = t.layer, slot = l % p.depth;
     const uint32_t stale = (t.flags & TF_SKIP_SIGNAL) ? (uint32_t)(p.L + 1) : 0u;
     const uint32_t ep = ver(p, l) - stale, ep_next = ver(p, l + 1) - stale;
@@ -1138,7 +1157,7 @@ __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, i
                 const float gte = y_of(0, rr, b), up = y_of(1, rr, b);
                 a = gte / (1.f + __expf(-gte)) * up;
             }
-            if (p.trace && ctid == 0) s.misc->t_x[0] = clock64() - c0;
+            if (TRACE(p) && ctid == 0) s.misc->t_x[0] = clock64() - c0;
             const float other = __shfl_down_sync(0xffffffffu, a, 1);
             if (j < items && q == 0)
                 st_ll(p.act + (((size_t)slot * p.Bmax + b) * p.I + t.r0 + 2 * pr) / 2, pack_bf2(a, other), ep);
@@ -1148,7 +1167,7 @@ __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, i
         for (int i = ctid; i < n * B; i += NCW * 32, ++k) {
             const int rr = i / B, b = i % B, row = t.r0 + rr;
             const float y0 = y_of(0, rr, b);
-            if (p.trace && ctid == 0 && k == 0) s.misc->t_x[0] = clock64() - c0;
+            if (TRACE(p) && ctid == 0 && k == 0) s.misc->t_x[0] = clock64() - c0;
             switch (t.op) {
             case OP_QKV: {
                 const int base = t.mat == MAT_Q ? 0 : t.mat == MAT_K ? p.nq * p.d : (p.nq + p.nkv) * p.d;
@@ -1171,10 +1190,10 @@ __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, i
             }
         }
     }
-    if (p.trace && ctid == 0) s.misc->t_x[1] = clock64() - c0;
+    if (TRACE(p) && ctid == 0) s.misc->t_x[1] = clock64() - c0;
     const bool ok = !cbar_or(s.misc->abort != 0);
-    if (p.trace && ctid == 0) s.misc->t_x[2] = clock64() - c0;
-    if (p.trace && ctid == 0) s.misc->t_epi = now_ns();
+    if (TRACE(p) && ctid == 0) s.misc->t_x[2] = clock64() - c0;
+    if (TRACE(p) && ctid == 0) s.misc->t_epi = now_ns();
     return ok;
 }
 
@@ -1205,19 +1224,19 @@ __device__ bool gemv_task_b1(const Params &p, Smem &s, const Task &t, int ti, Ri
     } else {
         copy_regs<I8, J>(p, s, p.act + (size_t)slot * p.Bmax * p.I / 2, cs, nch, hv, ver(p, l), ti, WB_ACT, lane);
     }
-    if (p.trace && ctid == 0) s.misc->t_pro = now_ns();
+    if (TRACE(p) && ctid == 0) s.misc->t_pro = now_ns();
     for (int rb = 0; rb < g.nrb; ++rb) {
         const int ra = t.r0 + rb * g.R, re = min(t.r1, ra + g.R);
         for (int m = 0; m < g.nmat; ++m, rg.advance(NS)) {
             const int sl = rg.slot;
-            const unsigned long long tw0 = p.trace ? now_ns() : 0;
+            const unsigned long long tw0 = TRACE(p) ? now_ns() : 0;
             if (!stage_ready(p, s, &s.full[sl], rg.pass & 1u, ti)) continue;
-            const unsigned long long tw1 = p.trace ? now_ns() : 0;
-            if (p.trace && rb == 0 && m == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
+            const unsigned long long tw1 = TRACE(p) ? now_ns() : 0;
+            if (TRACE(p) && rb == 0 && m == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
             float *res = s.res + (size_t)m * g.nrows + (ra - t.r0);
             gemv_stage_b1<I8, J>(s.ring + (size_t)sl * p.slot_bytes, re - ra, RG, rgp, rowc, cs, nch, hv, res,
                                  g.nmat * g.nrows, seg, lane);
-            if (p.trace && warp == 0 && lane == 0) {
+            if (TRACE(p) && warp == 0 && lane == 0) {
                 s.misc->t_wait_full += tw1 - tw0;
                 s.misc->t_tiles += now_ns() - tw1;
             }
@@ -1269,20 +1288,20 @@ __device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring 
             copy_prologue(p, s, p.act + (size_t)slot * p.Bmax * p.I / 2, p.I, k0, k1, ver(p, l), ti, WB_ACT, ctid);
         }
         if (cbar_or(s.misc->abort != 0)) return false;
-        if (p.trace && kp == 0 && ctid == 0) s.misc->t_pro = now_ns();
+        if (TRACE(p) && kp == 0 && ctid == 0) s.misc->t_pro = now_ns();
         for (int rb = 0; rb < g.nrb; ++rb) {
             const int ra = t.r0 + rb * g.R, re = min(t.r1, ra + g.R);
             for (int m = 0; m < g.nmat; ++m, rg.advance(NS)) {
                 const int sl = rg.slot;
-                const unsigned long long tw0 = p.trace ? now_ns() : 0;
+                const unsigned long long tw0 = TRACE(p) ? now_ns() : 0;
                 if (!stage_ready(p, s, &s.full[sl], rg.pass & 1u, ti)) continue;
-                const unsigned long long tw1 = p.trace ? now_ns() : 0;
-                if (p.trace && kp == 0 && rb == 0 && m == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
+                const unsigned long long tw1 = TRACE(p) ? now_ns() : 0;
+                if (TRACE(p) && kp == 0 && rb == 0 && m == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
                 float *res = s.res + ((size_t)m * g.nrows + (ra - t.r0)) * p.Bmax;
                 gemv_tile<I8, NB>(s.ring + (size_t)sl * p.slot_bytes, re - ra, S, g.Kc,
                                   reinterpret_cast<const uint32_t *>(s.act), p.batch, res, g.nmat * g.nrows, p.Bmax,
                                   kp == 0, warp, lane);
-                if (p.trace && warp == 0 && lane == 0) {
+                if (TRACE(p) && warp == 0 && lane == 0) {
                     s.misc->t_wait_full += tw1 - tw0;
                     s.misc->t_tiles += now_ns() - tw1;
                 }
@@ -1450,6 +1469,7 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
                 w[2 * u] = i < tot ? ld_ll1(src(i)) : 0ull;
                 w[2 * u + 1] = i < tot ? ld_ll1(src(i) + half) : 0ull;
             }
+
 #pragma unroll
             for (int u = 0; u < AU; ++u)
                 if (i0 + u * TS < tot) {
@@ -1478,7 +1498,7 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
         }
     }
     if (cbar_or(s.misc->abort != 0)) return false;
-    if (p.trace && ctid == 0) s.misc->t_pro = now_ns();
+    if (TRACE(p) && ctid == 0) s.misc->t_pro = now_ns();
     if (active_seq && (t.flags & TF_NEW_TOKEN)) {
         const size_t row = ((((size_t)l * p.Bmax + b) * p.nkv + grp) * p.Smax + ag.p) * d;
         for (int i = ctid; i < d; i += NCW * 32) {
@@ -1507,10 +1527,10 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
     bool new_done = false; /* warp-uniform */
     for (int k = 0; k < ag.ntile; ++k, rg.advance(NS)) {
         const int sl = rg.slot;
-        const unsigned long long tw0 = p.trace ? now_ns() : 0;
+        const unsigned long long tw0 = TRACE(p) ? now_ns() : 0;
         if (!stage_ready(p, s, &s.full[sl], rg.pass & 1u, ti)) continue;
-        const unsigned long long tw1 = p.trace ? now_ns() : 0;
-        if (p.trace && k == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
+        const unsigned long long tw1 = TRACE(p) ? now_ns() : 0;
+        if (TRACE(p) && k == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
         const int t0 = ag.s0 + k * t.rows_per_stage;
         const int nt = min(ag.e, t0 + (int)t.rows_per_stage) - t0;
         uint16_t *Kt = reinterpret_cast<uint16_t *>(s.ring + (size_t)sl * p.slot_bytes);
@@ -1534,7 +1554,7 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
             att_block<LP, GP>(st, Kt, Vt, j0, nb, d, sb, lane);
         }
         if (add_new) new_done = true;
-        if (p.trace && warp == 0 && lane == 0) {
+        if (TRACE(p) && warp == 0 && lane == 0) {
             s.misc->t_wait_full += tw1 - tw0;
             s.misc->t_tiles += now_ns() - tw1;
         }
@@ -1543,7 +1563,7 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
     }
     /* otherwise the new position on its own, from shared memory, on the last warp */
     if (with_new && !new_done && warp == NCW - 1) att_block<LP, GP>(st, as.knew, as.vnew, 0, 1, d, sb, lane);
-    if (p.trace && ctid == 0) s.misc->t_stages = now_ns();
+    if (TRACE(p) && ctid == 0) s.misc->t_stages = now_ns();
 
     /* the warp's state: o of every head, m and l of head lane (lane < GP) */
     {
@@ -1592,7 +1612,7 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
             st_ll(part + ((size_t)hh * p.C + t.r0) * (d + PART_PAD) + e, __float_as_uint(v), ep);
         }
     }
-    if (p.trace && ctid == 0) s.misc->t_epi = now_ns();
+    if (TRACE(p) && ctid == 0) s.misc->t_epi = now_ns();
     return !cbar_or(s.misc->abort != 0);
 }
 
@@ -1645,7 +1665,7 @@ __device__ bool mrg_task(const Params &p, Smem &s, const Task &t, int ti, int ct
             if (cl + k * NCL < C) mloc = fmaxf(mloc, ll_f(ml[k].x));
         }
         if (e4 == 0) mx[cl] = mloc;
-        if (p.trace && ctid == 0) s.misc->t_pro = now_ns();
+        if (TRACE(p) && ctid == 0) s.misc->t_pro = now_ns();
         cbar();
         float M = -INFINITY;
         for (int i = 0; i < NCL; ++i) M = fmaxf(M, mx[i]);
@@ -1666,7 +1686,7 @@ __device__ bool mrg_task(const Params &p, Smem &s, const Task &t, int ti, int ct
         *reinterpret_cast<float4 *>(num + (size_t)cl * d + 4 * e4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         if (e4 == 0) den[cl] = dl;
         cbar();
-        if (p.trace && ctid == 0) s.misc->t_stages = now_ns();
+        if (TRACE(p) && ctid == 0) s.misc->t_stages = now_ns();
         if (ctid < Q4) {
             float o[4] = {0.f, 0.f, 0.f, 0.f}, dd = 0.f;
             for (int i = 0; i < NCL; ++i) {
@@ -1684,7 +1704,7 @@ __device__ bool mrg_task(const Params &p, Smem &s, const Task &t, int ti, int ct
             st_ll(out + 1, pack_bf2(o[2] * inv, o[3] * inv), ep);
         }
     }
-    if (p.trace && ctid == 0) s.misc->t_epi = now_ns();
+    if (TRACE(p) && ctid == 0) s.misc->t_epi = now_ns();
     return !cbar_or(s.misc->abort != 0);
 }
 
@@ -1749,10 +1769,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p)
                     s.sc[i] = __ldg(op_scales(p, t, m) + t.r0 + rr);
                 }
             }
+#if AMK_L2_PREFETCH_CODE
             if (ctid == 0) s.misc->cons_op = t.op;
+#endif
             ResidPre rp;
             resid_prefetch(p, t, ctid, rp);
-            unsigned long long *tr = p.trace ? p.trace + 16 * (size_t)ti : nullptr;
+            unsigned long long *tr = TRACE(p) ? TRACE(p) + 16 * (size_t)ti : nullptr;
             if (tr && ctid == 0) {
                 tr[0] = tr[1] = now_ns();
                 s.misc->t_first = 0;
@@ -1797,6 +1819,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p)
 }
 
 /* ----------------------------------------------------------- host entry */
+
+bool kernel_has_trace() { return AMK_TRACE_CODE != 0; }
+bool kernel_has_l2_prefetch() { return AMK_L2_PREFETCH_CODE != 0; }
 
 KernelFn select_kernel(bool int8, int max_batch) {
     if (int8) return max_batch == 1 ? amk_decode_kernel<true, 1> : amk_decode_kernel<true, MAXB>;

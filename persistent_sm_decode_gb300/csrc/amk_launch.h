@@ -13,6 +13,10 @@ typedef void (*KernelFn)(const Params);
 KernelFn select_kernel(bool int8, int max_batch);
 cudaError_t prepare_kernel(KernelFn fn, int smem_bytes);
 cudaError_t occupancy(KernelFn fn, int smem_bytes, int *blocks_per_sm);
+/* whether this build's kernel carries the per-task timing code (trace
+ * option) and the loader's L2 prefetch (l2_prefetch_kb option) */
+bool kernel_has_trace();
+bool kernel_has_l2_prefetch();
 /* one cooperative launch of n_sm CTAs */
 cudaError_t launch_decode(KernelFn fn, const Params &p, int n_sm, int smem_bytes, cudaStream_t stream);
 }  // namespace amk
