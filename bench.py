@@ -114,6 +114,22 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x: float, dist, device: str) -> float:
+    """The largest x over all ranks (x itself without a process group): every
+    replica's timed region ends together only when the slowest one does."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, batch: int, steps: int, seconds: float) -> float:
+    """Tokens of every replica per second of the slowest one."""
+    return world * batch * steps / seconds
+
+
 def cpu_model() -> str:
     try:
         for ln in open("/proc/cpuinfo"):
@@ -279,12 +295,9 @@ def main():
     st = eng.sync()
     if st != amk.OK:
         raise amk.AmkError(st, "timed region: %s" % eng.last_error())
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, "cuda")
     ms_per_step = ms / args.steps
-    value = world * B * args.steps / (ms / 1e3)
+    value = whole_job_rate(world, B, args.steps, ms / 1e3)
 
     # ---- roofline of the (single) kernel ----
     positions = [wl.ctx + (i % window) for i in range(args.steps)]
@@ -321,12 +334,8 @@ def main():
             eng.step(t_in, p_in, kv, logits, stream=stream)
             out_pin.copy_(logits, non_blocking=True)
             stream.synchronize()   # the host needs the logits before it can pick the next token
-        dt = time.perf_counter() - t0
-        if dist:
-            t = torch.tensor([dt], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            dt = float(t.item())
-        e2e = {"value": world * B * n_e2e / dt, "unit": "tokens/s", "h2d_bytes_per_step": 2 * B * 4,
+        dt = max_over_ranks(time.perf_counter() - t0, dist, "cuda")
+        e2e = {"value": whole_job_rate(world, B, n_e2e, dt), "unit": "tokens/s", "h2d_bytes_per_step": 2 * B * 4,
                "d2h_bytes_per_step": B * wl.vocab * 4, "steps": n_e2e, "us_per_token": 1e6 * dt / (B * n_e2e)}
         assert eng.sync() == amk.OK
 
