@@ -227,9 +227,9 @@ amk_status amk_debug_read_residuals(const amk_handle *h, float *x_in, float *x_m
 /* Test and tuning support: per-task timings of the last step of a handle
  * created with options.trace = 1 (else AMK_ERR_UNSUPPORTED).  For every task
  * of every CTA, in CTA order then task order, sixteen uint64 entries:
- * globaltimer times (ns) [0] task start, [1] dependency met, [2] first tile
- * arrived, [3] end (after the completion signal), [6] prologue done (GEMV),
- * [7] last tile consumed (GEMV), [8] epilogue written (GEMV); durations (ns)
+ * globaltimer times (ns) [0] task start ([1] repeats it), [2] first tile
+ * arrived, [3] end (after the completion signal), [6] inputs met and
+ * prologue done, [7] last tile consumed, [8] epilogue written; durations (ns)
  * [4] consumer warp 0 waiting for tiles, [5] consumer warp 0 computing tiles,
  * [9] the loader waiting for free ring slots while issuing the task's tiles;
  * other entries are unused (0).  `out` holds n_tasks * 16 entries (n_tasks

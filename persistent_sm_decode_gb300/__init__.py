@@ -18,7 +18,8 @@ from typing import Dict, List, Optional, Sequence
 
 from . import _build
 
-__all__ = ["AmkError", "Config", "ScheduleOptions", "DecodeEngine", "Plan", "lib", "build",
+__all__ = ["AmkError", "Config", "ScheduleOptions", "DecodeEngine", "Plan", "lib", "build", "chrome_trace",
+           "level_times",
            "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_OOM", "ERR_SCHEDULE",
            "ERR_COOPERATIVE", "ERR_TIMEOUT", "WEIGHT_BF16", "WEIGHT_INT8"]
 
@@ -295,6 +296,65 @@ class DecodeEngine:
             self.close()
         except Exception:
             pass
+
+
+def chrome_trace(trace, plan: "Plan") -> dict:
+    """Chrome trace-event JSON (chrome://tracing, ui.perfetto.dev) of one
+    traced decode step: one track per CTA, one slice per task, with its
+    inputs-and-prologue, tiles and epilogue nested inside; times in µs from
+    the first task's start.
+
+    ``trace`` is ``DecodeEngine.read_trace()`` of a handle created with
+    ``options={"trace": 1}`` on the AMK_TRACE=1 build; ``plan`` is the host
+    ``Plan`` of the same configuration, batch (the config's max_batch), CTA
+    count and options.  The planner is deterministic, so its task tables are
+    the handle's, row for row."""
+    rows = iter(trace)
+    t0 = min((int(r[0]) for r in trace if int(r[0]) > 0), default=0)
+    us = lambda t: (int(t) - t0) / 1e3
+    ev = [{"name": "process_name", "ph": "M", "pid": 0, "args": {"name": "amk_decode_kernel"}}]
+    for sm in range(plan.n_sm):
+        ev.append({"name": "thread_name", "ph": "M", "pid": 0, "tid": sm, "args": {"name": "CTA %d" % sm}})
+        for t in plan.tasks(sm):
+            r = next(rows)
+            start, end = int(r[0]), int(r[3])
+            if start == 0 or end < start:
+                continue
+            name = "%s L%d" % (t["op"], t["layer"]) + (" c%d" % t["r0"] if t["op"] == "ATT" else "")
+            ev.append({"name": name, "ph": "X", "pid": 0, "tid": sm, "ts": us(start), "dur": (end - start) / 1e3,
+                       "args": {"rows": [t["r0"], t["r1"]], "seq": t["b"], "head": t["g"],
+                                "tile_wait_us": int(r[4]) / 1e3, "tile_us": int(r[5]) / 1e3,
+                                "loader_wait_us": int(r[9]) / 1e3}})
+            pro, last, epi = int(r[6]), int(r[7]), int(r[8])
+            for part, a, b in (("inputs + prologue", start, pro), ("tiles", pro, last), ("epilogue", last, epi)):
+                if a >= start and b >= a and b <= end and a > 0:
+                    ev.append({"name": part, "ph": "X", "pid": 0, "tid": sm, "ts": us(a), "dur": (b - a) / 1e3})
+    return {"traceEvents": ev, "displayTimeUnit": "ns"}
+
+
+def level_times(trace, plan: "Plan") -> List[dict]:
+    """Per dependency level of a traced step, in program order: the level's
+    last task end, and its time from the previous level's last task end
+    (the critical-path share of that level).  Arguments as for chrome_trace."""
+    rows = iter(trace)
+    ends: Dict[tuple, int] = {}
+    starts: Dict[tuple, int] = {}
+    for sm in range(plan.n_sm):
+        for t in plan.tasks(sm):
+            r = next(rows)
+            if int(r[0]) == 0:
+                continue
+            key = (t["layer"], t["op"])
+            ends[key] = max(ends.get(key, 0), int(r[3]))
+            starts[key] = min(starts.get(key, 1 << 63), int(r[0]))
+    order = {op: i for i, op in enumerate(("QKV", "ATT", "MRG", "OPR", "GUP", "DWN", "LMH"))}
+    keys = sorted(ends, key=lambda k: (k[0] + (1 if k[1] == "LMH" else 0), order[k[1]]))
+    out, prev = [], None
+    for k in keys:
+        base = prev if prev is not None else starts[k]
+        out.append({"layer": k[0], "op": k[1], "end_ns": ends[k], "level_us": (ends[k] - base) / 1e3})
+        prev = ends[k]
+    return out
 
 
 def decode_step_noalloc(cfg: Config, embed, final_norm, layers: Sequence[Dict], tokens, positions, kv_cache,
