@@ -140,11 +140,19 @@ def cpu_model() -> str:
     return "unknown"
 
 
-def time_oracle(model, kc, vc, wl, budget_s: float, max_steps: int):
-    """The oracle as it stands on the host cores: decode steps of the workload
-    until the budget or max_steps is reached.  Returns (tokens/s, steps, threads)."""
+def time_oracle(model, kc, vc, wl, budget_s: float, max_steps: int, threads: int = 0):
+    """The oracle as it stands on the host cores (``threads`` of them, 0: all):
+    decode steps of the workload until the budget or max_steps is reached.
+    Returns (tokens/s, steps, threads, seconds)."""
     import numpy as np
     import oracle
+    if threads:
+        every = oracle.num_threads()
+        oracle.set_num_threads(threads)
+        try:
+            return time_oracle(model, kc, vc, wl, budget_s, max_steps)
+        finally:
+            oracle.set_num_threads(every)
     orc = oracle.Oracle(model, kc, vc)
     B = kc.shape[1]
     tok = np.array([(1 + 7919 * b) % wl.vocab for b in range(B)], dtype=np.int32)
@@ -342,8 +350,12 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tps, n, threads, dt = time_oracle(model, kc, vc, wl, budget_s=15.0, max_steps=10 ** 6)
+        tps1, n1, _, dt1 = time_oracle(model, kc, vc, wl, budget_s=5.0, max_steps=10 ** 6, threads=1)
         cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": "%d decode steps of %s (%.1f s) on %s" % (n, wl.name, dt, cpu_model())}
+               "sample": "%d decode steps of %s (%.1f s) on %s" % (n, wl.name, dt, cpu_model()),
+               "us_per_token": 1e6 / tps,
+               "single_thread": {"value": tps1, "unit": "tokens/s", "us_per_token": 1e6 / tps1,
+                                 "sample": "%d decode steps (%.1f s) on one core" % (n1, dt1)}}
 
     plan = eng.plan_info()
     if rank == 0:
