@@ -278,8 +278,11 @@ class DecodeEngine:
         return xi, xm
 
     def read_trace(self):
-        """[n_tasks][16] timestamps and durations (ns) of the last step (needs
-        options={"trace": 1}), tasks in CTA order; see amk_debug_read_trace."""
+        """[n_tasks][16] timestamps and durations (ns) of the last step, tasks
+        in CTA order; see amk_debug_read_trace.  Needs a handle created with
+        options={"trace": 1} on the library built with AMK_TRACE=1 (the
+        default build leaves the timing code out and refuses the option).
+        chrome_trace and level_times turn the result into a timeline."""
         import numpy as np
         n = self.plan_info()["n_tasks"]
         out = np.zeros((n, 16), dtype=np.uint64)
