@@ -46,7 +46,11 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     stamp = os.path.join(OBJ, "flags.txt")
     prev = open(stamp).read() if os.path.exists(stamp) else None
     if prev != " ".join(flags):
+        # objects of other flags may be left behind: rebuild everything, and
+        # keep no stamp until the whole build has succeeded
         force = True
+        if prev is not None:
+            os.remove(stamp)
     common = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC] + flags
     procs, objs = [], []
     for src in SOURCES:
