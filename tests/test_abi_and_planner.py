@@ -79,6 +79,20 @@ def test_schedule_options_reach_the_planner(amk):
     assert on.info()["l2_evict_first"] == 1 and on.info()["att_chunks"] == 3
 
 
+def test_default_build_refuses_the_trace_option(amk):
+    # the default library carries no per-task timing code; amk_create says so
+    # before it touches the device (AMK_TRACE=1 builds the tuning variant)
+    import ctypes
+    import os
+    if os.environ.get("AMK_TRACE", "0") not in ("", "0"):
+        pytest.skip("timing build")
+    wl = synth.workload("tiny")
+    h = ctypes.c_void_p()
+    opts = amk.ScheduleOptions(trace=1)
+    st = amk.lib().amk_create(ctypes.byref(_cfg(amk, wl)), None, ctypes.byref(opts), ctypes.byref(h))
+    assert st == amk.ERR_UNSUPPORTED and not h.value
+
+
 def test_headline_schedule_is_the_measured_best_point(amk):
     # the 1.1B bf16 shape on 152 CTAs: the point the slot and chunk sweeps
     # measured fastest on GB300; a cost-model change that moves it needs a
