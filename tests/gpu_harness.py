@@ -43,9 +43,19 @@ class Result:
         self.steps = 0
         self.records = []         # (step, row, margin, gpu agrees, fp32-build max|dlogit| or None)
 
+    @property
+    def free_running(self) -> int:
+        """Steps over which the GPU's own greedy stream equals the oracle's for
+        every checked sequence: up to the first step where an argmax differs.
+        Until then teacher forcing feeds both sides the tokens a free-running
+        decode would, so no second run is needed."""
+        first = [s for (s, _b, _m, agree, _f) in self.records if not agree]
+        return min(first) if first else self.steps
+
     def __repr__(self):
-        return ("Result(worst=%.3g, floor=%.3g, max_abs=%.3g, argmax %d/%d, steps=%d)"
-                % (self.worst, self.floor, self.max_abs, self.argmax_agree, self.checked_argmax, self.steps))
+        return ("Result(worst=%.3g, floor=%.3g, max_abs=%.3g, argmax %d/%d, steps=%d, free-running %d)"
+                % (self.worst, self.floor, self.max_abs, self.argmax_agree, self.checked_argmax, self.steps,
+                   self.free_running))
 
 
 def teacher_forced(wl, model=None, kv=None, steps=None, options=None, batch=None, positions0=None,
