@@ -60,8 +60,77 @@ def step_bytes(wl, position: int, batch: int) -> int:
     return wl.weight_bytes() + batch * wl.hidden * 2 + kv + batch * wl.vocab * 4
 
 
+class NvmlClockSampler:
+    """SM clock and clock-event (throttle) reasons of one GPU, read through
+    NVML every millisecond or so on a host thread while the timed region
+    runs: a decode step takes well under a millisecond, so nvidia-smi's
+    sampling interval would see a whole timed region at most once.  Only
+    reads; no GPU setting is changed."""
+    # nvmlClocksEventReasons bits (nvml.h): sw power cap, hw slowdown, sw thermal, hw thermal
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            import ctypes
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            # CUDA's ordinal and NVML's index differ under CUDA_VISIBLE_DEVICES: find the GPU by the
+            # PCI address of the CUDA device
+            import torch
+            pr = torch.cuda.get_device_properties(gpu_index)
+            bus = None
+            if all(hasattr(pr, a) for a in ("pci_domain_id", "pci_bus_id", "pci_device_id")):
+                bus = "%08X:%02X:%02X.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+            if bus is None or self.nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)) != 0:
+                vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+                idx = int(vis.split(",")[gpu_index]) if vis and all(
+                    x.strip().isdigit() for x in vis.split(",")) else gpu_index
+                if self.nv.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(self.h)) != 0:
+                    return
+            self.c_uint, self.c_ull, self.byref = ctypes.c_uint, ctypes.c_ulonglong, ctypes.byref
+            mx = ctypes.c_uint()
+            self.max_mhz = float(mx.value) if self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0 \
+                else None
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _read(self):
+        while not self._stop.is_set():
+            clk, rs = self.c_uint(), self.c_ull()
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, self.byref(clk)) == 0 and \
+                    self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, self.byref(rs)) == 0:
+                self.samples.append((float(clk.value), int(rs.value)))
+            time.sleep(0.001)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        if not self.samples:
+            return None
+        reasons = sorted({name for _c, r in self.samples for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(c for c, _r in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples), "source": "nvml"}
+
+
 class ClockSampler:
-    """nvidia-smi samples of the GPU clocks and throttle reasons while running."""
+    """nvidia-smi samples of the GPU clocks and throttle reasons while running
+    (the fallback where NVML cannot be loaded)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -212,6 +281,162 @@ def config_block(wl):
             "l2": "weights %.2f GB per step > 129 MB L2: no flush needed" % (wl.weight_bytes() / 1e9)}
 
 
+def workload_dtype(wl) -> str:
+    """The arithmetic the path computes in: bf16 products with fp32 sums, or
+    int8 weights times bf16 activations (W8A16) with fp32 sums."""
+    return "int8xbf16" if wl.weight_dtype == "int8" else "bf16"
+
+
+def device_model(wl, seed: int):
+    """Weights of a workload's shape filled on the device by torch's seeded
+    generator, with the synthetic recipe's distributions (bf16 N(0, 0.02);
+    int8 uniform on [-127, 127] with row scales 0.02/127; norm gains 1.0).
+    Only the timing sub-records use these: the decode step's time does not
+    depend on the values, and drawing a 7B-shaped model on the host takes a
+    minute.  Parity tests always use the host generator's bits."""
+    import torch
+    from synth import mat_shapes
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    H, V = wl.hidden, wl.vocab
+
+    def mat(shape):
+        if wl.weight_dtype == "int8":
+            q = torch.randint(-127, 128, shape, generator=g, device="cuda", dtype=torch.int8)
+            return q, torch.full((shape[0],), wl.weight_std / 127.0, device="cuda", dtype=torch.float32)
+        return (torch.randn(shape, generator=g, device="cuda") * wl.weight_std).to(torch.bfloat16), None
+
+    ones = torch.ones(H, dtype=torch.bfloat16, device="cuda")
+    keys = {"wq": "s_q", "wk": "s_k", "wv": "s_v", "wo": "s_o", "w_gate": "s_gate", "w_up": "s_up",
+            "w_down": "s_down"}
+    layers = []
+    for _ in range(wl.n_layers):
+        d = {"attn_norm": ones.clone(), "mlp_norm": ones.clone()}
+        for m, shape in mat_shapes(wl).items():
+            q, sc = mat(shape)
+            d[m] = q
+            if sc is not None:
+                d[keys[m]] = sc
+        layers.append(d)
+    embed = (torch.randn((V, H), generator=g, device="cuda") * wl.weight_std).to(torch.bfloat16)
+    lm, s_lm = (None, None) if wl.tied else mat((V, H))
+    return {"embed": embed, "final_norm": ones.clone(), "layers": layers, "lm_head": lm, "s_lm": s_lm}
+
+
+def device_kv(wl, seed: int, batch: int):
+    """K then V cache [2][L][B][nkv][Smax][d] bf16 on the device: N(0, 1) at
+    the positions below the workload's context, zero above (timing only)."""
+    import torch
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    kv = torch.zeros((2, wl.n_layers, batch, wl.n_kv_heads, wl.max_seq, wl.head_dim), dtype=torch.bfloat16,
+                     device="cuda")
+    for l in range(wl.n_layers):
+        kv[:, l, :, :, : wl.ctx] = torch.randn((2, batch, wl.n_kv_heads, wl.ctx, wl.head_dim), generator=g,
+                                              device="cuda").to(torch.bfloat16)
+    return kv
+
+
+def make_engine(amk, wl, dev, opts):
+    cfg = amk.make_config(wl.n_layers, wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.intermediate,
+                          wl.vocab, wl.max_seq, wl.batch, wl.rms_eps, wl.rope_theta,
+                          int8=wl.weight_dtype == "int8", tied=wl.tied)
+    return amk.DecodeEngine(cfg, dev["embed"], dev["final_norm"], dev["layers"], dev["lm_head"], dev["s_lm"],
+                            opts or None)
+
+
+class Timed:
+    """One device-timed run of `steps` decode steps (one launch each) after
+    `warmup` untimed ones, inputs resident in HBM.  The positions walk the
+    workload's decode window from its context length and wrap around it."""
+
+    def __init__(self, amk, eng, wl, kv, steps, warmup, local, dist=None):
+        import numpy as np
+        import torch
+        B, window = wl.batch, wl.steps
+        self.wl, self.steps, self.window = wl, steps, window
+        stream = torch.cuda.current_stream()
+        rng = np.random.default_rng(3)
+        self.tok_host = rng.integers(0, wl.vocab, size=(window, B)).astype(np.int32)
+        self.pos_host = np.ascontiguousarray((wl.ctx + np.arange(window, dtype=np.int32))[:, None].repeat(B, axis=1))
+        tok_dev = torch.from_numpy(self.tok_host).cuda()
+        pos_dev = torch.from_numpy(self.pos_host).cuda()
+        self.logits = torch.empty((B, wl.vocab), dtype=torch.float32, device="cuda")
+        h, lib, s_ptr = eng.handle, amk.lib(), stream.cuda_stream
+
+        def launch(i):
+            j = i % window
+            st = lib.amk_decode_step(h, B, tok_dev[j].data_ptr(), pos_dev[j].data_ptr(), kv.data_ptr(),
+                                     self.logits.data_ptr(), s_ptr)
+            if st != amk.OK:
+                raise amk.AmkError(st, "amk_decode_step")
+
+        for i in range(warmup):
+            launch(i)
+        st = eng.sync()
+        if st != amk.OK:
+            raise amk.AmkError(st, "warm-up: %s" % eng.last_error())
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sampler = NvmlClockSampler(local)
+        if not sampler.ok:
+            sampler = ClockSampler(local)
+        with sampler as clocks:
+            ev0.record(stream)
+            for i in range(steps):
+                launch(i)
+            ev1.record(stream)
+            torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1)
+        st = eng.sync()
+        if st != amk.OK:
+            raise amk.AmkError(st, "timed region: %s" % eng.last_error())
+        self.ms = max_over_ranks(ms, dist, "cuda")
+        self.ms_per_step = self.ms / steps
+        self.clocks = clocks.summary()
+
+    def roofline(self, traffic):
+        wl, B = self.wl, self.wl.batch
+        positions = [wl.ctx + (i % self.window) for i in range(self.steps)]
+        alg = statistics.fmean(step_bytes(wl, p, B) for p in positions)
+        peak, src = measured_peak()
+        achieved = alg / (self.ms_per_step / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic, "peak_source": src, "algorithmic_bytes_per_launch": alg,
+                "frac_of_8TBps": achieved / NOMINAL_HBM_GBS, "kernel": "amk_decode_kernel"}
+
+
+SUB_WORKLOADS = ("tinyllama_1b1_w8a16", "llama2_7b", "llama2_7b_b8", "smollm2_135m")
+
+
+def sub_records(amk, args, local):
+    """The other targeted shapes on the same kernel, a few seconds each, with
+    device-filled weights (device_model)."""
+    import synth
+    import torch
+    out = {}
+    for name in args.sub:
+        wl = synth.workload(name)
+        dev = device_model(wl, seed=1)
+        kv = device_kv(wl, seed=2, batch=wl.batch)
+        eng = make_engine(amk, wl, dev, None)
+        steps = max(16, min(args.sub_steps, int(0.5e6 / max(1.0, 50.0 * wl.n_layers * wl.batch))))
+        t = Timed(amk, eng, wl, kv, steps=steps, warmup=8, local=local)
+        plan = eng.plan_info()
+        out[name] = {"ms_per_step": t.ms_per_step, "us_per_token": 1e3 * t.ms_per_step / wl.batch,
+                     "tokens_per_s": wl.batch / (t.ms_per_step / 1e3), "steps": steps, "warmup": 8,
+                     "dtype": workload_dtype(wl), "config": config_block(wl), "clocks": t.clocks,
+                     "roofline": t.roofline(traffic_from_profile(wl.name)),
+                     "data": "synthetic, weights and KV filled on the device by torch's seeded generator",
+                     "schedule": {k: plan[k] for k in ("att_chunks", "slot_bytes", "n_slots", "ksplit")}}
+        eng.close()
+        del dev, kv, eng
+        torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -221,10 +446,14 @@ def main():
     ap.add_argument("--impl", default="amk", choices=["amk", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sub", default=",".join(SUB_WORKLOADS),
+                    help="comma-separated workloads timed as sub-records beside the headline ('' for none)")
+    ap.add_argument("--sub-steps", type=int, default=512)
     ap.add_argument("--option", action="append", default=[], help="schedule option key=value (offline tuning)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    args.sub = [x for x in args.sub.split(",") if x]
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -256,75 +485,25 @@ def main():
     for kvp in args.option:
         k, v = kvp.split("=")
         opts[k] = int(v)
-    cfg = amk.make_config(wl.n_layers, wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.intermediate,
-                          wl.vocab, wl.max_seq, wl.batch, wl.rms_eps, wl.rope_theta,
-                          int8=wl.weight_dtype == "int8", tied=wl.tied)
-    eng = amk.DecodeEngine(cfg, dev["embed"], dev["final_norm"], dev["layers"], dev["lm_head"], dev["s_lm"],
-                           opts or None)
+    eng = make_engine(amk, wl, dev, opts)
     B = wl.batch
     stream = torch.cuda.current_stream()
-    window = wl.steps
-    # token and position streams, resident on the device
-    rng = np.random.default_rng(3)
-    tok_host = rng.integers(0, wl.vocab, size=(window, B)).astype(np.int32)
-    pos_host = (wl.ctx + np.arange(window, dtype=np.int32))[:, None].repeat(B, axis=1)
-    tok_dev = torch.from_numpy(tok_host).cuda()
-    pos_dev = torch.from_numpy(np.ascontiguousarray(pos_host)).cuda()
-    logits = torch.empty((B, wl.vocab), dtype=torch.float32, device="cuda")
-    h = eng.handle
-    lib = amk.lib()
-    s_ptr = stream.cuda_stream
-
-    def launch(i):
-        j = i % window
-        st = lib.amk_decode_step(h, B, tok_dev[j].data_ptr(), pos_dev[j].data_ptr(), kv.data_ptr(),
-                                 logits.data_ptr(), s_ptr)
-        if st != amk.OK:
-            raise amk.AmkError(st, "amk_decode_step")
-
-    for i in range(args.warmup):
-        launch(i)
-    st = eng.sync()
-    if st != amk.OK:
-        raise amk.AmkError(st, "warm-up: %s" % eng.last_error())
 
     # ---- device-timed region: inputs resident, one launch per step ----
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
-        ev0.record(stream)
-        for i in range(args.steps):
-            launch(i)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-    ms = ev0.elapsed_time(ev1)
-    st = eng.sync()
-    if st != amk.OK:
-        raise amk.AmkError(st, "timed region: %s" % eng.last_error())
-    ms = max_over_ranks(ms, dist, "cuda")
-    ms_per_step = ms / args.steps
-    value = whole_job_rate(world, B, args.steps, ms / 1e3)
-
-    # ---- roofline of the (single) kernel ----
-    positions = [wl.ctx + (i % window) for i in range(args.steps)]
-    alg_bytes = statistics.fmean(step_bytes(wl, p, B) for p in positions)
-    peak, peak_src = measured_peak()
-    achieved = alg_bytes / (ms_per_step / 1e3) / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": traffic_from_profile(wl.name), "peak_source": peak_src,
-                "algorithmic_bytes_per_launch": alg_bytes,
-                "frac_of_8TBps": achieved / NOMINAL_HBM_GBS, "kernel": "amk_decode_kernel"}
+    t = Timed(amk, eng, wl, kv, args.steps, args.warmup, local, dist)
+    value = whole_job_rate(world, B, args.steps, t.ms / 1e3)
+    roofline = t.roofline(traffic_from_profile(wl.name))
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
-        tok_pin = torch.from_numpy(tok_host).pin_memory()
-        pos_pin = torch.from_numpy(np.ascontiguousarray(pos_host)).pin_memory()
+        window = wl.steps
+        tok_pin = torch.from_numpy(t.tok_host).pin_memory()
+        pos_pin = torch.from_numpy(t.pos_host).pin_memory()
         out_pin = torch.empty((B, wl.vocab), dtype=torch.float32).pin_memory()
         t_in = torch.empty((B,), dtype=torch.int32, device="cuda")
         p_in = torch.empty((B,), dtype=torch.int32, device="cuda")
+        logits = t.logits
         n_e2e = min(args.steps, 512)
         for i in range(8):
             t_in.copy_(tok_pin[i % window], non_blocking=True)
@@ -347,6 +526,13 @@ def main():
                "d2h_bytes_per_step": B * wl.vocab * 4, "steps": n_e2e, "us_per_token": 1e6 * dt / (B * n_e2e)}
         assert eng.sync() == amk.OK
 
+    plan = eng.plan_info()
+    eng.close()
+    del dev, kv
+    torch.cuda.empty_cache()
+
+    subs = sub_records(amk, args, local) if (rank == 0 and world == 1 and args.sub) else None
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tps, n, threads, dt = time_oracle(model, kc, vc, wl, budget_s=15.0, max_steps=10 ** 6)
@@ -357,18 +543,17 @@ def main():
                "single_thread": {"value": tps1, "unit": "tokens/s", "us_per_token": 1e6 / tps1,
                                  "sample": "%d decode steps (%.1f s) on one core" % (n1, dt1)}}
 
-    plan = eng.plan_info()
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_token": 1e3 * ms_per_step / B,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "warmup": args.warmup, "ms_per_step": t.ms_per_step, "us_per_token": 1e3 * t.ms_per_step / B,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": workload_dtype(wl),
                 "data": "synthetic", "config": config_block(wl),
-                "clocks": clocks.summary(), "e2e": e2e, "gpu_launches": args.steps,
+                "clocks": t.clocks, "e2e": e2e, "gpu_launches": args.steps,
                 "roofline": roofline, "cpu_baseline": cpu,
                 "schedule": {k: plan[k] for k in ("n_sm", "att_chunks", "slot_bytes", "n_slots", "ksplit",
-                                                  "scratch_depth", "smem_bytes", "n_tasks")}}
+                                                  "scratch_depth", "smem_bytes", "n_tasks")},
+                "kernel_sha": kernel_hash(), "workloads": subs}
         print(json.dumps(line), flush=True)
-    eng.close()
     if dist:
         dist.destroy_process_group()
     return 0

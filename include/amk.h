@@ -165,9 +165,16 @@ amk_status amk_decode_step(amk_handle *h, int32_t batch, const int32_t *tokens,
  *     AMK_ERR_UNSUPPORTED (the needed size is printed to stderr).
  *   - tokens, positions, kv_cache, logits and stream are as in
  *     amk_decode_step.  The call waits for the step to finish and returns
- *     AMK_ERR_TIMEOUT or AMK_ERR_INVALID_ARG for a device-side failure.
+ *     AMK_ERR_TIMEOUT or AMK_ERR_INVALID_ARG for a device-side failure
+ *     (AMK_ERR_CUDA if the error word then cannot be cleared).  It runs the
+ *     same kernel on the same default schedule as a handle created with
+ *     options = NULL, so its logits and K/V slots are bit-identical to
+ *     amk_decode_step's on the same inputs.
  *   - All calls share the array: calls are serialised by a process-wide lock;
- *     calls that overlapped on the GPU would race. */
+ *     calls that overlapped on the GPU would race.  A call blocks on `stream`
+ *     (cudaStreamSynchronize) while it holds that lock, so it must not be
+ *     made from a stream callback or host function, nor while `stream` waits
+ *     on work that another thread's call would enqueue. */
 amk_status amk_decode_step_noalloc(const amk_config *config, const amk_weights *weights,
                                    int32_t batch, const int32_t *tokens,
                                    const int32_t *positions, void *kv_cache,
@@ -186,12 +193,16 @@ const char *amk_status_string(amk_status s);
 
 /* What the last failed wait saw (filled by amk_sync_status on a timeout). */
 typedef struct amk_error_info {
-    int32_t code;        /* 1 dependency counter, 2 ring full barrier, 3 ring empty barrier */
+    int32_t code;        /* 1 dependency (an activation word never became current), 2 ring full barrier,
+                            3 ring empty barrier, 4 out-of-range token or position */
     int32_t sm;          /* CTA that gave up */
-    int32_t task;        /* index of its task in that CTA's list */
-    int32_t counter;     /* counter index for code 1, else -1 */
-    uint32_t observed;   /* counter value seen */
-    uint32_t target;     /* value awaited */
+    int32_t task;        /* index of its task in that CTA's list (-1: none) */
+    int32_t counter;     /* code 1: which activation buffer the wait polled: 0 residual at a layer's input,
+                            1 residual after attention, 2 q/k/v, 3 attention chunk partials, 4 attention
+                            output, 5 SwiGLU output; else -1 */
+    uint32_t observed;   /* code 1: the epoch flag the stale word carried; codes 2, 3: 0 */
+    uint32_t target;     /* code 1: the flag awaited (epoch * (n_layers + 1) + layer); codes 2, 3: the
+                            barrier phase parity awaited */
 } amk_error_info;
 amk_status amk_last_error(const amk_handle *h, amk_error_info *info);
 

@@ -48,18 +48,24 @@ amk_status amk_plan_validate(const amk_plan *plan, char *msg, size_t msg_len);
 amk_status amk_plan_get_info(const amk_plan *plan, amk_plan_info *info);
 
 /* Number of tasks of CTA `sm`, and one task's fields:
- * out[0] op (0 QKV, 1 ATT, 2 OPR, 3 GUP, 4 DWN, 5 LMH), [1] layer, [2] r0, [3] r1,
- * [4] batch row, [5] kv head, [6] wait counter (-1 none), [7] wait count per step,
- * [8] number of signalled counters, [9..14] signalled counters. */
+ * out[0] op (0 QKV, 1 ATT, 2 OPR, 3 GUP, 4 DWN, 5 LMH, 6 MRG), [1] layer, [2] r0, [3] r1,
+ * [4] batch row, [5] kv head (MRG: query head), [6] the dependency the task waits on
+ * (-1 none), [7] its number of producer tasks, [8] number of dependencies the task
+ * produces for, [9..14] those dependencies, [15] QKV matrix (0 q, 1 k, 2 v).
+ * A dependency is an id of the schedule graph that the validator checks: its
+ * producers write a region of one activation buffer and its waiters read it.
+ * The kernel keeps no counter for it: every word of the region carries the
+ * epoch flag of the step and layer that wrote it, and a waiter polls the words
+ * it reads until they carry the flag it expects. */
 int32_t amk_plan_num_tasks(const amk_plan *plan, int32_t sm);
 amk_status amk_plan_get_task(const amk_plan *plan, int32_t sm, int32_t idx, int32_t out[16]);
 
 /* Adversarial mutation for validator tests.  kind:
- *   0 drop one signal (a counter loses a producer)
+ *   0 drop one signal (a dependency loses a producer)
  *   1 lower one wait count (a consumer may start before all producers)
  *   2 remove one wait (a consumer ignores its producers)
  *   3 move a consumer task in front of a producer on the same CTA (deadlock)
- *   4 redirect a wait to an unrelated counter
+ *   4 redirect a wait to an unrelated dependency
  *   5 raise one wait count (a wait that can never be met)
  * `seed` picks the victim deterministically.  AMK_OK if a mutation was applied. */
 amk_status amk_plan_mutate(amk_plan *plan, int32_t kind, uint64_t seed);

@@ -21,7 +21,10 @@
  * All calls on a device share the array, so two calls that overlapped on the
  * GPU would race on it.  To keep that from happening inside one process, each
  * call holds a process-wide lock and waits for its own step to finish before
- * it returns (which is also how it reports a device-side timeout).
+ * it returns (which is also how it reports a device-side timeout).  The wait
+ * is a cudaStreamSynchronize on the caller's stream made while the lock is
+ * held: do not call this from a stream callback or host function, nor while
+ * the caller's stream waits on work that another thread's call enqueues.
  */
 #include <cuda_runtime.h>
 
@@ -169,17 +172,24 @@ amk_status upload(DeviceState &ds, const amk_config *c, const amk_weights *w, in
         ds.plan = nullptr;
         return AMK_ERR_UNSUPPORTED;
     }
+    /* from here on every failure also drops the plan, so that a later call
+     * plans again instead of running a half-uploaded schedule */
+    auto drop = [&](amk_status why) {
+        amk_plan_destroy(ds.plan);
+        ds.plan = nullptr;
+        return why;
+    };
     ds.fn = select_kernel(c->weight_dtype == AMK_WEIGHT_INT8, c->max_batch);
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, (const void *)ds.fn) != cudaSuccess ||
         prepare_kernel(ds.fn, P.smem_bytes) != cudaSuccess) {
         cudaGetLastError();
-        return AMK_ERR_UNSUPPORTED;
+        return drop(AMK_ERR_UNSUPPORTED);
     }
     int per_sm = 0;
     if (occupancy(ds.fn, P.smem_bytes, &per_sm) != cudaSuccess || per_sm < 1) {
         cudaGetLastError();
-        return AMK_ERR_COOPERATIVE;
+        return drop(AMK_ERR_COOPERATIVE);
     }
     cudaError_t e = cudaMemset(ds.base, 0, off);
     if (e == cudaSuccess) e = cudaMemcpy(ds.base + o_tasks, tasks.data(), sizeof(Task) * tasks.size(), cudaMemcpyHostToDevice);
@@ -187,7 +197,7 @@ amk_status upload(DeviceState &ds, const amk_config *c, const amk_weights *w, in
     if (e == cudaSuccess) e = cudaMemcpy(ds.base + o_layers, lp.data(), sizeof(LayerPtrs) * L, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(ds.base + o_rope, rope.data(), sizeof(float) * rope.size(), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return fail(e);
+    if (e != cudaSuccess) return drop(fail(e));
 
     Params &p = ds.params;
     std::memset(&p, 0, sizeof p);
@@ -296,7 +306,10 @@ extern "C" amk_status amk_decode_step_noalloc(const amk_config *config, const am
     p.epoch_base = p.epoch * (uint32_t)(config->n_layers + 1);
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = launch_decode(ds.fn, p, ds.plan->n_sm, ds.plan->smem_bytes, s);
-    if (e != cudaSuccess) return fail(e);
+    if (e != cudaSuccess) {
+        --ds.epoch; /* nothing ran under this epoch */
+        return fail(e);
+    }
     /* synchronous: report a device-side timeout or bad input of this step */
     e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return fail(e);
@@ -304,8 +317,11 @@ extern "C" amk_status amk_decode_step_noalloc(const amk_config *config, const am
     e = cudaMemcpy(err, p.err, sizeof err, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return fail(e);
     if (err[0] != 0) {
-        cudaMemset(p.err, 0, sizeof err);
-        cudaDeviceSynchronize();
+        /* a step that sees a set error word does nothing, so the word must be
+         * clear before the next call; if clearing fails, say so */
+        e = cudaMemset(p.err, 0, sizeof err);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return fail(e);
         return err[0] == 4 ? AMK_ERR_INVALID_ARG : AMK_ERR_TIMEOUT;
     }
     return AMK_OK;
