@@ -113,39 +113,51 @@ struct Params {
     unsigned long long *trace; /* NULL, or [n_tasks][16] timings */
 };
 
-/* Batch-1 GEMV.  A row of a task's K slice is cut into S segments; consumer
- * warp w owns segment w % S and keeps that segment's activations in
- * registers for the whole task: J 16-byte chunks per lane (chunk c of the
- * segment sits in lane c % 32, slot c / 32).  Warps w / S = 0 .. 8/S - 1
- * share out the rows of every tile.  S is the largest power of two up to 8
- * that cuts K into whole chunks and still gives every lane a chunk; J is
- * rounded up to a supported value (the loops are unrolled per J). */
-constexpr int JMAX_BF16 = 6;
+/* Batch-1 GEMV.  A task's prologue writes the bf16 activations of its K
+ * slice to shared memory once; then every consumer warp copies the part it
+ * multiplies into registers.  A row of the K slice is cut into S segments
+ * (1, 2, 4 or 8): warp w owns segment w % S for the whole task, holding its
+ * activations as J 16-byte chunks per lane (chunk c of the segment in lane
+ * c % 32, slot c / 32), and the 8 / S warps that share a segment take turns
+ * over the rows of every tile, RPG1 rows at a time.  A lane carries its sums
+ * across the whole segment, so a warp reduces once per row and segment.  J is
+ * a loop bound, not a template parameter: the loop is unrolled to JMAX with
+ * a warp-uniform guard, so one code instance serves every K (each task type
+ * runs once per layer from a cold instruction cache, and its code size is
+ * what that costs).  S is the fewest segments that keep J <= JMAX, raised
+ * while a tile has too few rows to give every warp work. */
+constexpr int JMAX_BF16 = 8;
 constexpr int JMAX_INT8 = 2;
-
-/* K segments per row: batch 1 as above; larger batches read activations from
- * shared memory and use 8 / rows_per_stage segments when a tile has fewer
- * than 8 rows. */
-AMK_HD inline int gemv_segments(int batch_max, int Kc, bool int8, int rows_per_stage) {
-    if (batch_max == 1) {
-        const int epc = int8 ? 16 : 8;
-        int fallback = 1;
-        for (int S = NCW; S >= 1; S >>= 1) {
-            if (Kc % (S * epc) != 0) continue;
-            if (fallback == 1) fallback = S;
-            if (Kc / S >= 32 * epc) return S;
-        }
-        return fallback;
-    }
-    return rows_per_stage < NCW ? NCW / rows_per_stage : 1;
-}
+constexpr int RPG1 = 1;
 
 /* chunks per lane J of a batch-1 segment (0: the slice is too long) */
 AMK_HD inline int gemv_lane_chunks(int Kc, int S, bool int8) {
     const int epc = int8 ? 16 : 8;
-    const int j = (Kc / S / epc + 31) / 32;
-    const int J = j <= 1 ? 1 : j <= 2 ? 2 : j <= 3 ? 3 : j <= 4 ? 4 : j <= 6 ? 6 : 0;
+    const int nch = Kc / epc;
+    const int per = (nch + S - 1) / S;
+    const int J = (per + 31) / 32;
     return J > (int8 ? JMAX_INT8 : JMAX_BF16) ? 0 : J;
+}
+
+/* K segments per row.  Batch 1 as above; larger batches read activations
+ * from shared memory and use 8 / rows_per_stage segments when a tile has
+ * fewer than 8 rows. */
+AMK_HD inline int gemv_segments(int batch_max, int Kc, bool int8, int rows_per_stage) {
+    if (batch_max == 1) {
+        int S = 1;
+        while (S < NCW && gemv_lane_chunks(Kc, S, int8) == 0) S *= 2;
+        /* every warp gets rows: (8 / S) row groups of RPG1 rows per round */
+        while (S < NCW && rows_per_stage < (NCW / S) * RPG1) S *= 2;
+        return S;
+    }
+    return rows_per_stage < NCW ? NCW / rows_per_stage : 1;
+}
+
+/* Rows of stage rb of a GEMV task of n rows cut into nst stages: the rows are
+ * spread evenly over the stages (the loader and the consumers agree). */
+AMK_HD inline void stage_rows(int n, int nst, int rb, int &a, int &e) {
+    a = (int)((long long)rb * n / nst);
+    e = (int)((long long)(rb + 1) * n / nst);
 }
 
 /* Attention: positions per warp block; q heads per kv head rounded up to a

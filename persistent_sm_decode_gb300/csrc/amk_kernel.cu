@@ -50,13 +50,15 @@
  *                       layer from a cold instruction cache, and the
  *                       never-taken timing branches inside the hot loops
  *                       alone cost about 7 % of a step.
- *  AMK_L2_PREFETCH_CODE 0 compiles out the loader's L2 prefetch (the
- *                       l2_prefetch_kb option). */
+ *  AMK_L2_PREFETCH_CODE 1 compiles in the loader's L2 prefetch (the
+ *                       l2_prefetch_kb option; measured slower at every
+ *                       distance, and 24 KB of loader code the default build
+ *                       leaves out). */
 #ifndef AMK_TRACE_CODE
 #define AMK_TRACE_CODE 0
 #endif
 #ifndef AMK_L2_PREFETCH_CODE
-#define AMK_L2_PREFETCH_CODE 1
+#define AMK_L2_PREFETCH_CODE 0
 #endif
 #define TRACE(p) (AMK_TRACE_CODE ? (p).trace : (unsigned long long *)nullptr)
 
@@ -472,8 +474,9 @@ __device__ bool task_range(const Params &p, const Task &t, int idx, const uint8_
     }
     const int rb = idx / g.nmat, m = idx % g.nmat;
     if (rb >= g.nrb) return false;
-    const int ra = t.r0 + rb * g.R, re = min(t.r1, ra + g.R);
-    ptr = op_weights(p, t, m) + (size_t)ra * rowb;
+    int ra, re;
+    stage_rows(g.nrows, g.nrb, rb, ra, re);
+    ptr = op_weights(p, t, m) + (size_t)(t.r0 + ra) * rowb;
     bytes = (uint32_t)((size_t)(re - ra) * rowb);
     return true;
 }
@@ -584,8 +587,11 @@ __device__ void loader(const Params &p, Smem &s, int tbeg, int tend) {
         const uint8_t *W[2] = {op_weights(p, t, 0), op_weights(p, t, g.nmat - 1)};
         const size_t rowb = (size_t)g.K * web, segb = (size_t)g.Kc * web;
         for (int kp = 0; kp < g.ks; ++kp) {
-            for (int ra = t.r0; ra < t.r1; ra += g.R) {
-                const int re = min(t.r1, ra + g.R);
+            for (int rb = 0; rb < g.nrb; ++rb) {
+                int ra, re;
+                stage_rows(g.nrows, g.nrb, rb, ra, re);
+                ra += t.r0;
+                re += t.r0;
                 const uint32_t bytes = (uint32_t)((re - ra) * segb);
                 for (int m = 0; m < g.nmat; ++m) {
                     uint8_t *dst = loader_claim(p, s, r, bytes, ti, pf, tend);
@@ -660,6 +666,44 @@ __device__ void norm_prologue(const Params &p, Smem &s, const uint64_t *xbase, b
                               int lane) {
     const int H = p.H, H4 = H / 4;
     constexpr int TS = NCW * 32;
+    if (p.batch == 1 && need_r && k0 == 0 && k1 == H && H4 <= XU * TS) {
+        /* one sequence, the whole row, at most XU groups of four per thread:
+         * x is read once and stays in registers; the gains are read before
+         * the wait, and every thread adds the warps' sums itself after the
+         * one barrier */
+        const uint64_t *xs = from_embed ? nullptr : xbase;
+        const uint16_t *emb = from_embed ? p.embed + (size_t)__ldg(p.tokens) * H : nullptr;
+        uint2 gw[XU];
+#pragma unroll
+        for (int u = 0; u < XU; ++u) {
+            const int i = ctid + u * TS;
+            gw[u] = i < H4 ? __ldg(reinterpret_cast<const uint2 *>(gain) + i) : make_uint2(0u, 0u);
+        }
+        float4 x[XU];
+        load_x4s<XU>(p, s, xs, emb, [=](int u) { return ctid + u * TS < H4 ? ctid + u * TS : -1; }, x, f, task,
+                     which);
+        float ss = 0.f;
+#pragma unroll
+        for (int u = 0; u < XU; ++u) ss += x[u].x * x[u].x + x[u].y * x[u].y + x[u].z * x[u].z + x[u].w * x[u].w;
+        ss = warp_sum(ss);
+        if (lane == 0) s.misc->red[0][warp] = ss;
+        cbar();
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) tot += s.misc->red[0][w];
+        const float r = rsqrtf(tot / (float)H + p.eps);
+        uint2 *dst = reinterpret_cast<uint2 *>(s.act);
+#pragma unroll
+        for (int u = 0; u < XU; ++u) {
+            const int i = ctid + u * TS;
+            if (i < H4) {
+                const float4 v = x[u];
+                dst[i] = make_uint2(pack_bf2(v.x * r * bf_lo(gw[u].x), v.y * r * bf_hi(gw[u].x)),
+                                    pack_bf2(v.z * r * bf_lo(gw[u].y), v.w * r * bf_hi(gw[u].y)));
+            }
+        }
+        return;
+    }
     if (need_r) {
         for (int b = 0; b < p.batch; ++b) {
             const uint64_t *xs = from_embed ? nullptr : xbase + (size_t)b * H;
@@ -716,26 +760,28 @@ constexpr int CU = 8;
 __device__ void copy_prologue(const Params &p, Smem &s, const uint64_t *src0, int len, int k0, int k1, uint32_t f,
                               int task, int which, int ctid) {
     constexpr int TS = NCW * 32;
-    const int kc = k1 - k0, n4 = kc / 4, tot = p.batch * n4;
-    auto addr = [=](int i) { return src0 + ((size_t)(i / n4) * len + k0) / 2 + 2 * (size_t)(i % n4); };
-    for (int i0 = ctid; i0 < tot; i0 += CU * TS) {
-        ulonglong2 v[CU];
-        uint32_t pend = 0u;
+    const int kc = k1 - k0, n4 = kc / 4;
+    for (int b = 0; b < p.batch; ++b) {
+        /* word pair i of the slice holds elements k0 + 4 i .. k0 + 4 i + 3 */
+        const uint64_t *sb = src0 + ((size_t)b * len + k0) / 2;
+        uint2 *dst = reinterpret_cast<uint2 *>(s.act + (size_t)b * kc * 2);
+        for (int i0 = ctid; i0 < n4; i0 += CU * TS) {
+            ulonglong2 v[CU];
+            uint32_t pend = 0u;
 #pragma unroll
-        for (int u = 0; u < CU; ++u) {
-            const int i = i0 + u * TS;
-            v[u] = i < tot ? ld_ll2(addr(i)) : ulonglong2{0ull, 0ull};
-        }
+            for (int u = 0; u < CU; ++u) {
+                const int i = i0 + u * TS;
+                v[u] = i < n4 ? ld_ll2(sb + 2 * (size_t)i) : ulonglong2{0ull, 0ull};
+            }
 #pragma unroll
-        for (int u = 0; u < CU; ++u)
-            if (i0 + u * TS < tot && !ll_ok(f, v[u])) pend |= 1u << u;
-        settle_all(p, s, v, pend, [=](int u) { return addr(i0 + u * TS); }, f, task, which);
+            for (int u = 0; u < CU; ++u)
+                if (i0 + u * TS < n4 && !ll_ok(f, v[u])) pend |= 1u << u;
+            settle_all(p, s, v, pend, [=](int u) { return sb + 2 * (size_t)(i0 + u * TS); }, f, task, which);
 #pragma unroll
-        for (int u = 0; u < CU; ++u) {
-            const int i = i0 + u * TS;
-            if (i < tot)
-                reinterpret_cast<uint2 *>(s.act + (size_t)(i / n4) * kc * 2)[i % n4] =
-                    make_uint2((uint32_t)v[u].x, (uint32_t)v[u].y);
+            for (int u = 0; u < CU; ++u) {
+                const int i = i0 + u * TS;
+                if (i < n4) dst[i] = make_uint2((uint32_t)v[u].x, (uint32_t)v[u].y);
+            }
         }
     }
 }
@@ -869,18 +915,6 @@ __device__ __forceinline__ float xsum(float (&v)[R], int lane) {
     return xsum_g<R, 32>(v, lane);
 }
 
-/* Activations matching one 16-byte weight chunk, in registers: eight bf16
- * values packed in pairs (element order of the weights) for bf16 weights,
- * sixteen fp32 values for int8 weights. */
-template <bool I8>
-struct ActChunk {
-    uint32_t w[4];
-};
-template <>
-struct ActChunk<true> {
-    float4 v[4];
-};
-
 /* packed fp32 pairs (sm_100 and later): (a, b) += (c, d); (s0, s1) += (a, b) * (c, d) */
 __device__ __forceinline__ void add_f32x2(float &a, float &b, float c, float d) {
     asm("{\n\t.reg .b64 x, y;\n\tmov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\t"
@@ -895,183 +929,123 @@ __device__ __forceinline__ void fma_f32x2(float &s0, float &s1, float a, float b
         : "f"(a), "f"(b), "f"(c), "f"(d));
 }
 
-/* one 16-byte weight chunk (8 bf16 or 16 int8) against activations in registers */
+/* Activations matching one 16-byte weight chunk, in registers, bf16 packed
+ * two per word in element order: eight values for bf16 weights, sixteen for
+ * int8 weights. */
 template <bool I8>
-__device__ __forceinline__ float dot_reg(const uint4 &w, const ActChunk<I8> &h) {
-    float s0 = 0.f, s1 = 0.f;
-    if constexpr (I8) {
-        /* int8 -> fp32 as in i8_to_f: the byte-permute places b ^ 0x80 under
-         * the exponent of 2^23, the packed subtraction removes 2^23 + 128 from
-         * two values at once, and one packed FMA takes both products; the
-         * order of the sums is that of the scalar form */
-        const uint32_t x[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            float f0 = __uint_as_float(__byte_perm(x[q], 0x4B000000u, 0x7540u));
-            float f1 = __uint_as_float(__byte_perm(x[q], 0x4B000000u, 0x7541u));
-            float f2 = __uint_as_float(__byte_perm(x[q], 0x4B000000u, 0x7542u));
-            float f3 = __uint_as_float(__byte_perm(x[q], 0x4B000000u, 0x7543u));
-            add_f32x2(f0, f1, -8388736.0f, -8388736.0f);
-            add_f32x2(f2, f3, -8388736.0f, -8388736.0f);
-            fma_f32x2(s0, s1, f0, f1, h.v[q].x, h.v[q].y);
-            fma_f32x2(s0, s1, f2, f3, h.v[q].z, h.v[q].w);
-        }
-    } else {
-        fma_bf16_lo(s0, w.x, h.w[0]);
-        fma_bf16_hi(s1, w.x, h.w[0]);
-        fma_bf16_lo(s0, w.y, h.w[1]);
-        fma_bf16_hi(s1, w.y, h.w[1]);
-        fma_bf16_lo(s0, w.z, h.w[2]);
-        fma_bf16_hi(s1, w.z, h.w[2]);
-        fma_bf16_lo(s0, w.w, h.w[3]);
-        fma_bf16_hi(s1, w.w, h.w[3]);
-    }
-    return s0 + s1;
-}
-
-/* rows handled together by one warp: at most 8 chunk loads in flight per lane */
-template <int J>
-struct RowsPerGroup {
-    static constexpr int value = J >= 6 ? 1 : J >= 3 ? 2 : J == 2 ? 4 : 8;
+struct ActChunk {
+    uint32_t w[4];
+};
+template <>
+struct ActChunk<true> {
+    uint32_t w[8];
 };
 
-/* One ring tile of a batch-1 task.  This warp takes rows rgp, rgp + RG, ...
- * of the tile, RPG of them at a time: every chunk load of the group is issued
- * first, then each row's products are summed over the lane's chunks, and one
- * transposing reduction gives all RPG row sums at once.  res[seg * sstride + row]
- * receives the segment's partial sum. */
-template <bool I8, int J>
-__device__ __forceinline__ void gemv_stage_b1(const uint8_t *tile, int nrows, int RG, int rgp, int rowc, int cs,
-                                              int nch, const ActChunk<I8> (&hv)[J], float *res, int sstride, int seg,
-                                              int lane) {
-    constexpr int RPG = RowsPerGroup<J>::value;
-    const uint4 *W = reinterpret_cast<const uint4 *>(tile) + cs;
-    for (int r0 = rgp; r0 < nrows; r0 += RG * RPG) {
-        uint4 wv[RPG][J];
+/* (s0, s1) += one 16-byte weight chunk . its activations (fp32 sums; the
+ * products are exact).  bf16: the mixed-precision FMA takes both operands as
+ * bf16.  int8: the byte-permute places b ^ 0x80 under the exponent of 2^23,
+ * the packed subtraction removes 2^23 + 128 (exact for every int8), and the
+ * packed FMA takes two products at once; `hf` holds the sixteen activations
+ * already widened to fp32 (once per chunk, for all rows of a group). */
+__device__ __forceinline__ void acc_chunk(float &s0, float &s1, const uint4 &w, const ActChunk<false> &h) {
+    fma_bf16_lo(s0, w.x, h.w[0]);
+    fma_bf16_hi(s1, w.x, h.w[0]);
+    fma_bf16_lo(s0, w.y, h.w[1]);
+    fma_bf16_hi(s1, w.y, h.w[1]);
+    fma_bf16_lo(s0, w.z, h.w[2]);
+    fma_bf16_hi(s1, w.z, h.w[2]);
+    fma_bf16_lo(s0, w.w, h.w[3]);
+    fma_bf16_hi(s1, w.w, h.w[3]);
+}
+__device__ __forceinline__ void acc_chunk_i8(float &s0, float &s1, const uint4 &w, const float (&hf)[16]) {
+    const uint32_t x[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
 #pragma unroll
-        for (int i = 0; i < RPG; ++i) {
-            const int rr = r0 + i * RG;
+    for (int q = 0; q < 4; ++q) {
+        float f0 = __uint_as_float(__byte_perm(x[q], 0x4B000000u, 0x7540u));
+        float f1 = __uint_as_float(__byte_perm(x[q], 0x4B000000u, 0x7541u));
+        float f2 = __uint_as_float(__byte_perm(x[q], 0x4B000000u, 0x7542u));
+        float f3 = __uint_as_float(__byte_perm(x[q], 0x4B000000u, 0x7543u));
+        add_f32x2(f0, f1, -8388736.0f, -8388736.0f);
+        add_f32x2(f2, f3, -8388736.0f, -8388736.0f);
+        fma_f32x2(s0, s1, f0, f1, hf[4 * q], hf[4 * q + 1]);
+        fma_f32x2(s0, s1, f2, f3, hf[4 * q + 2], hf[4 * q + 3]);
+    }
+}
+
+/* This warp's activations from the benchmark's bf16 slice in shared memory:
+ * chunk j of the lane is chunk c0 + lane + 32 j of the row (zero past c1). */
+template <bool I8>
+__device__ __forceinline__ void act_regs(const uint8_t *act, int c0, int c1, ActChunk<I8> (&hv)[I8 ? JMAX_INT8 : JMAX_BF16],
+                                         int lane) {
+    constexpr int JM = I8 ? JMAX_INT8 : JMAX_BF16, NQ = I8 ? 2 : 1;
+    const uint4 *A = reinterpret_cast<const uint4 *>(act);
 #pragma unroll
-            for (int j = 0; j < J; ++j) {
-                const int c = lane + 32 * j;
-                wv[i][j] = (rr < nrows && c < nch) ? W[(size_t)rr * rowc + c] : make_uint4(0u, 0u, 0u, 0u);
+    for (int j = 0; j < JM; ++j) {
+        const int c = c0 + lane + 32 * j;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            const uint4 v = c < c1 ? A[(size_t)c * NQ + q] : make_uint4(0u, 0u, 0u, 0u);
+            hv[j].w[4 * q] = v.x;
+            hv[j].w[4 * q + 1] = v.y;
+            hv[j].w[4 * q + 2] = v.z;
+            hv[j].w[4 * q + 3] = v.w;
+        }
+    }
+}
+
+/* One ring tile of a batch-1 task: nrows rows of rowc 16-byte chunks.  Warp
+ * w multiplies K segment [c0, c1) (its registers hv) of rows g * RPG1 + i +
+ * k * RG * RPG1 (g = w / S its row group, RG = 8 / S groups): RPG1 rows at a
+ * time, each lane summing its chunks of those rows into two accumulators per
+ * row, then one transposing reduction for the group.  res[seg * sstride + row]
+ * receives the segment's sum (first K slice) or has it added (later ones). */
+template <bool I8>
+__device__ __forceinline__ void gemv_stage1(const uint8_t *tile, int nrows, int RG, int rgp, int rowc, int c0, int c1,
+                                            const ActChunk<I8> (&hv)[I8 ? JMAX_INT8 : JMAX_BF16], float *res,
+                                            int sstride, int seg, bool first, int lane) {
+    constexpr int JM = I8 ? JMAX_INT8 : JMAX_BF16, RPG = RPG1;
+    const uint4 *W = reinterpret_cast<const uint4 *>(tile);
+#pragma unroll 1
+    for (int r0 = rgp * RPG; r0 < nrows; r0 += RG * RPG) {
+        float a0[RPG], a1[RPG];
+#pragma unroll
+        for (int i = 0; i < RPG; ++i) a0[i] = a1[i] = 0.f;
+        /* every slot j runs, with its loads predicated: a branch per slot
+         * would keep the loads of slot j + 1 behind the products of slot j,
+         * while this way all of a group's loads are in flight at once (slots
+         * past the segment multiply zeros) */
+#pragma unroll
+        for (int j = 0; j < JM; ++j) {
+            const int c = c0 + lane + 32 * j;
+            uint4 wv[RPG];
+#pragma unroll
+            for (int i = 0; i < RPG; ++i)
+                wv[i] = (r0 + i < nrows && c < c1) ? W[(size_t)(r0 + i) * rowc + c] : make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (I8) {
+                float hf[16];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    hf[2 * q] = bf_lo(hv[j].w[q]);
+                    hf[2 * q + 1] = bf_hi(hv[j].w[q]);
+                }
+#pragma unroll
+                for (int i = 0; i < RPG; ++i) acc_chunk_i8(a0[i], a1[i], wv[i], hf);
+            } else {
+#pragma unroll
+                for (int i = 0; i < RPG; ++i) acc_chunk(a0[i], a1[i], wv[i], hv[j]);
             }
         }
         float v[RPG];
 #pragma unroll
-        for (int i = 0; i < RPG; ++i) {
-            float a = 0.f;
-#pragma unroll
-            for (int j = 0; j < J; ++j) a += dot_reg<I8>(wv[i][j], hv[j]);
-            v[i] = a;
-        }
+        for (int i = 0; i < RPG; ++i) v[i] = a0[i] + a1[i];
         const float y = xsum<RPG>(v, lane);
-        const int rr = r0 + (lane / (32 / RPG)) * RG;
-        if ((lane & (32 / RPG - 1)) == 0 && rr < nrows) res[seg * sstride + rr] = y;
-    }
-}
-
-/* RMSNorm of sequence 0 straight into this warp's activation registers:
- * hv[j] = bf16(x * r * gain) over chunk cs + lane + 32 j of the segment.  The
- * warps that own distinct segments (warp < S) add up the sum of squares. */
-template <bool I8, int J>
-__device__ __forceinline__ void norm_regs(const Params &p, Smem &s, const uint64_t *xs, const uint16_t *emb,
-                                          const uint16_t *gain, int cs, int nch, int S, ActChunk<I8> (&hv)[J],
-                                          uint32_t f, int task, int which, int warp, int lane) {
-    constexpr int EPC = I8 ? 16 : 8, Q = EPC / 4;
-    /* the gains are read before the wait when they fit in registers beside
-     * x (up to four groups of four per lane), else after it */
-    constexpr bool early_gain = J * Q <= 4;
-    uint2 gw[J][Q];
-    float4 x[J][Q];
-    auto load_gain = [&]() {
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-            const int c = lane + 32 * j;
-#pragma unroll
-            for (int q = 0; q < Q; ++q)
-                gw[j][q] = c < nch ? __ldg(reinterpret_cast<const uint2 *>(gain) + (size_t)(cs + c) * Q + q)
-                                   : make_uint2(0u, 0u);
-        }
-    };
-    if constexpr (early_gain) load_gain();
-    /* JG chunks (at most four groups of four values) per wait */
-    constexpr int JG = Q == 2 ? 2 : 1;
-#pragma unroll
-    for (int j0 = 0; j0 < J; j0 += JG) {
-        float4 xf[JG * Q];
-        load_x4s<JG * Q>(
-            p, s, xs, emb,
-            [=](int u) {
-                const int c = lane + 32 * (j0 + u / Q);
-                return j0 + u / Q < J && c < nch ? (cs + c) * Q + u % Q : -1;
-            },
-            xf, f, task, which);
-#pragma unroll
-        for (int u = 0; u < JG * Q; ++u)
-            if (j0 + u / Q < J) x[j0 + u / Q][u % Q] = xf[u];
-    }
-    float ss = 0.f;
-#pragma unroll
-    for (int j = 0; j < J; ++j)
-#pragma unroll
-        for (int q = 0; q < Q; ++q)
-            ss += x[j][q].x * x[j][q].x + x[j][q].y * x[j][q].y + x[j][q].z * x[j][q].z + x[j][q].w * x[j][q].w;
-    __syncwarp();
-    ss = warp_sum(ss);
-    if (lane == 0 && warp < S) s.misc->red[0][warp] = ss;
-    cbar();
-    float tot = 0.f;
-    for (int w = 0; w < S; ++w) tot += s.misc->red[0][w];
-    const float r = rsqrtf(tot / (float)p.H + p.eps);
-    if constexpr (!early_gain) load_gain();
-#pragma unroll
-    for (int j = 0; j < J; ++j)
-#pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            const float4 v = x[j][q];
-            const uint2 g = gw[j][q];
-            const float4 h = make_float4(round_bf(v.x * r * bf_lo(g.x)), round_bf(v.y * r * bf_hi(g.x)),
-                                         round_bf(v.z * r * bf_lo(g.y)), round_bf(v.w * r * bf_hi(g.y)));
-            if constexpr (I8) {
-                hv[j].v[q] = h;
-            } else {
-                /* the values are exactly bf16: keep their upper halves, two per word */
-                hv[j].w[2 * q] = (__float_as_uint(h.x) >> 16) | (__float_as_uint(h.y) & 0xffff0000u);
-                hv[j].w[2 * q + 1] = (__float_as_uint(h.z) >> 16) | (__float_as_uint(h.w) & 0xffff0000u);
-            }
-        }
-}
-
-/* bf16 activations (two per epoch-tagged word) of sequence 0 into this warp's
- * registers: every load is issued before the first wait */
-template <bool I8, int J>
-__device__ __forceinline__ void copy_regs(const Params &p, Smem &s, const uint64_t *src, int cs, int nch,
-                                          ActChunk<I8> (&hv)[J], uint32_t f, int task, int which, int lane) {
-    constexpr int EPC = I8 ? 16 : 8, Q = EPC / 4;
-    auto addr = [=](int u) { return src + ((size_t)(cs + lane + 32 * (u / Q)) * EPC + 4 * (u % Q)) / 2; };
-    ulonglong2 w[J * Q];
-    uint32_t pend = 0u;
-#pragma unroll
-    for (int u = 0; u < J * Q; ++u) w[u] = lane + 32 * (u / Q) < nch ? ld_ll2(addr(u)) : ulonglong2{0ull, 0ull};
-#pragma unroll
-    for (int u = 0; u < J * Q; ++u)
-        if (lane + 32 * (u / Q) < nch && !ll_ok(f, w[u])) pend |= 1u << u;
-    settle_all(p, s, w, pend, addr, f, task, which);
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-#pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            const uint32_t a = (uint32_t)w[j * Q + q].x, b = (uint32_t)w[j * Q + q].y;
-            if constexpr (I8) {
-                hv[j].v[q] = make_float4(bf_lo(a), bf_hi(a), bf_lo(b), bf_hi(b));
-            } else {
-                hv[j].w[2 * q] = a;
-                hv[j].w[2 * q + 1] = b;
-            }
+        const int rr = r0 + lane / (32 / RPG);
+        if ((lane & (32 / RPG - 1)) == 0 && rr < nrows) {
+            /* later K slices of a K split add to the first slice's sum */
+            float *r = res + seg * sstride + rr;
+            *r = first ? y : *r + y;
         }
     }
-    __syncwarp();
 }
 
 /* Residual inputs of a task's epilogue (O projection: x_in of the layer, or
@@ -1117,22 +1091,23 @@ __device__ __forceinline__ float resid_value(const Params &p, Smem &s, const Tas
 /* Epilogue: publish the task's rows as epoch-tagged words (a task marked
  * TF_SKIP_SIGNAL publishes them with a stale flag: timeout tests).  Partial
  * sums of the S segments are added in a fixed order. */
-template <bool I8>
+template <bool I8, int NB>
 __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, int S, const ResidPre &rp, int ctid) {
     if (TRACE(p) && ctid == 0) s.misc->t_stages = now_ns();
     const long long c0 = TRACE(p) ? clock64() : 0;
     const int l = t.layer, slot = l % p.depth;
     const uint32_t stale = (t.flags & TF_SKIP_SIGNAL) ? (uint32_t)(p.L + 1) : 0u;
     const uint32_t ep = ver(p, l) - stale, ep_next = ver(p, l + 1) - stale;
-    const int n = t.r1 - t.r0, B = p.batch;
+    const int n = t.r1 - t.r0, B = NB == 1 ? 1 : p.batch;
     /* partial sums are segment-major, res[((seg * nmat + m) * n + row) * Bmax + b]:
      * consecutive threads read consecutive words; the segments are added in order */
     const int nmat = t.op == OP_GUP ? 2 : 1;
-    const int sstride = nmat * n * p.Bmax;
+    const int Bmax = NB == 1 ? 1 : p.Bmax;
+    const int sstride = nmat * n * Bmax;
     /* (the epilogue runs once per task, from a cold instruction cache: the
      * segment loop stays rolled) */
     auto y_of = [&](int m, int rr, int b) {
-        const float *r = s.res + ((size_t)m * n + rr) * p.Bmax + b;
+        const float *r = s.res + ((size_t)m * n + rr) * Bmax + b;
         float y = 0.f;
 #pragma unroll 1
         for (int sg = 0; sg < S; ++sg) y += r[(size_t)sg * sstride];
@@ -1163,31 +1138,35 @@ __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, i
                 st_ll(p.act + (((size_t)slot * p.Bmax + b) * p.I + t.r0 + 2 * pr) / 2, pack_bf2(a, other), ep);
         }
     } else {
+        /* where row `row` of sequence b goes: dst + b * bstride + row, flag fl
+         * (logits: a plain fp32 store) */
+        uint64_t *dst = nullptr;
+        size_t bstride = 0;
+        uint32_t fl = ep;
+        if (t.op == OP_QKV) {
+            const int base = t.mat == MAT_Q ? 0 : t.mat == MAT_K ? p.nq * p.d : (p.nq + p.nkv) * p.d;
+            dst = p.qkv + (size_t)slot * p.Bmax * p.qkv_rows + base;
+            bstride = p.qkv_rows;
+        } else if (t.op == OP_OPR) {
+            dst = p.x_mid + (size_t)slot * p.Bmax * p.H;
+            bstride = p.H;
+        } else if (t.op == OP_DWN) {
+            dst = p.x_in + (size_t)((l + 1) % p.depth) * p.Bmax * p.H;
+            bstride = p.H;
+            fl = ep_next;
+        }
+        const bool resid = t.op == OP_OPR || t.op == OP_DWN;
         int k = 0;
         for (int i = ctid; i < n * B; i += NCW * 32, ++k) {
             const int rr = i / B, b = i % B, row = t.r0 + rr;
-            const float y0 = y_of(0, rr, b);
+            float y = y_of(0, rr, b);
             if (TRACE(p) && ctid == 0 && k == 0) s.misc->t_x[0] = clock64() - c0;
-            switch (t.op) {
-            case OP_QKV: {
-                const int base = t.mat == MAT_Q ? 0 : t.mat == MAT_K ? p.nq * p.d : (p.nq + p.nkv) * p.d;
-                st_ll(p.qkv + ((size_t)slot * p.Bmax + b) * p.qkv_rows + base + row, __float_as_uint(y0), ep);
-                break;
+            if (t.op == OP_LMH) {
+                p.logits[(size_t)b * p.V + row] = y;
+                continue;
             }
-            case OP_OPR: {
-                const float xr = resid_value(p, s, t, ti, rp, k, b, row);
-                st_ll(p.x_mid + ((size_t)slot * p.Bmax + b) * p.H + row, __float_as_uint(xr + y0), ep);
-                break;
-            }
-            case OP_DWN: {
-                const float xm = resid_value(p, s, t, ti, rp, k, b, row);
-                st_ll(p.x_in + ((size_t)((l + 1) % p.depth) * p.Bmax + b) * p.H + row, __float_as_uint(xm + y0),
-                      ep_next);
-                break;
-            }
-            default:
-                p.logits[(size_t)b * p.V + row] = y0;
-            }
+            if (resid) y += resid_value(p, s, t, ti, rp, k, b, row);
+            st_ll(dst + (size_t)b * bstride + row, __float_as_uint(y), fl);
         }
     }
     if (TRACE(p) && ctid == 0) s.misc->t_x[1] = clock64() - c0;
@@ -1197,110 +1176,80 @@ __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, i
     return ok;
 }
 
-/* Batch-1 task without a K split: prologue into registers, tiles, epilogue. */
-template <bool I8, int J>
-__device__ bool gemv_task_b1(const Params &p, Smem &s, const Task &t, int ti, Ring &rg, const ResidPre &rp, int ctid,
-                             int warp, int lane) {
-    constexpr int EPC = I8 ? 16 : 8;
-    const GemvGeo g = gemv_geo(p, t);
-    const int NS = p.n_slots, l = t.layer, slot = l % p.depth;
-    const int S = t.seg, RG = NCW / S, seg = warp % S, rgp = warp / S;
-    const int nch = g.K / S / EPC, cs = seg * nch, rowc = g.K / EPC;
-    ActChunk<I8> hv[J];
-    if (t.op == OP_QKV) {
-        const bool emb = l == 0;
-        norm_regs<I8, J>(p, s, emb ? nullptr : p.x_in + (size_t)slot * p.Bmax * p.H,
-                         emb ? p.embed + (size_t)__ldg(p.tokens) * p.H : nullptr, p.layers[l].attn_norm, cs, nch, S,
-                         hv, ver(p, l), ti, WB_XIN, warp, lane);
-    } else if (t.op == OP_GUP) {
-        norm_regs<I8, J>(p, s, p.x_mid + (size_t)slot * p.Bmax * p.H, nullptr, p.layers[l].mlp_norm, cs, nch, S, hv,
-                         ver(p, l), ti, WB_XMID, warp, lane);
-    } else if (t.op == OP_LMH) {
-        norm_regs<I8, J>(p, s, p.x_in + (size_t)(p.L % p.depth) * p.Bmax * p.H, nullptr, p.final_norm, cs, nch, S, hv,
-                         ver(p, p.L), ti, WB_XIN, warp, lane);
-    } else if (t.op == OP_OPR) {
-        copy_regs<I8, J>(p, s, p.aout + (size_t)slot * p.Bmax * p.nq * p.d / 2, cs, nch, hv, ver(p, l), ti, WB_AOUT,
-                         lane);
-    } else {
-        copy_regs<I8, J>(p, s, p.act + (size_t)slot * p.Bmax * p.I / 2, cs, nch, hv, ver(p, l), ti, WB_ACT, lane);
-    }
-    if (TRACE(p) && ctid == 0) s.misc->t_pro = now_ns();
-    for (int rb = 0; rb < g.nrb; ++rb) {
-        const int ra = t.r0 + rb * g.R, re = min(t.r1, ra + g.R);
-        for (int m = 0; m < g.nmat; ++m, rg.advance(NS)) {
-            const int sl = rg.slot;
-            const unsigned long long tw0 = TRACE(p) ? now_ns() : 0;
-            if (!stage_ready(p, s, &s.full[sl], rg.pass & 1u, ti)) continue;
-            const unsigned long long tw1 = TRACE(p) ? now_ns() : 0;
-            if (TRACE(p) && rb == 0 && m == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
-            float *res = s.res + (size_t)m * g.nrows + (ra - t.r0);
-            gemv_stage_b1<I8, J>(s.ring + (size_t)sl * p.slot_bytes, re - ra, RG, rgp, rowc, cs, nch, hv, res,
-                                 g.nmat * g.nrows, seg, lane);
-            if (TRACE(p) && warp == 0 && lane == 0) {
-                s.misc->t_wait_full += tw1 - tw0;
-                s.misc->t_tiles += now_ns() - tw1;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s.empty[sl]);
-        }
-    }
-    if (cbar_or(s.misc->abort != 0)) return false;
-    return gemv_epilogue<I8>(p, s, t, ti, S, rp, ctid);
-}
-
+/* A GEMV task: for each K slice (ksplit of them), the prologue writes the
+ * slice's bf16 activations to shared memory (the RMSNorm of the residual for
+ * QKV, gate/up and the LM head; the attention or SwiGLU output for the O and
+ * down projections), then the tiles stream through the ring; the epilogue
+ * adds the segments' partial sums and publishes the rows. */
 template <bool I8, int NB>
 __device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring &rg, const ResidPre &rp, int ctid,
                           int warp, int lane) {
     const GemvGeo g = gemv_geo(p, t);
-    if constexpr (NB == 1) {
-        if (g.ks == 1) {
-            const int J = gemv_lane_chunks(g.K, t.seg, I8);
-            if (J == 1) return gemv_task_b1<I8, 1>(p, s, t, ti, rg, rp, ctid, warp, lane);
-            if (J == 2) return gemv_task_b1<I8, 2>(p, s, t, ti, rg, rp, ctid, warp, lane);
-            if constexpr (!I8) {
-                if (J == 3) return gemv_task_b1<I8, 3>(p, s, t, ti, rg, rp, ctid, warp, lane);
-                if (J == 4) return gemv_task_b1<I8, 4>(p, s, t, ti, rg, rp, ctid, warp, lane);
-                if (J == 6) return gemv_task_b1<I8, 6>(p, s, t, ti, rg, rp, ctid, warp, lane);
-            }
-            return false;
-        }
-    }
-    /* activations of the K slice in shared memory */
     const int NS = p.n_slots;
     const int l = t.layer, slot = l % p.depth;
     const int S = t.seg;
+    /* one call site per prologue kind: the op only picks the pointers */
+    const bool norm = t.op == OP_QKV || t.op == OP_GUP || t.op == OP_LMH;
+    const uint64_t *src;
+    const uint16_t *gain = nullptr;
+    int which, ver_l = l, len = 0;
+    bool emb = false;
+    if (t.op == OP_QKV) {
+        emb = l == 0;
+        src = p.x_in + (size_t)slot * p.Bmax * p.H;
+        gain = p.layers[l].attn_norm;
+        which = WB_XIN;
+    } else if (t.op == OP_GUP) {
+        src = p.x_mid + (size_t)slot * p.Bmax * p.H;
+        gain = p.layers[l].mlp_norm;
+        which = WB_XMID;
+    } else if (t.op == OP_LMH) {
+        src = p.x_in + (size_t)(p.L % p.depth) * p.Bmax * p.H;
+        gain = p.final_norm;
+        which = WB_XIN;
+        ver_l = p.L;
+    } else if (t.op == OP_OPR) {
+        src = p.aout + (size_t)slot * p.Bmax * p.nq * p.d / 2;
+        len = p.nq * p.d;
+        which = WB_AOUT;
+    } else {
+        src = p.act + (size_t)slot * p.Bmax * p.I / 2;
+        len = p.I;
+        which = WB_ACT;
+    }
+    const uint32_t f = ver(p, ver_l);
+    /* batch 1: this warp's K segment and row group */
+    constexpr int EPC = I8 ? 16 : 8;
+    const int rowc = g.Kc / EPC, seg = warp % S, RG = NCW / S, rgp = warp / S;
+    const int c0 = seg * rowc / S, c1 = (seg + 1) * rowc / S;
     for (int kp = 0; kp < g.ks; ++kp) {
         const int k0 = kp * g.Kc, k1 = k0 + g.Kc;
-        if (t.op == OP_QKV) {
-            const bool emb = l == 0;
-            norm_prologue(p, s, emb ? nullptr : p.x_in + (size_t)slot * p.Bmax * p.H, emb, p.layers[l].attn_norm, k0, k1,
-                          kp == 0, ver(p, l), ti, WB_XIN, ctid, warp, lane);
-        } else if (t.op == OP_GUP) {
-            norm_prologue(p, s, p.x_mid + (size_t)slot * p.Bmax * p.H, false, p.layers[l].mlp_norm, k0, k1, kp == 0,
-                          ver(p, l), ti, WB_XMID, ctid, warp, lane);
-        } else if (t.op == OP_LMH) {
-            norm_prologue(p, s, p.x_in + (size_t)(p.L % p.depth) * p.Bmax * p.H, false, p.final_norm, k0, k1, kp == 0,
-                          ver(p, p.L), ti, WB_XIN, ctid, warp, lane);
-        } else if (t.op == OP_OPR) {
-            copy_prologue(p, s, p.aout + (size_t)slot * p.Bmax * p.nq * p.d / 2, p.nq * p.d, k0, k1, ver(p, l), ti,
-                          WB_AOUT, ctid);
-        } else {
-            copy_prologue(p, s, p.act + (size_t)slot * p.Bmax * p.I / 2, p.I, k0, k1, ver(p, l), ti, WB_ACT, ctid);
-        }
+        if (norm)
+            norm_prologue(p, s, src, emb, gain, k0, k1, kp == 0, f, ti, which, ctid, warp, lane);
+        else
+            copy_prologue(p, s, src, len, k0, k1, f, ti, which, ctid);
         if (cbar_or(s.misc->abort != 0)) return false;
         if (TRACE(p) && kp == 0 && ctid == 0) s.misc->t_pro = now_ns();
+        ActChunk<I8> hv[I8 ? JMAX_INT8 : JMAX_BF16];
+        if constexpr (NB == 1) act_regs<I8>(s.act, c0, c1, hv, lane);
         for (int rb = 0; rb < g.nrb; ++rb) {
-            const int ra = t.r0 + rb * g.R, re = min(t.r1, ra + g.R);
+            int ra, re;
+            stage_rows(g.nrows, g.nrb, rb, ra, re);
             for (int m = 0; m < g.nmat; ++m, rg.advance(NS)) {
                 const int sl = rg.slot;
                 const unsigned long long tw0 = TRACE(p) ? now_ns() : 0;
                 if (!stage_ready(p, s, &s.full[sl], rg.pass & 1u, ti)) continue;
                 const unsigned long long tw1 = TRACE(p) ? now_ns() : 0;
                 if (TRACE(p) && kp == 0 && rb == 0 && m == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
-                float *res = s.res + ((size_t)m * g.nrows + (ra - t.r0)) * p.Bmax;
-                gemv_tile<I8, NB>(s.ring + (size_t)sl * p.slot_bytes, re - ra, S, g.Kc,
-                                  reinterpret_cast<const uint32_t *>(s.act), p.batch, res, g.nmat * g.nrows, p.Bmax,
-                                  kp == 0, warp, lane);
+                const uint8_t *tile = s.ring + (size_t)sl * p.slot_bytes;
+                if constexpr (NB == 1) {
+                    gemv_stage1<I8>(tile, re - ra, RG, rgp, rowc, c0, c1, hv, s.res + (size_t)m * g.nrows + ra,
+                                    g.nmat * g.nrows, seg, kp == 0, lane);
+                } else {
+                    float *res = s.res + ((size_t)m * g.nrows + ra) * p.Bmax;
+                    gemv_tile<I8, NB>(tile, re - ra, S, g.Kc, reinterpret_cast<const uint32_t *>(s.act), p.batch, res,
+                                      g.nmat * g.nrows, p.Bmax, kp == 0, warp, lane);
+                }
                 if (TRACE(p) && warp == 0 && lane == 0) {
                     s.misc->t_wait_full += tw1 - tw0;
                     s.misc->t_tiles += now_ns() - tw1;
@@ -1311,7 +1260,7 @@ __device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring 
         }
         if (cbar_or(s.misc->abort != 0)) return false;
     }
-    return gemv_epilogue<I8>(p, s, t, ti, S, rp, ctid);
+    return gemv_epilogue<I8, NB>(p, s, t, ti, S, rp, ctid);
 }
 
 /* ----------------------------------------------------------- attention */
@@ -1436,7 +1385,8 @@ __device__ __forceinline__ void att_block(AttState<LP, GP> &st, const uint16_t *
 template <int LP, int GP>
 __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, Ring &rg, int ctid, int warp, int lane) {
     constexpr int EL = LP / 8;
-    const int d = p.d, G = p.G, NS = p.n_slots;
+    constexpr int d = 4 * LP; /* head_dim: LP = d / 4 lanes share a position */
+    const int G = p.G, NS = p.n_slots;
     const int l = t.layer, slot = l % p.depth, b = t.b, grp = t.g;
     const AttGeo ag = att_geo(p, t);
     const bool active_seq = b < p.batch;
@@ -1631,10 +1581,13 @@ __device__ bool att_task(const Params &p, Smem &s, const Task &t, int ti, Ring &
  * before the first wait; thread t takes four output elements (t % (d/4)) of
  * the chunks c = t / (d/4) (mod NCL); the NCL sums of each element are added
  * in a fixed order. */
+template <int D>
 __device__ bool mrg_task(const Params &p, Smem &s, const Task &t, int ti, int ctid) {
-    const int d = p.d, G = p.G, C = t.r1, slot = t.layer % p.depth, b = t.b, h = t.g;
+    constexpr int d = D;
+    const int G = p.G, C = t.r1, slot = t.layer % p.depth, b = t.b, h = t.g;
     const int grp = h / G, hh = h % G;
-    const int Q4 = d / 4, NCL = NCW * 32 / Q4, e4 = ctid % Q4, cl = ctid / Q4;
+    constexpr int Q4 = d / 4, NCL = NCW * 32 / Q4;
+    const int e4 = ctid % Q4, cl = ctid / Q4;
     constexpr int MAXCPT = MRG_MAX_CPT;
     float *num = s.fac;                  /* [NCL][d] */
     float *den = s.fac + NCL * d;        /* [NCL] */
@@ -1788,7 +1741,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p)
                 ok = p.d == 64 ? att_task<16>(p, s, t, ti, rg, ctid, warp, lane)
                                : att_task<32>(p, s, t, ti, rg, ctid, warp, lane);
             else if (t.op == OP_MRG)
-                ok = mrg_task(p, s, t, ti, ctid);
+                ok = p.d == 64 ? mrg_task<64>(p, s, t, ti, ctid) : mrg_task<128>(p, s, t, ti, ctid);
             else
                 ok = gemv_task<I8, NB>(p, s, t, ti, rg, rp, ctid, warp, lane);
             if (!ok) break;

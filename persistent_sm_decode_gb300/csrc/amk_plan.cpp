@@ -174,8 +174,8 @@ int rows_per_slot(const Geo &g, int op, int ks, int slot) {
 }
 
 /* Shared memory besides the ring.  One region serves whichever task runs:
- * a GEMV task's partial sums [rows][segments][B], int8 row scales and (batch
- * above 1 or a K split) its bf16 activation slice [B][K/ks]; an attention
+ * a GEMV task's partial sums [rows][segments][B], int8 row scales and its
+ * bf16 activation slice [B][K/ks]; an attention
  * task's q, new k/v and per-warp state; a merge task's sums.  Activations
  * in shared memory are bf16, two per word.  A tile of R < 8
  * rows at batch above 1 is split into 8/R K segments so every warp works. */
@@ -184,8 +184,9 @@ SmemModel smem_model(const Geo &g, int ks, int slot, int C, int n_sm) {
     int gemv_act = 0;
     for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN, OP_LMH}) {
         int kc = g.K(op) / ksplit_for(g, op, ks);
-        /* batch 1 without a K split keeps activations in registers */
-        if (g.B > 1 || ksplit_for(g, op, ks) > 1) gemv_act = std::max(gemv_act, g.B * kc * 2); /* bf16 */
+        /* the prologue writes the bf16 activations of the K slice (batch 1:
+         * the warps then copy their segments into registers) */
+        gemv_act = std::max(gemv_act, g.B * kc * 2);
         int R = rows_per_slot(g, op, ks, slot);
         int S = gemv_segments(g.B, kc, g.web(op) == 1, R);
         int rows = max_task_rows(g, op, n_sm) + 1;  /* +1: a QKV matrix boundary can split a block */
@@ -552,7 +553,8 @@ amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_c
             for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN, OP_LMH}) {
                 const int kc = g.K(op) / ksplit_for(g, op, ks);
                 if ((int64_t)kc * g.web(op) > slot) fits = false;
-                if (g.B == 1 && gemv_lane_chunks(kc, gemv_segments(1, kc, g.web(op) == 1, 1), g.web(op) == 1) == 0)
+                if (g.B == 1 && gemv_lane_chunks(kc, gemv_segments(1, kc, g.web(op) == 1, NCW * RPG1),
+                                                 g.web(op) == 1) == 0)
                     fits = false;
             }
             if (g.d * 4 > slot) fits = false;

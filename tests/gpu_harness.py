@@ -20,6 +20,21 @@ ABS_TOL = 1e-3
 MARGIN = 1e-2
 
 
+def log_parity(kind: str, record: dict) -> None:
+    """Append one test's measured parity figures to the JSON-lines file named
+    by AMK_PARITY_LOG (nothing without it).  tests/parity_report.py turns the
+    file into the committed per-configuration table."""
+    import json
+    import os
+    path = os.environ.get("AMK_PARITY_LOG")
+    if not path:
+        return
+    rec = {"test": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0], "kind": kind}
+    rec.update(record)
+    with open(path, "a") as f:
+        f.write(json.dumps(rec) + "\n")
+
+
 def engine_config(wl, max_batch=None):
     import persistent_sm_decode_gb300 as amk
     return amk.make_config(wl.n_layers, wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.intermediate,
@@ -51,6 +66,20 @@ class Result:
         decode would, so no second run is needed."""
         first = [s for (s, _b, _m, agree, _f) in self.records if not agree]
         return min(first) if first else self.steps
+
+    def relaxed_misses(self):
+        """Argmax disagreements that the deep-stack rule still counts: margin
+        above both 1e-2 and twice what fp32 rounding alone moved the logits."""
+        return [r for r in self.records if not r[3] and r[2] > max(MARGIN, 2.0 * (r[4] or 0.0))]
+
+    def summary(self) -> dict:
+        rows = sorted({r[1] for r in self.records})
+        return {"steps": self.steps, "rows": rows, "worst": self.worst, "floor": self.floor,
+                "max_abs": self.max_abs, "strict_logits_ok": self.worst <= 1.0,
+                "argmax_checked": self.checked_argmax, "argmax_agree": self.argmax_agree,
+                "strict_argmax_ok": self.argmax_agree == self.checked_argmax,
+                "relaxed_misses": len(self.relaxed_misses()), "free_running": self.free_running,
+                "min_margin": min((r[2] for r in self.records), default=None)}
 
     def __repr__(self):
         return ("Result(worst=%.3g, floor=%.3g, max_abs=%.3g, argmax %d/%d, steps=%d, free-running %d)"
@@ -141,6 +170,10 @@ def teacher_forced(wl, model=None, kv=None, steps=None, options=None, batch=None
 
 
 def assert_ok(res: Result):
+    """The flat acceptance: max|d logit| <= 1e-2 max|logit| + 1e-3 at every step
+    and row, and the GPU's argmax equals the oracle's wherever the oracle's
+    top-2 margin exceeds 1e-2."""
+    log_parity("end_to_end_strict", res.summary())
     assert res.worst <= 1.0, res
     assert res.argmax_agree == res.checked_argmax, res
 
@@ -151,9 +184,12 @@ def assert_end_to_end(res: Result):
     GPU must meet the bound, or stay within twice the fp32-accumulation
     build's deviation on the same run.  Its greedy token must equal the
     oracle's wherever the oracle's top-2 margin exceeds both 1e-2 and twice
-    what fp32 rounding alone moved the logits at that step."""
+    what fp32 rounding alone moved the logits at that step.  The record
+    logged beside it also says whether the flat bound and the flat 1e-2
+    margin rule held as written."""
+    log_parity("end_to_end_relaxed", res.summary())
     assert res.worst <= max(1.0, 2.0 * res.floor), res
-    bad = [r for r in res.records if not r[3] and r[2] > max(MARGIN, 2.0 * (r[4] or 0.0))]
+    bad = res.relaxed_misses()
     assert not bad, (res, bad[:5])
 
 
@@ -231,4 +267,6 @@ def layerwise(wl, steps=2, options=None, batch=None, positions0=None, check_rows
 
 
 def assert_layers_ok(res: LayerResult):
+    log_parity("per_layer", {"steps": res.steps, "layers_checked": res.layers_checked,
+                             "worst": dict(res.worst), "where": {k: list(v) for k, v in res.where.items()}})
     assert all(v <= 1.0 for v in res.worst.values()), res

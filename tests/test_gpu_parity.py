@@ -116,8 +116,8 @@ def test_llama2_7b_per_layer():
     assert_layers_ok(layerwise(synth.workload("llama2_7b"), steps=2))
 
 
-def test_llama2_7b_batch8_per_layer_sampled_rows():
-    assert_layers_ok(layerwise(synth.workload("llama2_7b_b8"), steps=1, check_rows=[0, 5, 7]))
+def test_llama2_7b_batch8_per_layer_all_rows():
+    assert_layers_ok(layerwise(synth.workload("llama2_7b_b8"), steps=1))
 
 
 def test_tiny_per_layer_batch4_ragged():
@@ -139,10 +139,14 @@ def test_tinyllama_1b1_w8a16_end_to_end_128_steps():
     assert_end_to_end(teacher_forced(synth.workload("tinyllama_1b1_w8a16"), floor=True))
 
 
-def test_llama2_7b_end_to_end():
-    assert_end_to_end(teacher_forced(synth.workload("llama2_7b"), steps=8, check_cache=False, floor=True))
+def test_llama2_7b_end_to_end_64_steps():
+    # the workload's full 64 greedy steps
+    assert_end_to_end(teacher_forced(synth.workload("llama2_7b"), check_cache=False, floor=True))
 
 
-def test_llama2_7b_batch8_end_to_end_sampled_rows():
+def test_llama2_7b_batch8_end_to_end_all_rows():
+    # all eight sequences over 16 steps: the oracle decodes every row in full
+    # (fp64 and the fp32-accumulation build), so the step count is what bounds
+    # the test's CPU time
     wl = synth.workload("llama2_7b_b8")
-    assert_end_to_end(teacher_forced(wl, steps=4, check_rows=[0, 7], check_cache=False, floor=True))
+    assert_end_to_end(teacher_forced(wl, steps=16, check_cache=False, floor=True))
