@@ -115,7 +115,9 @@ typedef struct amk_schedule_options {
     int32_t ksplit;          /* K-dimension split of GEMV tiles (1, 2, 4) */
     int32_t scratch_depth;   /* layers of activation scratch kept before reuse (>= 1) */
     int32_t l2_prefetch_kb;  /* KB each CTA's loader prefetches into L2 ahead of its ring fills, only while
-                                the ring is full; 0 or -1: none (the default; it measured slower) */
+                                the ring is full; 0 or -1: none (the default; it measured slower).  Only a
+                                library built with AMK_L2_PREFETCH=1 accepts a positive value; the default
+                                build leaves the code out and returns AMK_ERR_UNSUPPORTED. */
     int32_t trace;           /* 1: record per-task timestamps of every step (amk_debug_read_trace).  Only a
                                 library built with the timing code (AMK_TRACE=1 at build time) accepts it;
                                 the default build returns AMK_ERR_UNSUPPORTED. */
@@ -145,10 +147,32 @@ amk_status amk_create(const amk_config *config, const amk_weights *weights,
  *             positions < p of every sequence must hold its prefix;
  *   logits    device fp32 [batch][vocab], written by the step.
  * Argument errors are returned at once; a device-side timeout is reported by
- * the next amk_sync_status, and steps launched after it do no work. */
+ * the next amk_sync_status, and steps launched after it do no work.
+ * The step's epoch (the tag that tells this step's activation words from
+ * older ones) lives in handle-owned device memory and is advanced by the
+ * kernel itself, so launches of this call may be captured in a CUDA graph
+ * and the graph replayed: every replay is a new step.  The steps of one
+ * handle must still run one after another (one stream, or a graph whose
+ * steps are chained). */
 amk_status amk_decode_step(amk_handle *h, int32_t batch, const int32_t *tokens,
                            const int32_t *positions, void *kv_cache, float *logits,
                            amk_stream_t stream);
+
+/* Greedy decoding on the device: one decode step as amk_decode_step which,
+ * in the same launch, also reduces each sequence's logits to its greedy
+ * token, the argmax over the vocabulary with the lowest index winning ties
+ * (the AutoMegaKernel abstract reproduces greedy decode token for token),
+ * and writes the inputs of the next step:
+ *   next_tokens    device int32 [batch]: argmax of row b of `logits`;
+ *   next_positions device int32 [batch]: positions[b] + 1.
+ * They must not alias tokens / positions (the step reads those throughout);
+ * ping-pong two pairs of buffers, e.g. in a CUDA graph of two steps, and the
+ * host is needed only to read tokens back.  Errors as amk_decode_step, plus
+ * AMK_ERR_INVALID_ARG for NULL, misaligned or aliasing next_* pointers. */
+amk_status amk_decode_step_greedy(amk_handle *h, int32_t batch, const int32_t *tokens,
+                                  const int32_t *positions, void *kv_cache, float *logits,
+                                  int32_t *next_tokens, int32_t *next_positions,
+                                  amk_stream_t stream);
 
 /* A decode step that allocates nothing, for callers that cannot allocate
  * device memory (an external allocator owns the device, or allocation is
@@ -199,7 +223,7 @@ typedef struct amk_error_info {
     int32_t task;        /* index of its task in that CTA's list (-1: none) */
     int32_t counter;     /* code 1: which activation buffer the wait polled: 0 residual at a layer's input,
                             1 residual after attention, 2 q/k/v, 3 attention chunk partials, 4 attention
-                            output, 5 SwiGLU output; else -1 */
+                            output, 5 SwiGLU output, 6 LM-head partial argmaxes; else -1 */
     uint32_t observed;   /* code 1: the epoch flag the stale word carried; codes 2, 3: 0 */
     uint32_t target;     /* code 1: the flag awaited (epoch * (n_layers + 1) + layer); codes 2, 3: the
                             barrier phase parity awaited */

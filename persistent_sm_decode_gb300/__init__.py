@@ -25,7 +25,7 @@ __all__ = ["AmkError", "Config", "ScheduleOptions", "DecodeEngine", "Plan", "lib
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_SCHEDULE, ERR_COOPERATIVE, ERR_TIMEOUT = range(8)
 WEIGHT_BF16, WEIGHT_INT8 = 0, 1
-OPS = ("QKV", "ATT", "OPR", "GUP", "DWN", "LMH", "MRG")
+OPS = ("QKV", "ATT", "OPR", "GUP", "DWN", "LMH", "MRG", "ARG")
 
 i32, i64, f32, f64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_double, ctypes.c_void_p
 
@@ -97,6 +97,7 @@ def lib():
             L.amk_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights),
                                      ctypes.POINTER(ScheduleOptions), ctypes.POINTER(vp)]
             L.amk_decode_step.argtypes = [vp, i32, vp, vp, vp, vp, vp]
+            L.amk_decode_step_greedy.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp]
             L.amk_decode_step_noalloc.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), i32, vp, vp,
                                                   vp, vp, vp]
             L.amk_sync_status.argtypes = [vp]
@@ -117,7 +118,7 @@ def lib():
             L.amk_plan_last_message.restype = ctypes.c_char_p
             L.amk_plan_destroy.argtypes = [vp]
             L.amk_plan_destroy.restype = None
-            for f in ("amk_create", "amk_decode_step", "amk_decode_step_noalloc", "amk_sync_status", "amk_destroy", "amk_last_error",
+            for f in ("amk_create", "amk_decode_step", "amk_decode_step_greedy", "amk_decode_step_noalloc", "amk_sync_status", "amk_destroy", "amk_last_error",
                       "amk_get_plan_info", "amk_debug_drop_signal", "amk_debug_read_residuals", "amk_debug_read_trace", "amk_plan_build", "amk_plan_validate",
                       "amk_plan_get_info", "amk_plan_get_task", "amk_plan_mutate"):
                 getattr(L, f).restype = ctypes.c_int
@@ -247,6 +248,35 @@ class DecodeEngine:
         st = lib().amk_decode_step(self._h, B, _ptr(tokens), _ptr(positions), _ptr(kv_cache), _ptr(logits), s)
         _check(st, "amk_decode_step")
 
+    def step_greedy(self, tokens, positions, kv_cache, logits, next_tokens, next_positions, stream=None,
+                    batch: Optional[int] = None) -> None:
+        """Enqueue one decode step that also writes each sequence's greedy
+        token (argmax of its logits, lowest index on ties) to next_tokens and
+        positions + 1 to next_positions (device int32 [B], not aliasing the
+        inputs)."""
+        B = int(tokens.numel()) if batch is None else int(batch)
+        s = None if stream is None else (stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+        st = lib().amk_decode_step_greedy(self._h, B, _ptr(tokens), _ptr(positions), _ptr(kv_cache), _ptr(logits),
+                                          _ptr(next_tokens), _ptr(next_positions), s)
+        _check(st, "amk_decode_step_greedy")
+
+    def greedy_graph(self, tokens, positions, kv_cache, logits):
+        """A CUDA graph of two greedy steps that ping-pong between (tokens,
+        positions) and a second pair of device buffers: each replay decodes two
+        tokens per sequence with no host involvement.  Returns (graph,
+        (tokens_b, positions_b)); after a replay the latest inputs are back in
+        (tokens, positions).  The buffers must stay alive with the graph."""
+        import torch
+        tb, pb = torch.empty_like(tokens), torch.empty_like(positions)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            self.step_greedy(tokens, positions, kv_cache, logits, tb, pb, stream=s)
+            self.step_greedy(tb, pb, kv_cache, logits, tokens, positions, stream=s)
+        torch.cuda.current_stream().wait_stream(s)
+        return g, (tb, pb)
+
     def step_raw(self, batch: int, tokens: int, positions: int, kv_cache: int, logits: int, stream: int = 0) -> int:
         """The same call with raw device addresses; returns the status."""
         return lib().amk_decode_step(self._h, batch, tokens, positions, kv_cache, logits, stream or None)
@@ -350,8 +380,8 @@ def level_times(trace, plan: "Plan") -> List[dict]:
             key = (t["layer"], t["op"])
             ends[key] = max(ends.get(key, 0), int(r[3]))
             starts[key] = min(starts.get(key, 1 << 63), int(r[0]))
-    order = {op: i for i, op in enumerate(("QKV", "ATT", "MRG", "OPR", "GUP", "DWN", "LMH"))}
-    keys = sorted(ends, key=lambda k: (k[0] + (1 if k[1] == "LMH" else 0), order[k[1]]))
+    order = {op: i for i, op in enumerate(("QKV", "ATT", "MRG", "OPR", "GUP", "DWN", "LMH", "ARG"))}
+    keys = sorted(ends, key=lambda k: (k[0] + (1 if k[1] in ("LMH", "ARG") else 0), order[k[1]]))
     out, prev = [], None
     for k in keys:
         base = prev if prev is not None else starts[k]

@@ -37,12 +37,16 @@ def _stale(target: str, deps) -> bool:
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     """AMK_TRACE=1 in the environment builds the tuning variant whose kernel
-    carries the per-task timing code (schedule option ``trace``)."""
+    carries the per-task timing code (schedule option ``trace``);
+    AMK_L2_PREFETCH=1 the one with the loader's L2 prefetch (schedule option
+    ``l2_prefetch_kb``)."""
     os.makedirs(OBJ, exist_ok=True)
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, h) for h in ("amk.h", "amk_plan.h")]
     flags = list(extra_flags)
     if os.environ.get("AMK_TRACE", "0") not in ("", "0"):
         flags.append("-DAMK_TRACE_CODE=1")
+    if os.environ.get("AMK_L2_PREFETCH", "0") not in ("", "0"):
+        flags.append("-DAMK_L2_PREFETCH_CODE=1")
     stamp = os.path.join(OBJ, "flags.txt")
     prev = open(stamp).read() if os.path.exists(stamp) else None
     if prev != " ".join(flags):

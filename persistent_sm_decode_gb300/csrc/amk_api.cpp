@@ -29,6 +29,7 @@ struct amk_handle {
     int32_t *d_start = nullptr;
     LayerPtrs *d_layers = nullptr;
     uint32_t *d_err = nullptr;
+    uint32_t *d_epoch = nullptr; /* [2]: epoch of the next step, CTAs done with the current one */
     float *d_rope = nullptr;
     uint8_t *d_scratch = nullptr;
     size_t scratch_bytes = 0;
@@ -56,6 +57,7 @@ void free_handle(amk_handle *h) {
     cudaFree(h->d_start);
     cudaFree(h->d_layers);
     cudaFree(h->d_err);
+    cudaFree(h->d_epoch);
     cudaFree(h->d_rope);
     cudaFree(h->d_scratch);
     cudaFree(h->d_trace);
@@ -194,7 +196,8 @@ amk_status amk_create(const amk_config *config, const amk_weights *weights, cons
     size_t off_xin = 0, off_xmid = off_xin + ss.x_in * w8, off_qkv = off_xmid + ss.x_mid * w8;
     size_t off_part = off_qkv + ss.qkv * w8, off_aout = off_part + ss.part * w8;
     size_t off_act = off_aout + ss.aout * w8;
-    size_t scratch_bytes = ((off_act + ss.act * w8) + 255) / 256 * 256;
+    size_t off_argp = off_act + ss.act * w8;
+    size_t scratch_bytes = ((off_argp + ss.argp * w8) + 255) / 256 * 256;
     h->scratch_bytes = scratch_bytes;
     cudaError_t e = cudaSuccess;
     auto chk = [&](cudaError_t x) {
@@ -204,6 +207,7 @@ amk_status amk_create(const amk_config *config, const amk_weights *weights, cons
     chk(cudaMalloc(&h->d_start, sizeof(int32_t) * (n_sm + 1)));
     chk(cudaMalloc(&h->d_layers, sizeof(LayerPtrs) * L));
     chk(cudaMalloc(&h->d_err, sizeof(uint32_t) * ERR_WORDS));
+    chk(cudaMalloc(&h->d_epoch, sizeof(uint32_t) * 2));
     chk(cudaMalloc(&h->d_rope, sizeof(float) * rope.size()));
     chk(cudaMalloc(&h->d_scratch, scratch_bytes));
     if (options && options->trace)
@@ -214,6 +218,9 @@ amk_status amk_create(const amk_config *config, const amk_weights *weights, cons
         chk(cudaMemcpy(h->d_layers, lp.data(), sizeof(LayerPtrs) * L, cudaMemcpyHostToDevice));
         chk(cudaMemcpy(h->d_rope, rope.data(), sizeof(float) * rope.size(), cudaMemcpyHostToDevice));
         chk(cudaMemset(h->d_err, 0, sizeof(uint32_t) * ERR_WORDS));
+        /* epoch 1 first: the zeroed scratch carries flags of epoch 0 */
+        const uint32_t ep0[2] = {1u, 0u};
+        chk(cudaMemcpy(h->d_epoch, ep0, sizeof ep0, cudaMemcpyHostToDevice));
         chk(cudaMemset(h->d_scratch, 0, scratch_bytes));
         chk(cudaDeviceSynchronize());
     }
@@ -265,6 +272,9 @@ amk_status amk_create(const amk_config *config, const amk_weights *weights, cons
     p.part = (uint64_t *)(h->d_scratch + off_part);
     p.aout = (uint64_t *)(h->d_scratch + off_aout);
     p.act = (uint64_t *)(h->d_scratch + off_act);
+    p.argp = (uint64_t *)(h->d_scratch + off_argp);
+    p.n_lmh = P.n_lmh;
+    p.epoch_word = h->d_epoch;
     p.err = h->d_err;
     p.rope = h->d_rope;
     p.timeout_ns = (options && options->wait_timeout_ns > 0) ? options->wait_timeout_ns : 1000000000LL;
@@ -273,8 +283,12 @@ amk_status amk_create(const amk_config *config, const amk_weights *weights, cons
     return AMK_OK;
 }
 
-amk_status amk_decode_step(amk_handle *h, int32_t batch, const int32_t *tokens, const int32_t *positions,
-                           void *kv_cache, float *logits, amk_stream_t stream) {
+namespace {
+
+/* one launch of the step; the epoch comes from the handle's device word */
+amk_status launch_step(amk_handle *h, int32_t batch, const int32_t *tokens, const int32_t *positions,
+                       void *kv_cache, float *logits, int32_t *next_tokens, int32_t *next_positions,
+                       amk_stream_t stream) {
     if (!h || !tokens || !positions || !kv_cache || !logits) return AMK_ERR_INVALID_ARG;
     if (batch < 1 || batch > h->cfg.max_batch) return AMK_ERR_INVALID_ARG;
     if (!aligned16(kv_cache) || ((uintptr_t)tokens & 3u) || ((uintptr_t)positions & 3u) || ((uintptr_t)logits & 3u))
@@ -287,18 +301,32 @@ amk_status amk_decode_step(amk_handle *h, int32_t batch, const int32_t *tokens, 
     p.tokens = tokens;
     p.positions = positions;
     p.logits = logits;
+    p.next_tokens = next_tokens;
+    p.next_positions = next_positions;
     p.batch = batch;
-    p.epoch = ++h->epoch;
-    p.epoch_base = p.epoch * (uint32_t)(h->cfg.n_layers + 1);
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = launch_decode(h->fn, p, h->n_sm, h->plan->smem_bytes, s);
-    if (e != cudaSuccess) {
-        --h->epoch;
-        return cuda_fail(e);
-    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    ++h->epoch;
     h->last_stream = s;
     h->launched = true;
     return AMK_OK;
+}
+
+}  // namespace
+
+amk_status amk_decode_step(amk_handle *h, int32_t batch, const int32_t *tokens, const int32_t *positions,
+                           void *kv_cache, float *logits, amk_stream_t stream) {
+    return launch_step(h, batch, tokens, positions, kv_cache, logits, nullptr, nullptr, stream);
+}
+
+amk_status amk_decode_step_greedy(amk_handle *h, int32_t batch, const int32_t *tokens, const int32_t *positions,
+                                  void *kv_cache, float *logits, int32_t *next_tokens, int32_t *next_positions,
+                                  amk_stream_t stream) {
+    if (!next_tokens || !next_positions || ((uintptr_t)next_tokens & 3u) || ((uintptr_t)next_positions & 3u))
+        return AMK_ERR_INVALID_ARG;
+    if (next_tokens == tokens || next_positions == positions) return AMK_ERR_INVALID_ARG;
+    return launch_step(h, batch, tokens, positions, kv_cache, logits, next_tokens, next_positions, stream);
 }
 
 amk_status amk_sync_status(amk_handle *h) {

@@ -17,8 +17,11 @@ namespace amk {
 /* Task kinds: one per operator of the decode step.  QKV, OPR, GUP, DWN and
  * LMH are row blocks of a GEMV (each fused with its prologue/epilogue),
  * ATT is one context chunk of one (sequence, kv head), MRG merges the chunks
- * of one (sequence, kv head) into its heads' attention output. */
-enum : uint8_t { OP_QKV = 0, OP_ATT = 1, OP_OPR = 2, OP_GUP = 3, OP_DWN = 4, OP_LMH = 5, OP_MRG = 6, OP_COUNT = 7 };
+ * of one (sequence, kv head) into its heads' attention output.  ARG reduces
+ * the LM-head tasks' partial argmaxes to each sequence's greedy token (run
+ * only by the greedy entry point). */
+enum : uint8_t { OP_QKV = 0, OP_ATT = 1, OP_OPR = 2, OP_GUP = 3, OP_DWN = 4, OP_LMH = 5, OP_MRG = 6, OP_ARG = 7,
+                 OP_COUNT = 8 };
 
 enum : uint8_t {
     TF_SKIP_SIGNAL = 1u, /* debug: do not signal on completion (timeout tests) */
@@ -43,8 +46,9 @@ struct Task {
     uint8_t flags;
     uint16_t layer;
     int32_t r0, r1;          /* GEMV: output rows [r0, r1) within matrix `mat` (QKV) or the op;
-                                ATT: r0 = chunk index c, r1 = number of chunks C; MRG: r1 = C */
-    uint16_t b, g;           /* ATT, MRG: sequence and kv head */
+                                ATT: r0 = chunk index c, r1 = number of chunks C; MRG: r1 = C;
+                                ARG: r1 = number of LM-head tasks */
+    uint16_t b, g;           /* ATT, MRG: sequence and kv head; LMH: g = index of the LM-head task */
     uint16_t rows_per_stage; /* GEMV: rows per ring slot; ATT: positions per tile */
     uint8_t ksplit;          /* GEMV: K split (k-outer loop over ksplit slices) */
     uint8_t nsig;            /* number of valid entries of sig[] */
@@ -107,8 +111,17 @@ struct Params {
     uint16_t *kc, *vc;   /* [L][Bmax][nkv][Smax][d] */
     float *logits;       /* [batch][V] */
     int batch;
-    uint32_t epoch;
-    uint32_t epoch_base; /* epoch * (L + 1): flags of this step are epoch_base + version */
+    uint32_t epoch;      /* the step's epoch when epoch_word is NULL; flags of the step are
+                            epoch * (L + 1) + version */
+    uint32_t *epoch_word; /* device [2]: the epoch of the next step, and how many CTAs have finished the
+                             current one.  Every CTA reads word 0 at start; the last CTA to finish
+                             advances it.  Keeping the epoch on the device lets a captured CUDA graph
+                             replay steps: a kernel argument would repeat the same epoch. */
+    /* greedy feedback (NULL: none): next_tokens[b] = argmax of row b of the logits (lowest index on
+     * ties), next_positions[b] = positions[b] + 1 */
+    int32_t *next_tokens, *next_positions;
+    uint64_t *argp;      /* [Bmax][n_lmh][2] tagged partial argmax (value, index) of each LM-head task */
+    int n_lmh;           /* LM-head tasks of the schedule */
     long long timeout_ns;
     unsigned long long *trace; /* NULL, or [n_tasks][16] timings */
 };

@@ -211,6 +211,8 @@ struct Misc {
     int issued;
     float red[MAXB][NCW];
     float rnorm[MAXB];
+    float argv[NCW * MAXB]; /* greedy feedback: per-warp best value and row */
+    int argi[NCW * MAXB];
     unsigned long long t_first;     /* trace: first tile of the current task arrived */
     unsigned long long t_wait_full; /* trace: consumer warp 0 waiting for tiles (ns) */
     unsigned long long t_tiles;     /* trace: consumer warp 0 computing tiles (ns) */
@@ -219,6 +221,8 @@ struct Misc {
     unsigned long long t_epi;       /* trace: epilogue written */
     unsigned long long t_x[3];      /* trace: SM cycles from epilogue start to sums formed, stores issued, closing barrier (thread 0) */
 };
+
+static_assert(sizeof(Misc) <= SMEM_MISC, "Misc fits its shared-memory region");
 
 struct Smem {
     uint64_t *full, *empty;
@@ -277,10 +281,13 @@ __device__ __forceinline__ bool stage_ready(const Params &p, Smem &s, uint64_t *
 }
 
 /* Which activation buffer a poll waits on (reported in the error word). */
-enum : int { WB_XIN = 0, WB_XMID = 1, WB_QKV = 2, WB_PART = 3, WB_AOUT = 4, WB_ACT = 5 };
+enum : int { WB_XIN = 0, WB_XMID = 1, WB_QKV = 2, WB_PART = 3, WB_AOUT = 4, WB_ACT = 5, WB_ARGP = 6 };
+
+/* epoch * (L + 1) of the step this CTA runs, set once at kernel start */
+__shared__ uint32_t s_epoch_base;
 
 /* flag of the current step for data of layer `version` */
-__device__ __forceinline__ uint32_t ver(const Params &p, int version) { return p.epoch_base + (uint32_t)version; }
+__device__ __forceinline__ uint32_t ver(const Params &, int version) { return s_epoch_base + (uint32_t)version; }
 
 __device__ __forceinline__ bool ll_ok(uint32_t f, const ulonglong2 &v) { return ll_flag(v.x) == f && ll_flag(v.y) == f; }
 
@@ -453,7 +460,7 @@ __device__ __forceinline__ void l2_prefetch(const void *src, uint32_t bytes) {
  * task's row block of one matrix per stage (whole rows when K is split), an
  * attention tile's K then V.  False past the last range. */
 __device__ bool task_range(const Params &p, const Task &t, int idx, const uint8_t *&ptr, uint32_t &bytes) {
-    if (t.op == OP_MRG) return false;
+    if (t.op == OP_MRG || t.op == OP_ARG) return false;
     if (t.op == OP_ATT) {
         const AttGeo a = att_geo(p, t);
         const int k = idx / 2;
@@ -562,7 +569,7 @@ __device__ void loader(const Params &p, Smem &s, int tbeg, int tend) {
         Task t;
         load_task(p.tasks + ti, t);
         if (TRACE(p)) TRACE(p)[16 * (size_t)ti + 9] = 0;
-        if (t.op == OP_MRG) continue;
+        if (t.op == OP_MRG || t.op == OP_ARG) continue;
         if (t.op == OP_ATT) {
             const AttGeo a = att_geo(p, t);
             const size_t row = (((size_t)t.layer * p.Bmax + t.b) * p.nkv + t.g) * (size_t)p.Smax;
@@ -1088,6 +1095,92 @@ __device__ __forceinline__ float resid_value(const Params &p, Smem &s, const Tas
     return ll_wait1(p, s, p.x_mid + ((size_t)slot * p.Bmax + b) * p.H + row, ver(p, l), ti, WB_XMID);
 }
 
+/* (v, i) becomes the better of (v, i) and (v2, i2): the larger value, the
+ * lower index between equal values */
+__device__ __forceinline__ void arg_better(float &v, int &i, float v2, int i2) {
+    if (v2 > v || (v2 == v && i2 < i)) {
+        v = v2;
+        i = i2;
+    }
+}
+
+/* The LM-head task's argmax of every sequence over its rows, from each
+ * thread's best: a warp reduction, then across warps in shared memory; the
+ * result goes out as two tagged words (value, row) in argp. */
+template <int NB>
+__device__ void lmh_argmax(const Params &p, Smem &s, const Task &t, float (&bv)[NB], int (&bi)[NB], int ctid) {
+    const int warp = ctid >> 5, lane = ctid & 31;
+    float *wv = s.misc->argv; /* [NCW][NB] values */
+    int *wi = s.misc->argi;   /* [NCW][NB] rows */
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        float v = bv[b];
+        int i = bi[b];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) arg_better(v, i, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, i, o));
+        if (lane == 0) {
+            wv[warp * NB + b] = v;
+            wi[warp * NB + b] = i;
+        }
+    }
+    cbar();
+    const int B = NB == 1 ? 1 : p.batch;
+    if (ctid < B) {
+        float v = wv[ctid];
+        int i = wi[ctid];
+        for (int w = 1; w < NCW; ++w) arg_better(v, i, wv[w * NB + ctid], wi[w * NB + ctid]);
+        uint64_t *dst = p.argp + ((size_t)ctid * p.n_lmh + t.g) * 2;
+        const uint32_t f = ver(p, p.L) - ((t.flags & TF_SKIP_SIGNAL) ? (uint32_t)(p.L + 1) : 0u);
+        st_ll(dst, __float_as_uint(v), f);
+        st_ll(dst + 1, (uint32_t)i, f);
+    }
+}
+
+/* Greedy feedback: the argmax of every sequence over all LM-head tasks'
+ * partials (the larger value; the lower row between equal values), written
+ * as that sequence's next token, with its position advanced by one. */
+__device__ bool arg_task(const Params &p, Smem &s, const Task &t, int ti, int ctid) {
+    const int nt = t.r1, B = p.batch;
+    const uint32_t f = ver(p, p.L);
+    float *wv = s.misc->argv;
+    int *wi = s.misc->argi;
+    const int warp = ctid >> 5, lane = ctid & 31;
+    for (int b = 0; b < B; ++b) {
+        float v = -INFINITY;
+        int i = 0x7fffffff;
+        constexpr int AU = 4, TS = NCW * 32;
+        for (int j0 = ctid; j0 < nt; j0 += AU * TS) {
+            ulonglong2 w[AU];
+            uint32_t pend = 0u;
+#pragma unroll
+            for (int u = 0; u < AU; ++u) {
+                const int j = j0 + u * TS;
+                w[u] = j < nt ? ld_ll2(p.argp + ((size_t)b * p.n_lmh + j) * 2) : ulonglong2{0ull, 0ull};
+                if (j < nt && !ll_ok(f, w[u])) pend |= 1u << u;
+            }
+            settle_all(p, s, w, pend, [=](int u) { return p.argp + ((size_t)b * p.n_lmh + j0 + u * TS) * 2; }, f, ti,
+                       WB_ARGP);
+#pragma unroll
+            for (int u = 0; u < AU; ++u)
+                if (j0 + u * TS < nt) arg_better(v, i, ll_f(w[u].x), (int)(uint32_t)w[u].y);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) arg_better(v, i, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, i, o));
+        if (lane == 0) {
+            wv[warp] = v;
+            wi[warp] = i;
+        }
+        cbar();
+        if (ctid == 0) {
+            for (int w = 1; w < NCW; ++w) arg_better(v, i, wv[w], wi[w]);
+            p.next_tokens[b] = i;
+            p.next_positions[b] = __ldg(p.positions + b) + 1;
+        }
+        cbar();
+    }
+    return !cbar_or(s.misc->abort != 0);
+}
+
 /* Epilogue: publish the task's rows as epoch-tagged words (a task marked
  * TF_SKIP_SIGNAL publishes them with a stale flag: timeout tests).  Partial
  * sums of the S segments are added in a fixed order. */
@@ -1156,6 +1249,17 @@ __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, i
             fl = ep_next;
         }
         const bool resid = t.op == OP_OPR || t.op == OP_DWN;
+        /* greedy feedback: each thread keeps the best (value, row) of every
+         * sequence over its items; rows rise along a thread's items, so a
+         * strict comparison keeps the lowest row among equal values */
+        const bool arg = t.op == OP_LMH && p.next_tokens != nullptr;
+        float bv[NB];
+        int bi[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            bv[b] = -INFINITY;
+            bi[b] = 0x7fffffff;
+        }
         int k = 0;
         for (int i = ctid; i < n * B; i += NCW * 32, ++k) {
             const int rr = i / B, b = i % B, row = t.r0 + rr;
@@ -1163,11 +1267,20 @@ __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, i
             if (TRACE(p) && ctid == 0 && k == 0) s.misc->t_x[0] = clock64() - c0;
             if (t.op == OP_LMH) {
                 p.logits[(size_t)b * p.V + row] = y;
+                if (arg) {
+#pragma unroll
+                    for (int bb = 0; bb < NB; ++bb)
+                        if (bb == b && (y > bv[bb] || (y == bv[bb] && row < bi[bb]))) {
+                            bv[bb] = y;
+                            bi[bb] = row;
+                        }
+                }
                 continue;
             }
             if (resid) y += resid_value(p, s, t, ti, rp, k, b, row);
             st_ll(dst + (size_t)b * bstride + row, __float_as_uint(y), fl);
         }
+        if (arg) lmh_argmax<NB>(p, s, t, bv, bi, ctid);
     }
     if (TRACE(p) && ctid == 0) s.misc->t_x[1] = clock64() - c0;
     const bool ok = !cbar_or(s.misc->abort != 0);
@@ -1664,6 +1777,76 @@ __device__ bool mrg_task(const Params &p, Smem &s, const Task &t, int ti, int ct
 /* ----------------------------------------------------------- the kernel */
 
 template <bool I8, int NB>
+__device__ __forceinline__ void run_tasks(const Params &p, Smem &s, int tbeg, int tend, int tid, int warp, int lane) {
+    if (warp == NCW) {
+        if (lane == 0) loader(p, s, tbeg, tend);
+        __syncwarp();
+    } else {
+        const int ctid = tid;
+        Ring rg{0, 0, 0};
+        for (int ti = tbeg; ti < tend; ++ti) {
+            Task t;
+            load_task(p.tasks + ti, t);
+            /* weights-only inputs are fetched before the task's inputs are ready */
+            if (I8 && t.op != OP_ATT && t.op != OP_MRG && t.op != OP_ARG) {
+                const int n = t.r1 - t.r0, nm = t.op == OP_GUP ? 2 : 1;
+                for (int i = ctid; i < n * nm; i += NCW * 32) {
+                    const int m = i / n, rr = i % n;
+                    s.sc[i] = __ldg(op_scales(p, t, m) + t.r0 + rr);
+                }
+            }
+#if AMK_L2_PREFETCH_CODE
+            if (ctid == 0) s.misc->cons_op = t.op;
+#endif
+            ResidPre rp;
+            resid_prefetch(p, t, ctid, rp);
+            unsigned long long *tr = TRACE(p) ? TRACE(p) + 16 * (size_t)ti : nullptr;
+            if (tr && ctid == 0) {
+                tr[0] = tr[1] = now_ns();
+                s.misc->t_first = 0;
+                s.misc->t_wait_full = 0;
+                s.misc->t_tiles = 0;
+                s.misc->t_pro = s.misc->t_stages = s.misc->t_epi = 0;
+                s.misc->t_x[0] = s.misc->t_x[1] = s.misc->t_x[2] = 0;
+            }
+            bool ok;
+            if (t.op == OP_ATT)
+                ok = p.d == 64 ? att_task<16>(p, s, t, ti, rg, ctid, warp, lane)
+                               : att_task<32>(p, s, t, ti, rg, ctid, warp, lane);
+            else if (t.op == OP_MRG)
+                ok = p.d == 64 ? mrg_task<64>(p, s, t, ti, ctid) : mrg_task<128>(p, s, t, ti, ctid);
+            else if (t.op == OP_ARG)
+                ok = p.next_tokens ? arg_task(p, s, t, ti, ctid) : true;
+            else
+                ok = gemv_task<I8, NB>(p, s, t, ti, rg, rp, ctid, warp, lane);
+            if (!ok) break;
+            if (tr && ctid == 0) {
+                tr[2] = s.misc->t_first;
+                tr[3] = now_ns();
+                tr[4] = s.misc->t_wait_full;
+                tr[5] = s.misc->t_tiles;
+                tr[6] = s.misc->t_pro;
+                tr[7] = s.misc->t_stages;
+                tr[8] = s.misc->t_epi;
+                tr[10] = s.misc->t_x[0];
+                tr[11] = s.misc->t_x[1];
+                tr[12] = s.misc->t_x[2];
+            }
+        }
+    }
+    __syncthreads();
+    /* never leave with bulk copies in flight into this CTA's shared memory */
+    if (warp == NCW && lane == 0) {
+        const int issued = s.misc->issued, NS = p.n_slots;
+        for (int u = max(0, issued - NS); u < issued; ++u) {
+            uint64_t t0 = now_ns();
+            while (!mbar_test(&s.full[u % NS], (uint32_t)(u / NS) & 1u))
+                if ((long long)(now_ns() - t0) > p.timeout_ns) break;
+        }
+    }
+}
+
+template <bool I8, int NB>
 __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     Smem s;
@@ -1702,71 +1885,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p)
         }
         if (bad_input && blockIdx.x == 0) raise_error(p, s, 4, -1, -1, 0, 0);
     }
-    const bool stale = __syncthreads_or(tid == 0 && (bad_input || ld_relaxed(p.err) != 0u));
-    if (stale) return;
-
-    if (warp == NCW) {
-        if (lane == 0) loader(p, s, tbeg, tend);
-        __syncwarp();
-    } else {
-        const int ctid = tid;
-        Ring rg{0, 0, 0};
-        for (int ti = tbeg; ti < tend; ++ti) {
-            Task t;
-            load_task(p.tasks + ti, t);
-            /* weights-only inputs are fetched before the task's inputs are ready */
-            if (I8 && t.op != OP_ATT && t.op != OP_MRG) {
-                const int n = t.r1 - t.r0, nm = t.op == OP_GUP ? 2 : 1;
-                for (int i = ctid; i < n * nm; i += NCW * 32) {
-                    const int m = i / n, rr = i % n;
-                    s.sc[i] = __ldg(op_scales(p, t, m) + t.r0 + rr);
-                }
-            }
-#if AMK_L2_PREFETCH_CODE
-            if (ctid == 0) s.misc->cons_op = t.op;
-#endif
-            ResidPre rp;
-            resid_prefetch(p, t, ctid, rp);
-            unsigned long long *tr = TRACE(p) ? TRACE(p) + 16 * (size_t)ti : nullptr;
-            if (tr && ctid == 0) {
-                tr[0] = tr[1] = now_ns();
-                s.misc->t_first = 0;
-                s.misc->t_wait_full = 0;
-                s.misc->t_tiles = 0;
-                s.misc->t_pro = s.misc->t_stages = s.misc->t_epi = 0;
-                s.misc->t_x[0] = s.misc->t_x[1] = s.misc->t_x[2] = 0;
-            }
-            bool ok;
-            if (t.op == OP_ATT)
-                ok = p.d == 64 ? att_task<16>(p, s, t, ti, rg, ctid, warp, lane)
-                               : att_task<32>(p, s, t, ti, rg, ctid, warp, lane);
-            else if (t.op == OP_MRG)
-                ok = p.d == 64 ? mrg_task<64>(p, s, t, ti, ctid) : mrg_task<128>(p, s, t, ti, ctid);
-            else
-                ok = gemv_task<I8, NB>(p, s, t, ti, rg, rp, ctid, warp, lane);
-            if (!ok) break;
-            if (tr && ctid == 0) {
-                tr[2] = s.misc->t_first;
-                tr[3] = now_ns();
-                tr[4] = s.misc->t_wait_full;
-                tr[5] = s.misc->t_tiles;
-                tr[6] = s.misc->t_pro;
-                tr[7] = s.misc->t_stages;
-                tr[8] = s.misc->t_epi;
-                tr[10] = s.misc->t_x[0];
-                tr[11] = s.misc->t_x[1];
-                tr[12] = s.misc->t_x[2];
-            }
-        }
+    uint32_t epoch = p.epoch;
+    if (tid == 0) {
+        if (p.epoch_word) epoch = ld_relaxed(p.epoch_word);
+        s_epoch_base = epoch * (uint32_t)(p.L + 1);
     }
-    __syncthreads();
-    /* never leave with bulk copies in flight into this CTA's shared memory */
-    if (warp == NCW && lane == 0) {
-        const int issued = s.misc->issued, NS = p.n_slots;
-        for (int u = max(0, issued - NS); u < issued; ++u) {
-            uint64_t t0 = now_ns();
-            while (!mbar_test(&s.full[u % NS], (uint32_t)(u / NS) & 1u))
-                if ((long long)(now_ns() - t0) > p.timeout_ns) break;
+    const bool stale = __syncthreads_or(tid == 0 && (bad_input || ld_relaxed(p.err) != 0u));
+    if (!stale) run_tasks<I8, NB>(p, s, tbeg, tend, tid, warp, lane);
+    /* the last CTA to finish advances the device epoch for the next step (a
+     * CTA reads it only at its start, so every CTA of this step has) */
+    if (tid == 0 && p.epoch_word) {
+        __threadfence();
+        if (atomicAdd(p.epoch_word + 1, 1u) == gridDim.x - 1) {
+            p.epoch_word[1] = 0u;
+            p.epoch_word[0] = epoch + 1u;
         }
     }
 }

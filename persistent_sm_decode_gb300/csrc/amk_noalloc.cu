@@ -163,6 +163,8 @@ amk_status upload(DeviceState &ds, const amk_config *c, const amk_weights *w, in
     off += up256(8 * ss.aout);
     const size_t o_act = off;
     off += up256(8 * ss.act);
+    const size_t o_argp = off;
+    off += up256(8 * ss.argp);
     if (off > NOALLOC_BYTES) {
         std::fprintf(stderr,
                      "amk_decode_step_noalloc: this configuration needs %zu bytes of static device state; "
@@ -241,6 +243,9 @@ amk_status upload(DeviceState &ds, const amk_config *c, const amk_weights *w, in
     p.part = (uint64_t *)(ds.base + o_part);
     p.aout = (uint64_t *)(ds.base + o_aout);
     p.act = (uint64_t *)(ds.base + o_act);
+    p.argp = (uint64_t *)(ds.base + o_argp);
+    p.n_lmh = P.n_lmh;
+    p.epoch_word = nullptr; /* the epoch is passed with each launch */
     p.err = (uint32_t *)(ds.base + o_err);
     p.rope = (const float *)(ds.base + o_rope);
     p.timeout_ns = 1000000000LL;
@@ -303,7 +308,6 @@ extern "C" amk_status amk_decode_step_noalloc(const amk_config *config, const am
     p.logits = logits;
     p.batch = batch;
     p.epoch = ++ds.epoch;
-    p.epoch_base = p.epoch * (uint32_t)(config->n_layers + 1);
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = launch_decode(ds.fn, p, ds.plan->n_sm, ds.plan->smem_bytes, s);
     if (e != cudaSuccess) {

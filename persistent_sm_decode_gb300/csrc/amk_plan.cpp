@@ -260,6 +260,7 @@ struct Builder {
     int cid_opr(int l) const { return cid_att(l) + 1; }
     int cid_gup(int l) const { return cid_att(l) + 2; }
     int cid_dwn(int l) const { return cid_att(l) + 3; }
+    int cid_lmh() const { return g.L * per_layer; } /* the LM-head tasks, awaited by the argmax */
 
     Task base(int op, int l) const {
         Task t;
@@ -277,7 +278,9 @@ struct Builder {
         Access a;
         a.buf = buf;
         a.write = w;
-        a.slot = (uint16_t)(buf == BUF_KVNEW || buf == BUF_LOGITS ? 0 : version % k.depth);
+        a.slot = (uint16_t)(buf == BUF_KVNEW || buf == BUF_LOGITS || buf == BUF_ARGP || buf == BUF_NEXT
+                                ? 0
+                                : version % k.depth);
         if (buf == BUF_KVNEW) a.slot = (uint16_t)version;
         a.version = version;
         a.b0 = b0;
@@ -372,8 +375,12 @@ struct Builder {
                         ac.push_back(acc(BUF_XIN, true, l + 1, 0, g.B, a, b));
                     } else { /* LMH */
                         t.wait_id = (uint16_t)cid_dwn(g.L - 1);
+                        t.g = (uint16_t)P->n_lmh;
+                        t.sig[t.nsig++] = (uint16_t)cid_lmh();
                         ac.push_back(acc(BUF_XIN, false, g.L, 0, g.B, 0, g.H));
                         ac.push_back(acc(BUF_LOGITS, true, 0, 0, g.B, a, b));
+                        ac.push_back(acc(BUF_ARGP, true, g.L, 0, g.B, P->n_lmh, P->n_lmh + 1));
+                        P->n_lmh++;
                     }
                 }
                 add(s, t, std::move(ac));
@@ -439,9 +446,21 @@ struct Builder {
             gemv_level(OP_GUP, l);
             gemv_level(OP_DWN, l);
         }
+        P->n_lmh = 0;
         gemv_level(OP_LMH, g.L - 1);
-        P->n_counters = g.L * per_layer;
-        P->n_levels = 6 * g.L + 1;
+        {
+            /* greedy feedback: one task reduces the LM-head tasks' partial
+             * argmaxes (it runs only when a step asks for the next tokens) */
+            Task x = base(OP_ARG, g.L - 1);
+            x.r1 = P->n_lmh;
+            x.wait_id = (uint16_t)cid_lmh();
+            std::vector<Access> ac;
+            ac.push_back(acc(BUF_ARGP, false, g.L, 0, g.B, 0, P->n_lmh));
+            ac.push_back(acc(BUF_NEXT, true, g.L, 0, g.B, 0, 1));
+            add(0, x, std::move(ac));
+        }
+        P->n_counters = g.L * per_layer + 1;
+        P->n_levels = 6 * g.L + 2;
         /* wait counts = producers per counter */
         std::vector<uint32_t> prod(P->n_counters, 0);
         for (auto &v : P->sm_tasks)
@@ -491,6 +510,7 @@ ScratchSizes scratch_sizes(const amk_plan &p) {
     s.part = D * B * g.nkv * p.k.C * g.G * (g.d + PART_PAD);
     s.aout = D * B * g.nq * g.d / 2;
     s.act = D * B * g.I / 2;
+    s.argp = B * (int64_t)std::max(1, p.n_lmh) * 2;
     return s;
 }
 
@@ -613,12 +633,12 @@ amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_c
     wb += (int64_t)g.rows(OP_LMH) * g.row_bytes(OP_LMH);
     P->weight_bytes = wb;
     ScratchSizes ss = scratch_sizes(*P);
-    P->scratch_bytes = 8 * (ss.x_in + ss.x_mid + ss.qkv + ss.part + ss.aout + ss.act);
+    P->scratch_bytes = 8 * (ss.x_in + ss.x_mid + ss.qkv + ss.part + ss.aout + ss.act + ss.argp);
 
     /* every GEMV task's partial sums must fit the result buffer */
     for (int sm_i = 0; sm_i < n_sm; ++sm_i)
         for (const Task &t : P->sm_tasks[sm_i]) {
-            if (t.op == OP_ATT || t.op == OP_MRG) continue;
+            if (t.op == OP_ATT || t.op == OP_MRG || t.op == OP_ARG) continue;
             const int64_t need = (int64_t)(t.r1 - t.r0) * g.nmat(t.op) * t.seg * g.B * 4;
             if (need > P->result_bytes) {
                 *msg = fmt("task rows %d exceed the result buffer (%lld > %d bytes)", t.r1 - t.r0, (long long)need,
@@ -791,7 +811,8 @@ bool plan_validate(const amk_plan &p, std::string *msg) {
         return x->b0 < y->b1 && y->b0 < x->b1 && x->e0 < y->e1 && y->e0 < x->e1;
     };
     static const char *bufname[BUF_COUNT] = {"x_in",       "x_mid",      "qkv",     "attn_partials",
-                                             "attn_output", "swiglu_act", "kv_slot", "logits"};
+                                             "attn_output", "swiglu_act", "kv_slot", "logits",
+                                             "argmax_partials", "next_tokens"};
     auto where = [&](int t) { return fmt("cta %d task %d", sm_of[t], idx_of[t]); };
     for (auto &gk : groups) {
         const char *bn = bufname[gk.first.first];

@@ -14,7 +14,8 @@ namespace amk {
 
 /* Activation buffers whose accesses the validator tracks.  A buffer has
  * `depth` slots; the data of layer l lives in slot l % depth ("version" l). */
-enum : uint8_t { BUF_XIN = 0, BUF_XMID, BUF_QKV, BUF_PART, BUF_AOUT, BUF_ACT, BUF_KVNEW, BUF_LOGITS, BUF_COUNT };
+enum : uint8_t { BUF_XIN = 0, BUF_XMID, BUF_QKV, BUF_PART, BUF_AOUT, BUF_ACT, BUF_KVNEW, BUF_LOGITS, BUF_ARGP, BUF_NEXT,
+                 BUF_COUNT };
 
 /* One read or write of a rectangle [b0, b1) x [e0, e1) of (buffer, slot). */
 struct Access {
@@ -64,6 +65,7 @@ struct amk_plan {
     std::vector<std::vector<amk::Task>> sm_tasks;
     std::vector<std::vector<std::vector<amk::Access>>> acc; /* parallel to sm_tasks */
     int n_counters = 0, n_levels = 0;
+    int n_lmh = 0; /* LM-head tasks (each publishes one partial argmax per sequence) */
     int act_bytes = 0, result_bytes = 0, scale_bytes = 0, fac_bytes = 0, work_bytes = 0, smem_bytes = 0;
     int64_t weight_bytes = 0, scratch_bytes = 0;
     double modeled_us = 0, search_ms = 0;
@@ -79,6 +81,7 @@ bool plan_validate(const amk_plan &p, std::string *msg);
 /* Element counts of the scratch buffers described in Params. */
 struct ScratchSizes {
     int64_t x_in, x_mid, qkv, part, aout, act; /* 8-byte epoch-tagged words */
+    int64_t argp;                              /* [Bmax][n_lmh][2]: LM-head partial argmaxes */
 };
 ScratchSizes scratch_sizes(const amk_plan &p);
 }  // namespace amk

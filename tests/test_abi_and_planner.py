@@ -39,7 +39,8 @@ def test_library_exports_every_declared_symbol(amk):
     for h in ("amk.h", "amk_plan.h"):
         src = open(os.path.join(ROOT, "include", h)).read()
         names |= set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(amk_\w+)\s*\(", src, re.M))
-    assert len(names) == 19 and {"amk_create", "amk_decode_step", "amk_destroy", "amk_plan_build"} <= names, names
+    assert len(names) == 20 and {"amk_create", "amk_decode_step", "amk_decode_step_greedy", "amk_destroy",
+                                 "amk_plan_build"} <= names, names
     for n in sorted(names):
         assert hasattr(lib, n), "libamk.so does not export %s" % n
 
@@ -54,7 +55,7 @@ def test_plans_validate_for_every_workload(amk, name):
     wl = synth.workload(name)
     p = amk.Plan(_cfg(amk, wl), wl.batch, 152)
     info = p.info()
-    assert info["n_levels"] == 6 * wl.n_layers + 1
+    assert info["n_levels"] == 6 * wl.n_layers + 2  # six per layer, the LM head, the greedy argmax
     assert info["smem_bytes"] <= 232448
     assert p.validate()[0] == amk.OK
     assert info["weight_bytes"] == wl.weight_bytes() - (2 * wl.n_layers + 1) * wl.hidden * 2

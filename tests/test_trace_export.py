@@ -78,7 +78,8 @@ def test_level_times_follow_program_order_and_add_up(plan):
     ops = [(x["layer"], x["op"]) for x in lv]
     L = max(l for l, _ in ops)
     assert ops[:6] == [(0, "QKV"), (0, "ATT"), (0, "MRG"), (0, "OPR"), (0, "GUP"), (0, "DWN")]
-    assert ops[-1] == (L, "LMH")
+    # the LM head, then the greedy argmax (which runs when a step asks for it)
+    assert ops[-2:] == [(L, "LMH"), (L, "ARG")]
     assert all(x["level_us"] >= 0 for x in lv)
     # the levels tile the step: their times add up to last end - first start
     total = sum(x["level_us"] for x in lv)
