@@ -35,7 +35,8 @@ class OrcConfig(ctypes.Structure):
     _fields_ = [("n_layers", c_i32), ("hidden", c_i32), ("n_heads", c_i32), ("n_kv_heads", c_i32),
                 ("head_dim", c_i32), ("intermediate", c_i32), ("vocab", c_i32),
                 ("weight_int8", c_i32), ("lm_head_int8", c_i32),
-                ("rms_eps", c_dbl), ("rope_theta", c_dbl)]
+                ("rms_eps", c_dbl), ("rope_theta", c_dbl),
+                ("weight_int4", c_i32), ("lm_head_int4", c_i32), ("group_size", c_i32)]
 
 
 class OrcLayer(ctypes.Structure):
@@ -86,6 +87,8 @@ def load(path: str):
     L.orc_rmsnorm.restype = None
     L.orc_gemv.argtypes = [ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp, vp, vp]
     L.orc_gemv.restype = None
+    L.orc_gemv_int4.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp]
+    L.orc_gemv_int4.restype = None
     L.orc_rope.argtypes = [ctypes.c_int, ctypes.c_int, c_dbl, vp]
     L.orc_rope.restype = None
     L.orc_attention.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp]
@@ -165,6 +168,21 @@ def gemv(W: np.ndarray, h_bits: np.ndarray, scales: Optional[np.ndarray] = None)
     return y
 
 
+def gemv_int4(W_packed: np.ndarray, h_bits: np.ndarray, scales: np.ndarray, group: int) -> np.ndarray:
+    """y = W h for 4-bit codes (two per byte, element 2j in the low nibble of
+    byte j; value = scale * (code - 8)) with one scale per `group` weights
+    along K (scales [rows][K / group])."""
+    W = np.ascontiguousarray(W_packed, dtype=np.uint8)
+    h = np.ascontiguousarray(h_bits, dtype=np.uint16)
+    rows, K = W.shape[0], 2 * W.shape[1]
+    assert h.size == K and K % group == 0
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
+    assert sc.shape == (rows, K // group)
+    y = np.empty(rows, dtype=np.float64)
+    lib().orc_gemv_int4(rows, K, group, _p(W), _p(sc), _p(h), _p(y))
+    return y
+
+
 def rope(u: np.ndarray, pos: int, theta: float) -> np.ndarray:
     u = np.array(u, dtype=np.float64, copy=True)
     lib().orc_rope(u.size, pos, theta, _p(u))
@@ -218,9 +236,11 @@ class Oracle:
         self.Bmax = self.kc.shape[1]
         self.Smax = self.kc.shape[3]
         i8 = wl.weight_dtype == "int8"
+        i4 = wl.weight_dtype == "int4"
         self.cfg = OrcConfig(wl.n_layers, wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim,
                              wl.intermediate, wl.vocab, int(i8), int(i8 and not wl.tied),
-                             wl.rms_eps, wl.rope_theta)
+                             wl.rms_eps, wl.rope_theta, int(i4), int(i4 and not wl.tied),
+                             getattr(wl, "group_size", 128))
         n = wl.n_layers
         self._layers = (OrcLayer * n)()
         for l, hl in enumerate(model.layers):

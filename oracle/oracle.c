@@ -125,6 +125,33 @@ void orc_gemv(int rows, int K, const void *W, int w_int8, const float *scales,
     free(hd);
 }
 
+/* y[o] = sum_g s[o][g] * sum_{i in group g} (u[o][i] - 8) * h[i] for 4-bit
+ * weight codes u in [0, 15] around the zero point 8 (the symmetric 4-bit
+ * weight-only quantisation of W4A16), packed two per byte with element 2j in
+ * the low nibble of byte j, and one fp32 scale per `group` weights along K
+ * (scales [rows][K / group]). */
+void orc_gemv_int4(int rows, int K, int group, const uint8_t *W, const float *scales, const uint16_t *h,
+                   double *y) {
+    double *hd = (double *)malloc(sizeof(double) * (size_t)K);
+    for (int i = 0; i < K; ++i) hd[i] = orc_bf16_to_double(h[i]);
+    const int ng = K / group;
+#pragma omp parallel for schedule(static)
+    for (int o = 0; o < rows; ++o) {
+        const uint8_t *w = W + (size_t)o * (K / 2);
+        double tot = 0.0;
+        for (int g = 0; g < ng; ++g) {
+            acc_t acc = 0;
+            for (int i = g * group; i < (g + 1) * group; ++i) {
+                const int u = (w[i / 2] >> (4 * (i & 1))) & 15;
+                acc += (double)(u - 8) * hd[i];
+            }
+            tot += (double)scales[(size_t)o * ng + g] * acc;
+        }
+        y[o] = tot;
+    }
+    free(hd);
+}
+
 /* Rotary position embedding (Su et al., RoFormer 2021), rotate-half pairing:
  * for i < d/2, theta_i = pos * base^(-2i/d) and the pair (u_i, u_{i+d/2}) is
  * rotated by theta_i. */
@@ -186,13 +213,25 @@ typedef struct {
     int32_t weight_int8;  /* 0: bf16 layer matrices; 1: int8 layer matrices + fp32 per-row scales */
     int32_t lm_head_int8; /* 1: the LM head is int8 with per-row scales */
     double rms_eps, rope_theta;
+    int32_t weight_int4;  /* 1: 4-bit layer matrices + fp32 scales per `group_size` weights (orc_gemv_int4) */
+    int32_t lm_head_int4; /* 1: the LM head is 4-bit as well */
+    int32_t group_size;
 } orc_config;
 
 typedef struct {
     const uint16_t *attn_norm, *mlp_norm;          /* [H] bf16 gains */
     const void *wq, *wk, *wv, *wo, *wg, *wu, *wd;  /* [out, in] row-major */
-    const float *sq, *sk, *sv, *so, *sg, *su, *sd; /* per-row scales, int8 only */
+    const float *sq, *sk, *sv, *so, *sg, *su, *sd; /* int8: per-row scales; int4: [out][in / group_size] */
 } orc_layer;
+
+/* one layer matrix in the model's weight format */
+static void mat_vec(const orc_config *c, int lm, int rows, int K, const void *W, const float *s, const uint16_t *h,
+                    double *y) {
+    if (lm ? c->lm_head_int4 : c->weight_int4)
+        orc_gemv_int4(rows, K, c->group_size, (const uint8_t *)W, s, h, y);
+    else
+        orc_gemv(rows, K, W, lm ? c->lm_head_int8 : c->weight_int8, s, h, y);
+}
 
 typedef struct {
     const uint16_t *embed;      /* [V, H] bf16 */
@@ -234,7 +273,6 @@ int orc_layer_forward(const orc_config *c, const orc_layer *w, int l, int b, int
     const int I = c->intermediate;
     if (nkv < 1 || nq % nkv != 0 || d % 2 != 0 || p < 0 || p >= Smax || b < 0 || b >= Bmax) return -1;
     const int G = nq / nkv;
-    const int i8 = c->weight_int8;
     double *y = malloc(sizeof(double) * (H > I ? H : I));
     double *q = malloc(sizeof(double) * nq * d), *k = malloc(sizeof(double) * nkv * d);
     double *v = malloc(sizeof(double) * nkv * d), *o = malloc(sizeof(double) * nq * d);
@@ -244,9 +282,9 @@ int orc_layer_forward(const orc_config *c, const orc_layer *w, int l, int b, int
 
     orc_rmsnorm(H, x, w->attn_norm, c->rms_eps, y);
     round_vec(H, y, hb);
-    orc_gemv(nq * d, H, w->wq, i8, w->sq, hb, q);
-    orc_gemv(nkv * d, H, w->wk, i8, w->sk, hb, k);
-    orc_gemv(nkv * d, H, w->wv, i8, w->sv, hb, v);
+    mat_vec(c, 0, nq * d, H, w->wq, w->sq, hb, q);
+    mat_vec(c, 0, nkv * d, H, w->wk, w->sk, hb, k);
+    mat_vec(c, 0, nkv * d, H, w->wv, w->sv, hb, v);
     for (int j = 0; j < nq; ++j) orc_rope(d, p, c->rope_theta, q + (size_t)j * d);
     for (int g = 0; g < nkv; ++g) orc_rope(d, p, c->rope_theta, k + (size_t)g * d);
 
@@ -265,16 +303,16 @@ int orc_layer_forward(const orc_config *c, const orc_layer *w, int l, int b, int
                       o + (size_t)j * d);
     }
     round_vec(nq * d, o, ob);
-    orc_gemv(H, nq * d, w->wo, i8, w->so, ob, y);
+    mat_vec(c, 0, H, nq * d, w->wo, w->so, ob, y);
     for (int i = 0; i < H; ++i) x[i] += y[i];
     if (x_mid) memcpy(x_mid, x, sizeof(double) * H);
 
     orc_rmsnorm(H, x, w->mlp_norm, c->rms_eps, y);
     round_vec(H, y, hb);
-    orc_gemv(I, H, w->wg, i8, w->sg, hb, gt);
-    orc_gemv(I, H, w->wu, i8, w->su, hb, up);
+    mat_vec(c, 0, I, H, w->wg, w->sg, hb, gt);
+    mat_vec(c, 0, I, H, w->wu, w->su, hb, up);
     for (int i = 0; i < I; ++i) hb[i] = orc_double_to_bf16(orc_silu(gt[i]) * up[i]);
-    orc_gemv(H, I, w->wd, i8, w->sd, hb, y);
+    mat_vec(c, 0, H, I, w->wd, w->sd, hb, y);
     for (int i = 0; i < H; ++i) x[i] += y[i];
 
     free(y); free(q); free(k); free(v); free(o); free(gt); free(up); free(hb); free(ob);
@@ -288,7 +326,7 @@ void orc_lm_head(const orc_config *c, const orc_weights *wt, const double *x, do
     uint16_t *hb = malloc(sizeof(uint16_t) * H);
     orc_rmsnorm(H, x, wt->final_norm, c->rms_eps, y);
     round_vec(H, y, hb);
-    orc_gemv(c->vocab, H, wt->lm_head, c->lm_head_int8, wt->s_lm, hb, logits);
+    mat_vec(c, 1, c->vocab, H, wt->lm_head, wt->s_lm, hb, logits);
     free(y);
     free(hb);
 }

@@ -50,11 +50,12 @@ def lib():
             L.synth_normal_bf16.argtypes = [u64, cp, c_d, c_d, u64, vp, i64]
             L.synth_normal_f32.argtypes = [u64, cp, c_d, c_d, u64, vp, i64]
             L.synth_uniform_i8.argtypes = [u64, cp, u64, vp, i64]
+            L.synth_uniform_u4.argtypes = [u64, cp, u64, vp, i64]
             L.synth_scales_f32.argtypes = [u64, cp, c_d, c_d, vp, i64]
             L.synth_raw_u64.argtypes = [u64, cp, u64, vp, i64]
             L.synth_kv_cache.argtypes = [u64, c_i, c_i, c_i, c_i, c_i, c_i, vp, vp]
             L.synth_splitmix64_seq.argtypes = [u64, i64, vp]
-            for f in ("synth_normal_bf16", "synth_normal_f32", "synth_uniform_i8",
+            for f in ("synth_normal_bf16", "synth_normal_f32", "synth_uniform_i8", "synth_uniform_u4",
                       "synth_scales_f32", "synth_raw_u64", "synth_kv_cache", "synth_splitmix64_seq"):
                 getattr(L, f).restype = None
             _lib = L
@@ -83,6 +84,16 @@ def normal_f32(seed: int, name: str, shape, std: float = 1.0, mean: float = 0.0,
 def uniform_i8(seed: int, name: str, shape, offset: int = 0) -> np.ndarray:
     out = np.empty(shape, dtype=np.int8)
     lib().synth_uniform_i8(seed, name.encode(), offset, _ptr(out), out.size)
+    return out
+
+
+def uniform_u4(seed: int, name: str, shape, offset: int = 0) -> np.ndarray:
+    """4-bit codes uniform in [1, 15], packed two per byte (element 2j in the
+    low nibble of byte j); `shape` is the unpacked shape, its last dimension even."""
+    shape = tuple(shape)
+    assert shape[-1] % 2 == 0
+    out = np.empty(shape[:-1] + (shape[-1] // 2,), dtype=np.uint8)
+    lib().synth_uniform_u4(seed, name.encode(), offset, _ptr(out), int(np.prod(shape)))
     return out
 
 
@@ -132,7 +143,8 @@ class Workload:
     rms_eps: float = 1e-5
     rope_theta: float = 1e4
     tied: bool = False
-    weight_dtype: str = "bf16"   # "bf16" or "int8" (W8A16)
+    weight_dtype: str = "bf16"   # "bf16", "int8" (W8A16) or "int4" (W4A16: 4-bit codes, group scales)
+    group_size: int = 128        # int4 only: weights per scale along K
     weight_std: float = 0.02
     scale_jitter: float = 0.0    # int8 only: per-row scale = 0.02/127 * (1 + jitter*U)
     description: str = ""
@@ -145,16 +157,21 @@ class Workload:
     def qkv_rows(self) -> int:
         return (self.n_heads + 2 * self.n_kv_heads) * self.head_dim
 
+    def matrix_bytes(self, rows: int, k: int) -> int:
+        """Bytes of one [rows, k] matrix in the workload's weight format, with its scales."""
+        if self.weight_dtype == "int8":
+            return rows * k + rows * 4
+        if self.weight_dtype == "int4":
+            return rows * k // 2 + rows * (k // self.group_size) * 4
+        return rows * k * 2
+
     def weight_bytes(self) -> int:
-        """Bytes of every linear weight (plus int8 row scales) read by one step."""
+        """Bytes of every linear weight (plus int8 row or int4 group scales) read by one step."""
         H, I, V, d = self.hidden, self.intermediate, self.vocab, self.head_dim
         per_layer_rows_k = [(self.qkv_rows, H), (H, self.n_heads * d), (2 * I, H), (H, I)]
-        eb = 1 if self.weight_dtype == "int8" else 2
-        tot = 0
-        for rows, k in per_layer_rows_k:
-            tot += rows * k * eb + (rows * 4 if eb == 1 else 0)
-        tot *= self.n_layers
-        tot += V * H * eb + (V * 4 if eb == 1 else 0)  # LM head (tied: the embedding, read once)
+        tot = sum(self.matrix_bytes(rows, k) for rows, k in per_layer_rows_k) * self.n_layers
+        # LM head (tied: the bf16 embedding, read once)
+        tot += V * H * 2 if self.tied else self.matrix_bytes(V, H)
         tot += (2 * self.n_layers + 1) * H * 2          # norm gains
         return tot
 
@@ -185,6 +202,15 @@ WORKLOADS: Dict[str, Workload] = {
     "llama2_7b_b8": Workload(
         "llama2_7b_b8", 32, 4096, 32, 32, 128, 11008, 32000, ctx=4096, max_seq=4160, steps=64, batch=8,
         description="Llama-2-7B shape at batch 8, context 4096, 64 steps"),
+    "tinyllama_1b1_w4a16": Workload(
+        "tinyllama_1b1_w4a16", 22, 2048, 32, 4, 64, 5632, 32000, ctx=1024, max_seq=1152, steps=128,
+        weight_dtype="int4",
+        description="TinyLlama-1.1B shape, W4A16: 4-bit codes uniform in [1, 15] around zero point 8, one "
+                    "fp32 scale 0.02/7 per 128 weights along K; context 1024; 128 steps"),
+    "tinyllama_1b1_short": Workload(
+        "tinyllama_1b1_short", 22, 2048, 32, 4, 64, 5632, 32000, ctx=64, max_seq=80, steps=12,
+        description="TinyLlama-1.1B shape with a short sequence: 64 prompt positions, 12 decode steps; the "
+                    "batch-size sweep (1, 2, 4, 8, 16) runs on it"),
 }
 
 
@@ -231,6 +257,12 @@ def mat_shapes(wl: Workload) -> Dict[str, tuple]:
 
 
 def _matrix(wl: Workload, seed: int, name: str, shape):
+    if wl.weight_dtype == "int4":
+        assert shape[1] % wl.group_size == 0, "K must be a whole number of scale groups"
+        q = uniform_u4(seed, name, shape)
+        s = scales_f32(seed, name + ".scale", shape[0] * (shape[1] // wl.group_size), wl.weight_std / 7.0,
+                       wl.scale_jitter).reshape(shape[0], shape[1] // wl.group_size)
+        return q, s
     if wl.weight_dtype == "int8":
         q = uniform_i8(seed, name, shape)
         s = scales_f32(seed, name + ".scale", shape[0], wl.weight_std / 127.0, wl.scale_jitter)

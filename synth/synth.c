@@ -101,6 +101,22 @@ void synth_uniform_i8(uint64_t seed, const char *name, uint64_t offset, int8_t *
     }
 }
 
+/* n 4-bit codes, each uniform in [1, 15] (the values -7..7 around the zero
+ * point 8), packed two per byte: code 2j in the low nibble of out[j], code
+ * 2j + 1 in the high nibble (n even) */
+void synth_uniform_u4(uint64_t seed, const char *name, uint64_t offset, uint8_t *out, int64_t n) {
+    uint64_t st = stream_state(seed, name);
+#pragma omp parallel for schedule(static, 65536)
+    for (int64_t j = 0; j < n / 2; ++j) {
+        uint8_t c[2];
+        for (int h = 0; h < 2; ++h) {
+            uint64_t r = draw(st, offset + (uint64_t)(2 * j + h)) >> 32;
+            c[h] = (uint8_t)(1 + ((r * 15u) >> 32));
+        }
+        out[j] = (uint8_t)(c[0] | (c[1] << 4));
+    }
+}
+
 /* out[i] = base * (1 + jitter * U_i), U_i uniform in [0, 1) */
 void synth_scales_f32(uint64_t seed, const char *name, double base, double jitter,
                       float *out, int64_t n) {

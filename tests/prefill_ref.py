@@ -27,6 +27,12 @@ def bits(b) -> np.ndarray:
 def dense(W, scales=None) -> np.ndarray:
     if W.dtype == np.int8:
         return W.astype(np.float64) * np.asarray(scales, dtype=np.float64)[:, None]
+    if W.dtype == np.uint8:
+        # 4-bit codes two per byte (low nibble first), value scale[row][k // group] * (code - 8)
+        codes = np.stack([W & 15, W >> 4], axis=-1).reshape(W.shape[0], 2 * W.shape[1]).astype(np.float64)
+        sc = np.asarray(scales, dtype=np.float64)
+        group = codes.shape[1] // sc.shape[1]
+        return (codes - 8.0) * np.repeat(sc, group, axis=1)
     return bits(W)
 
 

@@ -77,6 +77,18 @@ def test_decode_matches_prefill_int8_weights():
     np.testing.assert_allclose(dec, ref, rtol=0, atol=1e-10 * np.abs(ref).max())
 
 
+def test_decode_matches_prefill_int4_weights():
+    wl = synth.workload("tiny", weight_dtype="int4", group_size=16, scale_jitter=0.5)  # I = 688 = 43 x 16
+    model = with_random_gains(synth.make_model(wl, seed=3))
+    kc, vc = synth.make_kv(wl, seed=4)
+    tokens = [11, 12, 1000]
+    dec, _ = _decode_sequence(model, kc, vc, tokens, start=wl.ctx)
+    prior_k = [kc[l, 0, :, : wl.ctx] for l in range(wl.n_layers)]
+    prior_v = [vc[l, 0, :, : wl.ctx] for l in range(wl.n_layers)]
+    ref = prefill_logits(model, tokens, prior_k, prior_v)
+    np.testing.assert_allclose(dec, ref, rtol=0, atol=1e-10 * np.abs(ref).max())
+
+
 def test_zero_output_projections_make_every_layer_the_identity(tiny):
     # With Wo = Wd = 0 the residual stream never changes, so the logits have the
     # closed form W_lm . bf16(rmsnorm(E[t]) * g_final).

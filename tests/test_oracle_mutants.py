@@ -35,8 +35,13 @@ MUTANTS = {
     "cache_stores_v_as_k": ("kcache[(row + p) * d + i] = orc_double_to_bf16(k[(size_t)g * d + i]);",
                             "kcache[(row + p) * d + i] = orc_double_to_bf16(v[(size_t)g * d + i]);"),
     "k_not_rotated": ("for (int g = 0; g < nkv; ++g) orc_rope(d, p, c->rope_theta, k + (size_t)g * d);", ""),
-    "attn_residual_dropped": ("orc_gemv(H, nq * d, w->wo, i8, w->so, ob, y);\n    for (int i = 0; i < H; ++i) x[i] += y[i];",
-                              "orc_gemv(H, nq * d, w->wo, i8, w->so, ob, y);\n    for (int i = 0; i < H; ++i) x[i] = y[i];"),
+    "attn_residual_dropped": ("mat_vec(c, 0, H, nq * d, w->wo, w->so, ob, y);\n    for (int i = 0; i < H; ++i) x[i] += y[i];",
+                              "mat_vec(c, 0, H, nq * d, w->wo, w->so, ob, y);\n    for (int i = 0; i < H; ++i) x[i] = y[i];"),
+    "gemv_int4_high_nibble_first": ("const int u = (w[i / 2] >> (4 * (i & 1))) & 15;",
+                                    "const int u = (w[i / 2] >> (4 * (1 - (i & 1)))) & 15;"),
+    "gemv_int4_one_scale_per_row": ("tot += (double)scales[(size_t)o * ng + g] * acc;",
+                                    "tot += (double)scales[(size_t)o * ng] * acc;"),
+    "gemv_int4_no_zero_point": ("acc += (double)(u - 8) * hd[i];", "acc += (double)u * hd[i];"),
     "swiglu_gate_up_swapped": ("orc_silu(gt[i]) * up[i]", "orc_silu(up[i]) * gt[i]"),
     "silu_wrong_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
     "norm_gains_swapped": ("orc_rmsnorm(H, x, w->attn_norm, c->rms_eps, y);", "orc_rmsnorm(H, x, w->mlp_norm, c->rms_eps, y);"),

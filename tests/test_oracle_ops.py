@@ -126,6 +126,33 @@ def test_gemv_brute_force_against_numpy_matmul():
     np.testing.assert_array_equal(oracle.gemv(W8, h8, s), ref8)
 
 
+def _unpack_u4(Wp):
+    """4-bit codes from bytes, element 2j from the low nibble of byte j (numpy, independent of the oracle)."""
+    return np.stack([Wp & 15, Wp >> 4], axis=-1).reshape(Wp.shape[0], 2 * Wp.shape[1]).astype(np.int64)
+
+
+def test_gemv_int4_onehot_returns_scaled_column():
+    # element i is code u = nibble (i % 2) of byte i // 2, value s[row][i // 128] * (u - 8)
+    Wp = synth.uniform_u4(5, "W4", (19, 384))
+    s = synth.scales_f32(5, "W4.scale", 19 * 3, 0.02 / 7, 0.5).reshape(19, 3)   # jittered per group
+    u = _unpack_u4(Wp)
+    for i in (0, 1, 127, 128, 255, 383):
+        want = s[:, i // 128].astype(np.float64) * (u[:, i] - 8).astype(np.float64)
+        np.testing.assert_array_equal(oracle.gemv_int4(Wp, _onehot_bf16(384, i), s, 128), want)
+
+
+def test_gemv_int4_brute_force_against_numpy_dequantised_matmul():
+    Wp = synth.uniform_u4(6, "W4", (33, 512))
+    s = synth.scales_f32(6, "W4.scale", 33 * 8, 0.02 / 7, 0.5).reshape(33, 8)
+    h = synth.normal_bf16(6, "h4", (512,), std=1.0)
+    dq = (_unpack_u4(Wp) - 8).astype(np.float64) * np.repeat(s.astype(np.float64), 64, axis=1)
+    got = oracle.gemv_int4(Wp, h, s, 64)
+    np.testing.assert_allclose(got, dq @ bits(h), rtol=1e-13, atol=1e-15)
+    # the codes cover 1..15 only (values -7..7) and are roughly uniform
+    u = _unpack_u4(Wp)
+    assert u.min() == 1 and u.max() == 15 and abs(u.mean() - 8.0) < 0.2
+
+
 # ----------------------------------------------------------------- RoPE
 
 def test_rope_identity_at_position_zero():
