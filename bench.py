@@ -283,8 +283,8 @@ def config_block(wl):
 
 def workload_dtype(wl) -> str:
     """The arithmetic the path computes in: bf16 products with fp32 sums, or
-    int8 weights times bf16 activations (W8A16) with fp32 sums."""
-    return "int8xbf16" if wl.weight_dtype == "int8" else "bf16"
+    int8 / int4 weights times bf16 activations (W8A16 / W4A16) with fp32 sums."""
+    return {"int8": "int8xbf16", "int4": "int4xbf16"}.get(wl.weight_dtype, "bf16")
 
 
 def device_model(wl, seed: int):
@@ -301,6 +301,11 @@ def device_model(wl, seed: int):
     H, V = wl.hidden, wl.vocab
 
     def mat(shape):
+        if wl.weight_dtype == "int4":
+            codes = torch.randint(0, 256, (shape[0], shape[1] // 2), generator=g, device="cuda",
+                                  dtype=torch.int32).to(torch.uint8)
+            return codes, torch.full((shape[0], shape[1] // wl.group_size), wl.weight_std / 7.0, device="cuda",
+                                     dtype=torch.float32)
         if wl.weight_dtype == "int8":
             q = torch.randint(-127, 128, shape, generator=g, device="cuda", dtype=torch.int8)
             return q, torch.full((shape[0],), wl.weight_std / 127.0, device="cuda", dtype=torch.float32)
@@ -340,7 +345,8 @@ def device_kv(wl, seed: int, batch: int):
 def make_engine(amk, wl, dev, opts):
     cfg = amk.make_config(wl.n_layers, wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.intermediate,
                           wl.vocab, wl.max_seq, wl.batch, wl.rms_eps, wl.rope_theta,
-                          int8=wl.weight_dtype == "int8", tied=wl.tied)
+                          int8=wl.weight_dtype == "int8", tied=wl.tied,
+                          int4=wl.weight_dtype == "int4", group_size=wl.group_size)
     return amk.DecodeEngine(cfg, dev["embed"], dev["final_norm"], dev["layers"], dev["lm_head"], dev["s_lm"],
                             opts or None)
 
@@ -408,17 +414,78 @@ class Timed:
                 "frac_of_8TBps": achieved / NOMINAL_HBM_GBS, "kernel": "amk_decode_kernel"}
 
 
-SUB_WORKLOADS = ("tinyllama_1b1_w8a16", "llama2_7b", "llama2_7b_b8", "smollm2_135m")
+SUB_WORKLOADS = ("tinyllama_1b1_w8a16", "tinyllama_1b1_w4a16", "llama2_7b", "llama2_7b_b8", "smollm2_135m",
+                 # the batch-size sweep on the short-sequence shape (64 prompt positions, 12 steps)
+                 "tinyllama_1b1_short@1", "tinyllama_1b1_short@2", "tinyllama_1b1_short@4",
+                 "tinyllama_1b1_short@8", "tinyllama_1b1_short@16",
+                 # the same step as one launch per operator, CUDA-graphed
+                 "unfused:tinyllama_1b1")
+
+
+def unfused_record(amk, wl, steps, local):
+    """The per-operator path (one launch per operator) on the same shape and
+    device-filled data: one step captured in a CUDA graph, replayed `steps`
+    times after warm-up, timed with CUDA events."""
+    import numpy as np
+    import torch
+    dev = device_model(wl, seed=1)
+    kv = device_kv(wl, seed=2, batch=wl.batch)
+    cfg = amk.make_config(wl.n_layers, wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.intermediate,
+                          wl.vocab, wl.max_seq, wl.batch, wl.rms_eps, wl.rope_theta,
+                          int8=wl.weight_dtype == "int8", tied=wl.tied,
+                          int4=wl.weight_dtype == "int4", group_size=wl.group_size)
+    u = amk.UnfusedEngine(cfg, dev["embed"], dev["final_norm"], dev["layers"], dev["lm_head"], dev["s_lm"])
+    tok = torch.ones(wl.batch, dtype=torch.int32, device="cuda")
+    pos = torch.full((wl.batch,), wl.ctx, dtype=torch.int32, device="cuda")
+    lg = torch.empty((wl.batch, wl.vocab), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            u.step(tok, pos, kv, lg, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        u.step(tok, pos, kv, lg, stream=s)
+    for _ in range(8):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = NvmlClockSampler(local)
+    if not sampler.ok:
+        sampler = ClockSampler(local)
+    with sampler as clocks:
+        e0.record()
+        for _ in range(steps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    u.close()
+    n_launch = 3 + 12 * wl.n_layers
+    return {"ms_per_step": ms, "us_per_token": 1e3 * ms / wl.batch, "tokens_per_s": wl.batch / (ms / 1e3),
+            "steps": steps, "launches_per_step": n_launch, "clocks": clocks.summary(), "config": config_block(wl),
+            "data": "synthetic, weights and KV filled on the device by torch's seeded generator",
+            "what": "one kernel launch per operator, one step captured in a CUDA graph and replayed"}
 
 
 def sub_records(amk, args, local):
     """The other targeted shapes on the same kernel, a few seconds each, with
-    device-filled weights (device_model)."""
+    device-filled weights (device_model): 'name' is a workload, 'name@B' the
+    workload at batch B, 'unfused:name' the per-operator path on it."""
     import synth
     import torch
     out = {}
     for name in args.sub:
-        wl = synth.workload(name)
+        if name.startswith("unfused:"):
+            out[name] = unfused_record(amk, synth.workload(name.split(":", 1)[1]), 64, local)
+            torch.cuda.empty_cache()
+            continue
+        if "@" in name:
+            base, b = name.split("@")
+            wl = synth.workload(base, batch=int(b))
+        else:
+            wl = synth.workload(name)
         dev = device_model(wl, seed=1)
         kv = device_kv(wl, seed=2, batch=wl.batch)
         eng = make_engine(amk, wl, dev, None)

@@ -54,7 +54,11 @@ typedef enum amk_status {
 
 typedef enum amk_weight_dtype {
     AMK_WEIGHT_BF16 = 0, /* bf16 matrices */
-    AMK_WEIGHT_INT8 = 1  /* W8A16: int8 matrices, one fp32 scale per output row, bf16 activations */
+    AMK_WEIGHT_INT8 = 1, /* W8A16: int8 matrices, one fp32 scale per output row, bf16 activations */
+    AMK_WEIGHT_INT4 = 2  /* W4A16 (Ada-MK summary, Key Contributions): 4-bit codes u in 0..15, value
+                            scale * (u - 8), two codes per byte with element 2j in the low nibble of byte j;
+                            one fp32 scale per group_size weights along K ([out][in / group_size]); bf16
+                            activations; batch 1 only (max_batch = 1) */
 } amk_weight_dtype;
 
 /* Model and capacity.  head_dim must be 64 or 128 and even; n_heads a
@@ -70,15 +74,18 @@ typedef struct amk_config {
     int32_t vocab;         /* V */
     float rms_eps;
     float rope_theta;      /* RoPE base; rotate-half pairs (i, i + d/2) */
-    int32_t max_batch;     /* 1..8 sequences per step */
+    int32_t max_batch;     /* 1..16 sequences per step */
     int32_t max_seq;       /* KV-cache capacity per sequence (Smax) */
     int32_t weight_dtype;  /* amk_weight_dtype */
     int32_t tied_embeddings; /* 1: the LM head is the bf16 embedding matrix */
+    int32_t group_size;    /* AMK_WEIGHT_INT4: weights per scale along K, a multiple of 32 dividing hidden,
+                              n_heads*head_dim and intermediate; 0: 128.  Ignored for other formats. */
 } amk_config;
 
 /* Device pointers of one layer, each matrix [out, in] row-major, rows
- * 16-byte aligned.  The s_* scales (fp32, one per output row) are read only
- * for AMK_WEIGHT_INT8.  Norm gains are bf16 [H]. */
+ * 16-byte aligned.  The s_* scales (fp32) are read only for the scaled
+ * formats: one per output row for AMK_WEIGHT_INT8, [out][in / group_size]
+ * for AMK_WEIGHT_INT4.  Norm gains are bf16 [H]. */
 typedef struct amk_layer_weights {
     const void *attn_norm, *mlp_norm;
     const void *wq;     /* [n_heads*d, H]    */
@@ -93,7 +100,8 @@ typedef struct amk_layer_weights {
 
 /* Whole-model weights.  `layers` is a HOST array of n_layers entries whose
  * members are device pointers.  embed is bf16 [V, H]; lm_head is [V, H] in
- * the weight dtype (ignored when tied_embeddings); s_lm its int8 row scales.
+ * the weight dtype (ignored when tied_embeddings); s_lm its scales (int8: [V];
+ * int4: [V][H / group_size]).
  * The caller keeps every weight allocated and unchanged while the handle
  * lives; the handle copies only the pointers. */
 typedef struct amk_weights {
@@ -125,6 +133,9 @@ typedef struct amk_schedule_options {
     int32_t l2_evict_first;  /* 1 or 0 (the default): ring fills carry an L2 evict-first hint, so that the
                                 once-per-step weight and KV stream does not push code and activation scratch
                                 out of L2; -1: no hint.  Results are identical either way. */
+    int32_t task_order;      /* placement of attention chunks and merges: 0 the search chooses (by the
+                                task-level simulation), 1 both spread over all CTAs in step, 2 merges on the
+                                CTAs that run no attention chunk (chunks filled from the top) */
 } amk_schedule_options;
 
 typedef struct amk_handle amk_handle;
@@ -238,10 +249,12 @@ typedef struct amk_plan_info {
     int32_t max_tasks_per_sm;
     int64_t weight_bytes;     /* linear-weight bytes streamed per step (incl. int8 scales) */
     int64_t scratch_bytes;    /* device activation scratch */
-    double modeled_us;        /* the search's cost-model estimate for one step */
+    double modeled_us;        /* the analytic per-level model's estimate for one step */
     double search_ms;         /* host time of DAG build + search + solidify + validate */
-    int32_t candidates;       /* schedule points the search evaluated */
+    int32_t candidates;       /* schedule points the search evaluated (analytic + simulated) */
     int32_t l2_evict_first;   /* 1 if ring fills carry the L2 evict-first hint */
+    double simulated_us;      /* the task-level simulation's step time for the chosen plan */
+    int32_t task_order;       /* the chosen placement (task_order values of amk_schedule_options) */
 } amk_plan_info;
 amk_status amk_get_plan_info(const amk_handle *h, amk_plan_info *info);
 

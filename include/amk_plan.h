@@ -48,7 +48,7 @@ amk_status amk_plan_validate(const amk_plan *plan, char *msg, size_t msg_len);
 amk_status amk_plan_get_info(const amk_plan *plan, amk_plan_info *info);
 
 /* Number of tasks of CTA `sm`, and one task's fields:
- * out[0] op (0 QKV, 1 ATT, 2 OPR, 3 GUP, 4 DWN, 5 LMH, 6 MRG), [1] layer, [2] r0, [3] r1,
+ * out[0] op (0 QKV, 1 ATT, 2 OPR, 3 GUP, 4 DWN, 5 LMH, 6 MRG, 7 ARG), [1] layer, [2] r0, [3] r1,
  * [4] batch row, [5] kv head (MRG: query head), [6] the dependency the task waits on
  * (-1 none), [7] its number of producer tasks, [8] number of dependencies the task
  * produces for, [9..14] those dependencies, [15] QKV matrix (0 q, 1 k, 2 v).
@@ -69,6 +69,23 @@ amk_status amk_plan_get_task(const amk_plan *plan, int32_t sm, int32_t idx, int3
  *   5 raise one wait count (a wait that can never be met)
  * `seed` picks the victim deterministically.  AMK_OK if a mutation was applied. */
 amk_status amk_plan_mutate(amk_plan *plan, int32_t kind, uint64_t seed);
+
+/* The search's task-level simulation of one decode step of a solidified
+ * plan (Ada-MK summary, Methodology, Phase I: the offline search scores
+ * candidate execution traces).  Every CTA's consumers run its tasks in order;
+ * a task starts when its CTA is free and every producer of what it waits on
+ * has finished, plus the hand-off latency; its tiles cannot finish before
+ * the CTA's loader has streamed their bytes, in task order, at the CTA's
+ * share of HBM and at most one ring ahead of what the consumers released.
+ * consts: NULL for the built-in constants (fitted to GB300), or n_consts = 14
+ * values in this order: [0] hand-off s, [1] RMSNorm prologue s, [2] copy
+ * prologue s, [3] GEMV epilogue s, [4] bf16 consumer bytes/s per CTA, [5]
+ * int8 consumer bytes/s per CTA, [6] HBM bytes/s, [7] attention prologue s,
+ * [8] attention s per (position, head, element), [9] attention epilogue s,
+ * [10] merge s, [11] s per ring stage, [12] s of prologue per further
+ * sequence at batch > 1, [13] most bytes/s one CTA's loader pulls.
+ * Writes the step time in microseconds to *step_us. */
+amk_status amk_plan_simulate(const amk_plan *plan, const double *consts, int32_t n_consts, double *step_us);
 
 /* Message of the last build/validate failure on this thread. */
 const char *amk_plan_last_message(void);

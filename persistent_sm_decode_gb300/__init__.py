@@ -18,13 +18,14 @@ from typing import Dict, List, Optional, Sequence
 
 from . import _build
 
-__all__ = ["AmkError", "Config", "ScheduleOptions", "DecodeEngine", "Plan", "lib", "build", "chrome_trace",
+__all__ = ["AmkError", "Config", "ScheduleOptions", "DecodeEngine", "UnfusedEngine", "Plan", "lib", "build",
+           "chrome_trace",
            "level_times",
            "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_OOM", "ERR_SCHEDULE",
-           "ERR_COOPERATIVE", "ERR_TIMEOUT", "WEIGHT_BF16", "WEIGHT_INT8"]
+           "ERR_COOPERATIVE", "ERR_TIMEOUT", "WEIGHT_BF16", "WEIGHT_INT8", "WEIGHT_INT4"]
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_SCHEDULE, ERR_COOPERATIVE, ERR_TIMEOUT = range(8)
-WEIGHT_BF16, WEIGHT_INT8 = 0, 1
+WEIGHT_BF16, WEIGHT_INT8, WEIGHT_INT4 = 0, 1, 2
 OPS = ("QKV", "ATT", "OPR", "GUP", "DWN", "LMH", "MRG", "ARG")
 
 i32, i64, f32, f64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_double, ctypes.c_void_p
@@ -33,7 +34,8 @@ i32, i64, f32, f64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.
 class Config(ctypes.Structure):
     _fields_ = [("n_layers", i32), ("hidden", i32), ("n_heads", i32), ("n_kv_heads", i32), ("head_dim", i32),
                 ("intermediate", i32), ("vocab", i32), ("rms_eps", f32), ("rope_theta", f32),
-                ("max_batch", i32), ("max_seq", i32), ("weight_dtype", i32), ("tied_embeddings", i32)]
+                ("max_batch", i32), ("max_seq", i32), ("weight_dtype", i32), ("tied_embeddings", i32),
+                ("group_size", i32)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -49,7 +51,7 @@ class Weights(ctypes.Structure):
 class ScheduleOptions(ctypes.Structure):
     _fields_ = [("n_sm", i32), ("att_chunks", i32), ("slot_bytes", i32), ("n_slots", i32), ("ksplit", i32),
                 ("scratch_depth", i32), ("l2_prefetch_kb", i32), ("trace", i32), ("wait_timeout_ns", i64),
-                ("l2_evict_first", i32)]
+                ("l2_evict_first", i32), ("task_order", i32)]
 
 
 class ErrorInfo(ctypes.Structure):
@@ -62,7 +64,7 @@ class PlanInfo(ctypes.Structure):
                                    "n_slots", "ksplit", "scratch_depth", "att_tile", "smem_bytes",
                                    "max_tasks_per_sm")] + \
                [("weight_bytes", i64), ("scratch_bytes", i64), ("modeled_us", f64), ("search_ms", f64),
-                ("candidates", i32), ("l2_evict_first", i32)]
+                ("candidates", i32), ("l2_evict_first", i32), ("simulated_us", f64), ("task_order", i32)]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -116,11 +118,17 @@ def lib():
             L.amk_plan_get_task.argtypes = [vp, i32, i32, ctypes.POINTER(i32)]
             L.amk_plan_mutate.argtypes = [vp, i32, ctypes.c_uint64]
             L.amk_plan_last_message.restype = ctypes.c_char_p
+            L.amk_plan_simulate.argtypes = [vp, ctypes.POINTER(f64), i32, ctypes.POINTER(f64)]
+            L.amk_plan_simulate.restype = ctypes.c_int
             L.amk_plan_destroy.argtypes = [vp]
             L.amk_plan_destroy.restype = None
+            L.amk_unfused_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), ctypes.POINTER(vp)]
+            L.amk_unfused_decode_step.argtypes = [vp, i32, vp, vp, vp, vp, vp]
+            L.amk_unfused_destroy.argtypes = [vp]
             for f in ("amk_create", "amk_decode_step", "amk_decode_step_greedy", "amk_decode_step_noalloc", "amk_sync_status", "amk_destroy", "amk_last_error",
                       "amk_get_plan_info", "amk_debug_drop_signal", "amk_debug_read_residuals", "amk_debug_read_trace", "amk_plan_build", "amk_plan_validate",
-                      "amk_plan_get_info", "amk_plan_get_task", "amk_plan_mutate"):
+                      "amk_plan_get_info", "amk_plan_get_task", "amk_plan_mutate", "amk_unfused_create",
+                      "amk_unfused_decode_step", "amk_unfused_destroy"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -141,9 +149,10 @@ def _options(opts: Optional[dict]) -> Optional[ScheduleOptions]:
 
 
 def make_config(n_layers, hidden, n_heads, n_kv_heads, head_dim, intermediate, vocab, max_seq, max_batch=1,
-                rms_eps=1e-5, rope_theta=1e4, int8=False, tied=False) -> Config:
+                rms_eps=1e-5, rope_theta=1e4, int8=False, tied=False, int4=False, group_size=0) -> Config:
+    wd = WEIGHT_INT4 if int4 else WEIGHT_INT8 if int8 else WEIGHT_BF16
     return Config(n_layers, hidden, n_heads, n_kv_heads, head_dim, intermediate, vocab, rms_eps, rope_theta,
-                  max_batch, max_seq, WEIGHT_INT8 if int8 else WEIGHT_BF16, int(bool(tied)))
+                  max_batch, max_seq, wd, int(bool(tied)), int(group_size))
 
 
 # --------------------------------------------------------------- planner
@@ -181,6 +190,15 @@ class Plan:
             out.append({"op": OPS[v[0]], "layer": v[1], "r0": v[2], "r1": v[3], "b": v[4], "g": v[5],
                         "wait": v[6], "wait_count": v[7], "sig": v[9:9 + v[8]], "mat": v[15]})
         return out
+
+    def simulate(self, consts: Optional[Sequence[float]] = None) -> float:
+        """The task-level simulation's step time (µs) under the built-in cost
+        constants, or under `consts` (14 values; see amk_plan_simulate)."""
+        out = f64()
+        arr = None if consts is None else (f64 * len(consts))(*consts)
+        _check(lib().amk_plan_simulate(self._p, arr, 0 if consts is None else len(consts), ctypes.byref(out)),
+               "amk_plan_simulate")
+        return out.value
 
     def mutate(self, kind: int, seed: int) -> int:
         return lib().amk_plan_mutate(self._p, kind, seed)
@@ -388,6 +406,43 @@ def level_times(trace, plan: "Plan") -> List[dict]:
         out.append({"layer": k[0], "op": k[1], "end_ns": ends[k], "level_us": (ends[k] - base) / 1e3})
         prev = ends[k]
     return out
+
+
+class UnfusedEngine:
+    """The same decode step as one kernel launch per operator
+    (include/amk_unfused.h), for comparison with DecodeEngine on the same
+    device and data.  Arguments as for DecodeEngine; ``step`` as
+    DecodeEngine.step."""
+
+    def __init__(self, cfg: Config, embed, final_norm, layers: Sequence[Dict], lm_head=None, s_lm=None):
+        self.cfg = cfg
+        self._keep = [embed, final_norm, lm_head, s_lm] + [v for d in layers for v in d.values()]
+        arr = (LayerWeights * cfg.n_layers)()
+        for l, d in enumerate(layers):
+            for k in _LAYER_KEYS + _SCALE_KEYS:
+                setattr(arr[l], k, _ptr(d.get(k)))
+        self._arr = arr
+        w = Weights(_ptr(embed), _ptr(final_norm), _ptr(lm_head), _ptr(s_lm), arr)
+        self._h = vp()
+        _check(lib().amk_unfused_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(self._h)),
+               "amk_unfused_create")
+
+    def step(self, tokens, positions, kv_cache, logits, stream=None, batch: Optional[int] = None) -> None:
+        B = int(tokens.numel()) if batch is None else int(batch)
+        s = None if stream is None else (stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+        _check(lib().amk_unfused_decode_step(self._h, B, _ptr(tokens), _ptr(positions), _ptr(kv_cache),
+                                             _ptr(logits), s), "amk_unfused_decode_step")
+
+    def close(self) -> None:
+        if self._h:
+            lib().amk_unfused_destroy(self._h)
+            self._h = vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def decode_step_noalloc(cfg: Config, embed, final_norm, layers: Sequence[Dict], tokens, positions, kv_cache,

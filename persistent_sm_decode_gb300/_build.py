@@ -16,7 +16,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libamk.so")
 
-SOURCES = ["amk_kernel.cu", "amk_api.cpp", "amk_plan.cpp", "amk_noalloc.cu"]
+SOURCES = ["amk_kernel.cu", "amk_api.cpp", "amk_plan.cpp", "amk_noalloc.cu", "amk_unfused.cu"]
 HEADERS = ["amk_internal.h", "amk_launch.h", "amk_plan_impl.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -41,7 +41,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     AMK_L2_PREFETCH=1 the one with the loader's L2 prefetch (schedule option
     ``l2_prefetch_kb``)."""
     os.makedirs(OBJ, exist_ok=True)
-    hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, h) for h in ("amk.h", "amk_plan.h")]
+    hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, h)
+                                                       for h in ("amk.h", "amk_plan.h", "amk_unfused.h")]
     flags = list(extra_flags)
     if os.environ.get("AMK_TRACE", "0") not in ("", "0"):
         flags.append("-DAMK_TRACE_CODE=1")

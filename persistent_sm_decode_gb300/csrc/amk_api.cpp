@@ -67,7 +67,7 @@ void free_handle(amk_handle *h) {
 
 amk_status check_weights(const amk_config &c, const amk_weights *w) {
     if (!w || !w->embed || !w->final_norm || !w->layers) return AMK_ERR_INVALID_ARG;
-    const bool i8 = c.weight_dtype == AMK_WEIGHT_INT8;
+    const bool i8 = c.weight_dtype == AMK_WEIGHT_INT8 || c.weight_dtype == AMK_WEIGHT_INT4; /* scaled formats */
     if (!aligned16(w->embed) || !aligned16(w->final_norm)) return AMK_ERR_INVALID_ARG;
     if (!c.tied_embeddings) {
         if (!w->lm_head || !aligned16(w->lm_head)) return AMK_ERR_INVALID_ARG;
@@ -143,7 +143,7 @@ amk_status amk_create(const amk_config *config, const amk_weights *weights, cons
     const amk_plan &P = *h->plan;
 
     /* the sm_103a image must exist for this device; no other path is built */
-    h->fn = select_kernel(config->weight_dtype == AMK_WEIGHT_INT8, config->max_batch);
+    h->fn = select_kernel(config->weight_dtype, config->max_batch);
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, (const void *)h->fn) != cudaSuccess) {
         cudaGetLastError();
@@ -245,8 +245,9 @@ amk_status amk_create(const amk_config *config, const amk_weights *weights, cons
     p.qkv_rows = g.qkv_rows;
     p.eps = config->rms_eps;
     p.qk_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
-    p.wint8 = g.i8;
-    p.lm_int8 = g.lm_i8;
+    p.wf = g.wf;
+    p.lm_wf = g.lm_wf;
+    p.group = g.group;
     p.tasks = h->d_tasks;
     p.task_start = h->d_start;
     p.C = P.k.C;

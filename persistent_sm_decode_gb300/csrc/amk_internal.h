@@ -35,7 +35,7 @@ constexpr uint16_t NO_WAIT = 0xFFFFu;
 constexpr int MAX_SIG = 6;
 constexpr int NCW = 8;                    /* consumer warps per CTA */
 constexpr int NTHREADS = (NCW + 1) * 32;  /* + one loader warp */
-constexpr int MAXB = 8;                   /* sequences per step */
+constexpr int MAXB = 16;                  /* sequences per step (the M of one tensor-core tile) */
 constexpr int MAX_SLOTS = 32;
 constexpr int PART_PAD = 4;               /* attention partial: o[d], m, l, 2 pad floats */
 constexpr int ERR_WORDS = 8;
@@ -65,7 +65,7 @@ static_assert(sizeof(Task) == 48, "Task layout");
 /* Device pointers of one layer. */
 struct LayerPtrs {
     const void *w[7];        /* wq, wk, wv, wo, w_gate, w_up, w_down */
-    const float *s[7];       /* int8 row scales, same order */
+    const float *s[7];       /* int8 row scales or int4 group scales [rows][K / group], same order */
     const uint16_t *attn_norm, *mlp_norm;
 };
 enum : int { W_Q = 0, W_K = 1, W_V = 2, W_O = 3, W_GATE = 4, W_UP = 5, W_DOWN = 6 };
@@ -76,7 +76,8 @@ struct Params {
     int L, H, nq, nkv, d, I, V, G, Bmax, Smax, qkv_rows;
     float eps;
     float qk_scale_log2;     /* log2(e) / sqrt(d) */
-    int wint8, lm_int8;
+    int wf, lm_wf;       /* weight format of the layer matrices and of the LM head (WF_*) */
+    int group;           /* WF_I4: weights per scale along K */
     /* schedule */
     const Task *tasks;
     const int32_t *task_start; /* [n_sm + 1] */
@@ -126,6 +127,14 @@ struct Params {
     unsigned long long *trace; /* NULL, or [n_tasks][16] timings */
 };
 
+/* Weight formats: bf16; int8 with one fp32 scale per output row (W8A16);
+ * 4-bit codes around the zero point 8, two per byte (element 2j in the low
+ * nibble of byte j), with one fp32 scale per `group` weights along K
+ * (W4A16).  A 16-byte chunk holds wf_epc weights. */
+enum : int { WF_BF16 = 0, WF_I8 = 1, WF_I4 = 2 };
+AMK_HD constexpr int wf_epc(int wf) { return wf == WF_BF16 ? 8 : wf == WF_I8 ? 16 : 32; }
+AMK_HD constexpr long long wf_bytes(int wf, long long k) { return k * 16 / wf_epc(wf); }
+
 /* Batch-1 GEMV.  A task's prologue writes the bf16 activations of its K
  * slice to shared memory once; then every consumer warp copies the part it
  * multiplies into registers.  A row of the K slice is cut into S segments
@@ -141,24 +150,28 @@ struct Params {
  * while a tile has too few rows to give every warp work. */
 constexpr int JMAX_BF16 = 8;
 constexpr int JMAX_INT8 = 2;
+constexpr int JMAX_INT4 = 2;
 constexpr int RPG1 = 1;
+AMK_HD constexpr int wf_jmax(int wf) { return wf == WF_BF16 ? JMAX_BF16 : wf == WF_I8 ? JMAX_INT8 : JMAX_INT4; }
 
 /* chunks per lane J of a batch-1 segment (0: the slice is too long) */
-AMK_HD inline int gemv_lane_chunks(int Kc, int S, bool int8) {
-    const int epc = int8 ? 16 : 8;
-    const int nch = Kc / epc;
+AMK_HD inline int gemv_lane_chunks(int Kc, int S, int wf) {
+    const int nch = Kc / wf_epc(wf);
     const int per = (nch + S - 1) / S;
     const int J = (per + 31) / 32;
-    return J > (int8 ? JMAX_INT8 : JMAX_BF16) ? 0 : J;
+    return J > wf_jmax(wf) ? 0 : J;
 }
 
-/* K segments per row.  Batch 1 as above; larger batches read activations
- * from shared memory and use 8 / rows_per_stage segments when a tile has
+/* K segments per row.  Batch 1 as above.  Larger batches read activations
+ * from shared memory: bf16 weights go through the tensor cores with each of
+ * the 8 warps taking one K segment of every row block (S = 8); int8 weights
+ * use the CUDA-core tile with 8 / rows_per_stage segments when a tile has
  * fewer than 8 rows. */
-AMK_HD inline int gemv_segments(int batch_max, int Kc, bool int8, int rows_per_stage) {
+AMK_HD inline int gemv_segments(int batch_max, int Kc, int wf, int rows_per_stage) {
+    if (batch_max > 1 && wf == WF_BF16) return NCW;
     if (batch_max == 1) {
         int S = 1;
-        while (S < NCW && gemv_lane_chunks(Kc, S, int8) == 0) S *= 2;
+        while (S < NCW && gemv_lane_chunks(Kc, S, wf) == 0) S *= 2;
         /* every warp gets rows: (8 / S) row groups of RPG1 rows per round */
         while (S < NCW && rows_per_stage < (NCW / S) * RPG1) S *= 2;
         return S;
@@ -183,7 +196,15 @@ AMK_HD inline int att_max_chunks(int d) { return (NCW * 32 / (d / 4)) * MRG_MAX_
 
 /* shared-memory layout (bytes), common to host sizing and device carving */
 constexpr int SMEM_BARRIERS = 2 * MAX_SLOTS * 8;
-constexpr int SMEM_MISC = 1024;
+constexpr int SMEM_MISC = 2048;
+
+/* At batch above 1, every weight row of a ring slot and every activation row
+ * of the K slice sits in shared memory at a pitch of its bytes rounded up to
+ * 128 plus 32: the rows that one tensor-core fragment load reads (four rows,
+ * 32 bytes apart in K) then fall on distinct banks. */
+AMK_HD inline int smem_pitch(int row_bytes, int batch_max) {
+    return batch_max > 1 ? (row_bytes + 127) / 128 * 128 + 32 : row_bytes;
+}
 
 AMK_HD inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 

@@ -213,6 +213,7 @@ struct Misc {
     float rnorm[MAXB];
     float argv[NCW * MAXB]; /* greedy feedback: per-warp best value and row */
     int argi[NCW * MAXB];
+    uint32_t epoch_base;    /* epoch * (L + 1) of the step this CTA runs */
     unsigned long long t_first;     /* trace: first tile of the current task arrived */
     unsigned long long t_wait_full; /* trace: consumer warp 0 waiting for tiles (ns) */
     unsigned long long t_tiles;     /* trace: consumer warp 0 computing tiles (ns) */
@@ -283,11 +284,14 @@ __device__ __forceinline__ bool stage_ready(const Params &p, Smem &s, uint64_t *
 /* Which activation buffer a poll waits on (reported in the error word). */
 enum : int { WB_XIN = 0, WB_XMID = 1, WB_QKV = 2, WB_PART = 3, WB_AOUT = 4, WB_ACT = 5, WB_ARGP = 6 };
 
-/* epoch * (L + 1) of the step this CTA runs, set once at kernel start */
-__shared__ uint32_t s_epoch_base;
+/* the CTA's dynamic shared memory (barriers first, then Misc) */
+extern __shared__ __align__(1024) uint8_t smem[];
 
-/* flag of the current step for data of layer `version` */
-__device__ __forceinline__ uint32_t ver(const Params &, int version) { return s_epoch_base + (uint32_t)version; }
+/* flag of the current step for data of layer `version`: Misc holds epoch *
+ * (L + 1) of the step this CTA runs, set once at kernel start */
+__device__ __forceinline__ uint32_t ver(const Params &, int version) {
+    return reinterpret_cast<const Misc *>(smem + SMEM_BARRIERS)->epoch_base + (uint32_t)version;
+}
 
 __device__ __forceinline__ bool ll_ok(uint32_t f, const ulonglong2 &v) { return ll_flag(v.x) == f && ll_flag(v.y) == f; }
 
@@ -472,7 +476,7 @@ __device__ bool task_range(const Params &p, const Task &t, int idx, const uint8_
         return true;
     }
     const GemvGeo g = gemv_geo(p, t);
-    const size_t rowb = (size_t)g.K * ((t.op == OP_LMH ? p.lm_int8 : p.wint8) ? 1 : 2);
+    const size_t rowb = (size_t)wf_bytes(t.op == OP_LMH ? p.lm_wf : p.wf, g.K);
     if (g.ks > 1) {
         if (idx >= g.nmat) return false;
         ptr = op_weights(p, t, idx) + (size_t)t.r0 * rowb;
@@ -590,9 +594,11 @@ __device__ void loader(const Params &p, Smem &s, int tbeg, int tend) {
             continue;
         }
         const GemvGeo g = gemv_geo(p, t);
-        const int web = (t.op == OP_LMH ? p.lm_int8 : p.wint8) ? 1 : 2;
+        const int wf = t.op == OP_LMH ? p.lm_wf : p.wf;
         const uint8_t *W[2] = {op_weights(p, t, 0), op_weights(p, t, g.nmat - 1)};
-        const size_t rowb = (size_t)g.K * web, segb = (size_t)g.Kc * web;
+        const size_t rowb = (size_t)wf_bytes(wf, g.K), segb = (size_t)wf_bytes(wf, g.Kc);
+        /* batch 1: rows back to back; larger batches: rows at the padded pitch */
+        const size_t pitch = (size_t)smem_pitch((int)segb, p.Bmax);
         for (int kp = 0; kp < g.ks; ++kp) {
             for (int rb = 0; rb < g.nrb; ++rb) {
                 int ra, re;
@@ -606,12 +612,12 @@ __device__ void loader(const Params &p, Smem &s, int tbeg, int tend) {
                         s.misc->issued = (int)r.count;
                         return;
                     }
-                    if (g.ks == 1) {
+                    if (g.ks == 1 && pitch == segb) {
                         ring_copy(dst, W[m] + (size_t)ra * rowb, bytes, &s.full[r.slot], hint, pol);
                     } else {
                         const uint8_t *src = W[m] + (size_t)ra * rowb + (size_t)kp * segb;
                         for (int q = 0; q < re - ra; ++q)
-                            ring_copy(dst + (size_t)q * segb, src + (size_t)q * rowb, (uint32_t)segb, &s.full[r.slot],
+                            ring_copy(dst + (size_t)q * pitch, src + (size_t)q * rowb, (uint32_t)segb, &s.full[r.slot],
                                       hint, pol);
                     }
                     r.advance(NS);
@@ -735,12 +741,12 @@ __device__ void norm_prologue(const Params &p, Smem &s, const uint64_t *xbase, b
         }
         cbar();
     }
-    const int kc = k1 - k0, a4 = k0 / 4, n4 = kc / 4;
+    const int kc = k1 - k0, a4 = k0 / 4, n4 = kc / 4, apitch = smem_pitch(kc * 2, p.Bmax);
     for (int b = 0; b < p.batch; ++b) {
         const uint64_t *xs = from_embed ? nullptr : xbase + (size_t)b * H;
         const uint16_t *emb = from_embed ? p.embed + (size_t)__ldg(p.tokens + b) * H : nullptr;
         const float r = s.misc->rnorm[b];
-        uint2 *dst = reinterpret_cast<uint2 *>(s.act + (size_t)b * kc * 2);
+        uint2 *dst = reinterpret_cast<uint2 *>(s.act + (size_t)b * apitch);
         for (int i0 = ctid; i0 < n4; i0 += XU * TS) {
             float4 x[XU];
             load_x4s<XU>(p, s, xs, emb, [=](int u) { return i0 + u * TS < n4 ? a4 + i0 + u * TS : -1; }, x, f, task,
@@ -767,11 +773,11 @@ constexpr int CU = 8;
 __device__ void copy_prologue(const Params &p, Smem &s, const uint64_t *src0, int len, int k0, int k1, uint32_t f,
                               int task, int which, int ctid) {
     constexpr int TS = NCW * 32;
-    const int kc = k1 - k0, n4 = kc / 4;
+    const int kc = k1 - k0, n4 = kc / 4, apitch = smem_pitch(kc * 2, p.Bmax);
     for (int b = 0; b < p.batch; ++b) {
         /* word pair i of the slice holds elements k0 + 4 i .. k0 + 4 i + 3 */
         const uint64_t *sb = src0 + ((size_t)b * len + k0) / 2;
-        uint2 *dst = reinterpret_cast<uint2 *>(s.act + (size_t)b * kc * 2);
+        uint2 *dst = reinterpret_cast<uint2 *>(s.act + (size_t)b * apitch);
         for (int i0 = ctid; i0 < n4; i0 += CU * TS) {
             ulonglong2 v[CU];
             uint32_t pend = 0u;
@@ -847,29 +853,31 @@ __device__ __forceinline__ float dot_chunk(const uint4 &w, const uint32_t *h) {
     return s0 + s1;
 }
 
-/* Batched tile: activations act[b][0..Kc) in shared memory.  With S > 1
+/* Batched CUDA-core tile (int8 weights): activations act[b][0..Kc) at
+ * `apitch` bytes per sequence, weight rows at `wpitch` bytes.  With S > 1
  * segments per row warp w takes row w / S, K segment w % S; with S == 1 warp
  * w takes rows w, w + 8, ...  Partial sums go to res[(seg * sstride + row) * Bmax + b]
  * (accumulating over K-split passes); the epilogue adds the S segments in a
  * fixed order, so results do not depend on timing. */
 template <bool I8, int NB>
-__device__ void gemv_tile(const uint8_t *tile, int nrows, int S, int Kc, const uint32_t *act, int batch, float *res,
-                          int sstride, int Bmax, bool first, int warp, int lane) {
+__device__ void gemv_tile(const uint8_t *tile, int nrows, int S, int Kc, int wpitch, const uint8_t *act, int apitch,
+                          int batch, float *res, int sstride, int Bmax, bool first, int warp, int lane) {
     constexpr int EPC = I8 ? 16 : 8;
     const int nch = Kc / EPC;
-    const size_t rowb = (size_t)Kc * (I8 ? 1 : 2);
     const int RG = NCW / S, seg = warp % S;
     const int c0 = seg * nch / S, c1 = (seg + 1) * nch / S;
     for (int rr = warp / S; rr < nrows; rr += RG) {
         float a[NB];
 #pragma unroll
         for (int b = 0; b < NB; ++b) a[b] = 0.f;
-        const uint4 *w = reinterpret_cast<const uint4 *>(tile + rr * rowb);
+        const uint4 *w = reinterpret_cast<const uint4 *>(tile + (size_t)rr * wpitch);
         for (int c = c0 + lane; c < c1; c += 32) {
             const uint4 wv = w[c];
 #pragma unroll
             for (int b = 0; b < NB; ++b)
-                if (b < batch) a[b] += dot_chunk<I8>(wv, act + ((size_t)b * Kc + (size_t)c * EPC) / 2);
+                if (b < batch)
+                    a[b] += dot_chunk<I8>(wv, reinterpret_cast<const uint32_t *>(act + (size_t)b * apitch) +
+                                                  (size_t)c * EPC / 2);
         }
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
@@ -878,6 +886,73 @@ __device__ void gemv_tile(const uint8_t *tile, int nrows, int S, int Kc, const u
                 if (lane == 0) {
                     float *r = res + ((size_t)seg * sstride + rr) * Bmax + b;
                     *r = first ? v : *r + v;
+                }
+            }
+        }
+    }
+}
+
+/* D += A.B on the tensor cores: m16n8k16, bf16 operands, fp32 accumulators */
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+/* Batched tensor-core tile (bf16 weights, batch 2..16).  One m16n8k16 takes
+ * the activations as A (M = the sequences, rows 8..15 zero up to batch 8)
+ * and 8 weight rows as B (N = 8 output rows), so D holds 8 outputs of every
+ * sequence.  The sum over K is the same for any order of K, so each k16 step
+ * pairs A and B through one permutation: thread t of a fragment row supplies
+ * the four consecutive elements 4t .. 4t + 3 (one 8-byte shared load) where
+ * the fragment layout names elements 2t, 2t + 1, 2t + 8, 2t + 9.  Warp w
+ * takes K segment w of 8 for every row block of the stage, up to RB row
+ * blocks at once: one activation load serves them all and their
+ * accumulators form independent chains.  res[(w * sstride + row) * Bmax + b]
+ * receives the warp's partial sums (added over K-split passes). */
+template <int NB>
+__device__ void gemv_tile_mma(const uint8_t *tile, int nrows, int Kc, int wpitch, const uint8_t *act, int apitch,
+                              int batch, float *res, int sstride, int Bmax, bool first, int warp, int lane) {
+    constexpr int RB = 4;
+    const int g = lane >> 2, t = lane & 3;
+    const int nblk = Kc / 16, k0 = warp * nblk / NCW, k1 = (warp + 1) * nblk / NCW;
+    const bool lo = g < batch, hi = NB > 8 && g + 8 < batch;
+    const uint8_t *x0 = act + (size_t)g * apitch + 8 * t;
+    const uint8_t *x1 = act + (size_t)(g + 8) * apitch + 8 * t;
+    for (int rb0 = 0; rb0 < nrows; rb0 += 8 * RB) {
+        float d[RB][4];
+        const uint8_t *wr[RB];
+        bool rok[RB];
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            d[r][0] = d[r][1] = d[r][2] = d[r][3] = 0.f;
+            rok[r] = rb0 + 8 * r + g < nrows;
+            wr[r] = tile + (size_t)(rb0 + 8 * r + g) * wpitch + 8 * t;
+        }
+        const int nrb = min(RB, (nrows - rb0 + 7) / 8); /* warp-uniform: row blocks with rows */
+#pragma unroll 2
+        for (int kb = k0; kb < k1; ++kb) {
+            const uint2 a = lo ? *reinterpret_cast<const uint2 *>(x0 + 32 * kb) : make_uint2(0u, 0u);
+            const uint2 c = hi ? *reinterpret_cast<const uint2 *>(x1 + 32 * kb) : make_uint2(0u, 0u);
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                if (r >= nrb) break;
+                const uint2 w = rok[r] ? *reinterpret_cast<const uint2 *>(wr[r] + 32 * kb) : make_uint2(0u, 0u);
+                mma_bf16_16816(d[r], a.x, c.x, a.y, c.y, w.x, w.y);
+            }
+        }
+        /* d0, d1: sequence g, rows 2t, 2t + 1 of the block; d2, d3: sequence g + 8 */
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int b = g + (q >= 2 ? 8 : 0), rr = rb0 + 8 * r + 2 * t + (q & 1);
+                if (b < batch && rr < nrows) {
+                    float *o = res + ((size_t)warp * sstride + rr) * Bmax + b;
+                    *o = first ? d[r][q] : *o + d[r][q];
                 }
             }
         }
@@ -937,15 +1012,12 @@ __device__ __forceinline__ void fma_f32x2(float &s0, float &s1, float a, float b
 }
 
 /* Activations matching one 16-byte weight chunk, in registers, bf16 packed
- * two per word in element order: eight values for bf16 weights, sixteen for
- * int8 weights. */
-template <bool I8>
+ * two per word: eight values for bf16 weights, sixteen for int8, thirty-two
+ * for int4 (whose pairs are ordered to match the weight pairs that
+ * acc_chunk_i4 forms: see act_regs). */
+template <int WF>
 struct ActChunk {
-    uint32_t w[4];
-};
-template <>
-struct ActChunk<true> {
-    uint32_t w[8];
+    uint32_t w[wf_epc(WF) / 2];
 };
 
 /* (s0, s1) += one 16-byte weight chunk . its activations (fp32 sums; the
@@ -954,7 +1026,7 @@ struct ActChunk<true> {
  * the packed subtraction removes 2^23 + 128 (exact for every int8), and the
  * packed FMA takes two products at once; `hf` holds the sixteen activations
  * already widened to fp32 (once per chunk, for all rows of a group). */
-__device__ __forceinline__ void acc_chunk(float &s0, float &s1, const uint4 &w, const ActChunk<false> &h) {
+__device__ __forceinline__ void acc_chunk(float &s0, float &s1, const uint4 &w, const ActChunk<WF_BF16> &h) {
     fma_bf16_lo(s0, w.x, h.w[0]);
     fma_bf16_hi(s1, w.x, h.w[0]);
     fma_bf16_lo(s0, w.y, h.w[1]);
@@ -979,12 +1051,49 @@ __device__ __forceinline__ void acc_chunk_i8(float &s0, float &s1, const uint4 &
     }
 }
 
+/* bf16 pair (x, y) -= (8, 8)... as a packed bf16 subtraction: (128 + u) - 136
+ * is u - 8, exact for every 4-bit code u */
+__device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+/* int4: one word holds elements 0..7 of its group of eight, byte j holding
+ * elements 2j (low nibble) and 2j + 1 (high nibble).  t = the low nibbles
+ * (elements 0, 2, 4, 6 in bytes 0..3), u = the high nibbles (1, 3, 5, 7); a
+ * byte-permute against 0x43 bytes makes bf16 pairs 128 + code, which the
+ * packed subtraction turns into code - 8 exactly.  The pairs come out as
+ * (0, 2), (4, 6), (1, 3), (5, 7): act_regs stores the activations in that
+ * order, so each pair meets its activations in one mixed-precision FMA. */
+__device__ __forceinline__ void acc_chunk_i4(float &s0, float &s1, const uint4 &w, const ActChunk<WF_I4> &h) {
+    const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t t = x[q] & 0x0F0F0F0Fu, u = (x[q] >> 4) & 0x0F0F0F0Fu;
+        const uint32_t p02 = sub_bf16x2(__byte_perm(t, 0x43434343u, 0x4140u), 0x43084308u);
+        const uint32_t p46 = sub_bf16x2(__byte_perm(t, 0x43434343u, 0x4342u), 0x43084308u);
+        const uint32_t p13 = sub_bf16x2(__byte_perm(u, 0x43434343u, 0x4140u), 0x43084308u);
+        const uint32_t p57 = sub_bf16x2(__byte_perm(u, 0x43434343u, 0x4342u), 0x43084308u);
+        fma_bf16_lo(s0, p02, h.w[4 * q]);
+        fma_bf16_hi(s1, p02, h.w[4 * q]);
+        fma_bf16_lo(s0, p46, h.w[4 * q + 1]);
+        fma_bf16_hi(s1, p46, h.w[4 * q + 1]);
+        fma_bf16_lo(s0, p13, h.w[4 * q + 2]);
+        fma_bf16_hi(s1, p13, h.w[4 * q + 2]);
+        fma_bf16_lo(s0, p57, h.w[4 * q + 3]);
+        fma_bf16_hi(s1, p57, h.w[4 * q + 3]);
+    }
+}
+
 /* This warp's activations from the benchmark's bf16 slice in shared memory:
- * chunk j of the lane is chunk c0 + lane + 32 j of the row (zero past c1). */
-template <bool I8>
-__device__ __forceinline__ void act_regs(const uint8_t *act, int c0, int c1, ActChunk<I8> (&hv)[I8 ? JMAX_INT8 : JMAX_BF16],
+ * chunk j of the lane is chunk c0 + lane + 32 j of the row (zero past c1).
+ * For int4, each group of eight activations (h0 .. h7, four words) is
+ * reordered to the pairs (h0, h2), (h4, h6), (h1, h3), (h5, h7). */
+template <int WF>
+__device__ __forceinline__ void act_regs(const uint8_t *act, int c0, int c1, ActChunk<WF> (&hv)[wf_jmax(WF)],
                                          int lane) {
-    constexpr int JM = I8 ? JMAX_INT8 : JMAX_BF16, NQ = I8 ? 2 : 1;
+    constexpr int JM = wf_jmax(WF), NQ = wf_epc(WF) / 8;
     const uint4 *A = reinterpret_cast<const uint4 *>(act);
 #pragma unroll
     for (int j = 0; j < JM; ++j) {
@@ -992,10 +1101,17 @@ __device__ __forceinline__ void act_regs(const uint8_t *act, int c0, int c1, Act
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
             const uint4 v = c < c1 ? A[(size_t)c * NQ + q] : make_uint4(0u, 0u, 0u, 0u);
-            hv[j].w[4 * q] = v.x;
-            hv[j].w[4 * q + 1] = v.y;
-            hv[j].w[4 * q + 2] = v.z;
-            hv[j].w[4 * q + 3] = v.w;
+            if constexpr (WF == WF_I4) {
+                hv[j].w[4 * q] = __byte_perm(v.x, v.y, 0x5410u);     /* (h0, h2) */
+                hv[j].w[4 * q + 1] = __byte_perm(v.z, v.w, 0x5410u); /* (h4, h6) */
+                hv[j].w[4 * q + 2] = __byte_perm(v.x, v.y, 0x7632u); /* (h1, h3) */
+                hv[j].w[4 * q + 3] = __byte_perm(v.z, v.w, 0x7632u); /* (h5, h7) */
+            } else {
+                hv[j].w[4 * q] = v.x;
+                hv[j].w[4 * q + 1] = v.y;
+                hv[j].w[4 * q + 2] = v.z;
+                hv[j].w[4 * q + 3] = v.w;
+            }
         }
     }
 }
@@ -1005,12 +1121,15 @@ __device__ __forceinline__ void act_regs(const uint8_t *act, int c0, int c1, Act
  * k * RG * RPG1 (g = w / S its row group, RG = 8 / S groups): RPG1 rows at a
  * time, each lane summing its chunks of those rows into two accumulators per
  * row, then one transposing reduction for the group.  res[seg * sstride + row]
- * receives the segment's sum (first K slice) or has it added (later ones). */
-template <bool I8>
+ * receives the segment's sum (first K slice) or has it added (later ones).
+ * int4: each chunk's sum is multiplied by its group's scale, sc[row * ng +
+ * (kbase + 32 c) / group] (the task's scales in shared memory). */
+template <int WF>
 __device__ __forceinline__ void gemv_stage1(const uint8_t *tile, int nrows, int RG, int rgp, int rowc, int c0, int c1,
-                                            const ActChunk<I8> (&hv)[I8 ? JMAX_INT8 : JMAX_BF16], float *res,
-                                            int sstride, int seg, bool first, int lane) {
-    constexpr int JM = I8 ? JMAX_INT8 : JMAX_BF16, RPG = RPG1;
+                                            const ActChunk<WF> (&hv)[wf_jmax(WF)], float *res, int sstride, int seg,
+                                            bool first, int lane, const float *sc = nullptr, int ng = 0,
+                                            int kbase = 0, int group = 1) {
+    constexpr int JM = wf_jmax(WF), RPG = RPG1;
     const uint4 *W = reinterpret_cast<const uint4 *>(tile);
 #pragma unroll 1
     for (int r0 = rgp * RPG; r0 < nrows; r0 += RG * RPG) {
@@ -1028,7 +1147,7 @@ __device__ __forceinline__ void gemv_stage1(const uint8_t *tile, int nrows, int 
 #pragma unroll
             for (int i = 0; i < RPG; ++i)
                 wv[i] = (r0 + i < nrows && c < c1) ? W[(size_t)(r0 + i) * rowc + c] : make_uint4(0u, 0u, 0u, 0u);
-            if constexpr (I8) {
+            if constexpr (WF == WF_I8) {
                 float hf[16];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
@@ -1037,6 +1156,16 @@ __device__ __forceinline__ void gemv_stage1(const uint8_t *tile, int nrows, int 
                 }
 #pragma unroll
                 for (int i = 0; i < RPG; ++i) acc_chunk_i8(a0[i], a1[i], wv[i], hf);
+            } else if constexpr (WF == WF_I4) {
+                const int gi = (kbase + 32 * c) / group;
+#pragma unroll
+                for (int i = 0; i < RPG; ++i) {
+                    float t0 = 0.f, t1 = 0.f;
+                    acc_chunk_i4(t0, t1, wv[i], hv[j]);
+                    const float scl = (r0 + i < nrows && c < c1) ? sc[(size_t)(r0 + i) * ng + gi] : 0.f;
+                    a0[i] = fmaf(scl, t0, a0[i]);
+                    a1[i] = fmaf(scl, t1, a1[i]);
+                }
             } else {
 #pragma unroll
                 for (int i = 0; i < RPG; ++i) acc_chunk(a0[i], a1[i], wv[i], hv[j]);
@@ -1184,7 +1313,7 @@ __device__ bool arg_task(const Params &p, Smem &s, const Task &t, int ti, int ct
 /* Epilogue: publish the task's rows as epoch-tagged words (a task marked
  * TF_SKIP_SIGNAL publishes them with a stale flag: timeout tests).  Partial
  * sums of the S segments are added in a fixed order. */
-template <bool I8, int NB>
+template <int WF, int NB>
 __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, int S, const ResidPre &rp, int ctid) {
     if (TRACE(p) && ctid == 0) s.misc->t_stages = now_ns();
     const long long c0 = TRACE(p) ? clock64() : 0;
@@ -1204,7 +1333,7 @@ __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, i
         float y = 0.f;
 #pragma unroll 1
         for (int sg = 0; sg < S; ++sg) y += r[(size_t)sg * sstride];
-        return I8 ? y * s.sc[m * n + rr] : y;
+        return WF == WF_I8 ? y * s.sc[m * n + rr] : y; /* int8: the row scale; int4's are in the sums */
     };
     if (t.op == OP_GUP) {
         /* one SwiGLU output per thread; the thread of the even row packs its
@@ -1294,9 +1423,10 @@ __device__ bool gemv_epilogue(const Params &p, Smem &s, const Task &t, int ti, i
  * QKV, gate/up and the LM head; the attention or SwiGLU output for the O and
  * down projections), then the tiles stream through the ring; the epilogue
  * adds the segments' partial sums and publishes the rows. */
-template <bool I8, int NB>
+template <int WF, int NB>
 __device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring &rg, const ResidPre &rp, int ctid,
                           int warp, int lane) {
+    constexpr bool I8 = WF == WF_I8;
     const GemvGeo g = gemv_geo(p, t);
     const int NS = p.n_slots;
     const int l = t.layer, slot = l % p.depth;
@@ -1332,8 +1462,9 @@ __device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring 
     }
     const uint32_t f = ver(p, ver_l);
     /* batch 1: this warp's K segment and row group */
-    constexpr int EPC = I8 ? 16 : 8;
+    constexpr int EPC = wf_epc(WF);
     const int rowc = g.Kc / EPC, seg = warp % S, RG = NCW / S, rgp = warp / S;
+    const int ng = WF == WF_I4 ? g.K / p.group : 0; /* int4 scale groups per row */
     const int c0 = seg * rowc / S, c1 = (seg + 1) * rowc / S;
     for (int kp = 0; kp < g.ks; ++kp) {
         const int k0 = kp * g.Kc, k1 = k0 + g.Kc;
@@ -1343,8 +1474,8 @@ __device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring 
             copy_prologue(p, s, src, len, k0, k1, f, ti, which, ctid);
         if (cbar_or(s.misc->abort != 0)) return false;
         if (TRACE(p) && kp == 0 && ctid == 0) s.misc->t_pro = now_ns();
-        ActChunk<I8> hv[I8 ? JMAX_INT8 : JMAX_BF16];
-        if constexpr (NB == 1) act_regs<I8>(s.act, c0, c1, hv, lane);
+        ActChunk<WF> hv[wf_jmax(WF)];
+        if constexpr (NB == 1) act_regs<WF>(s.act, c0, c1, hv, lane);
         for (int rb = 0; rb < g.nrb; ++rb) {
             int ra, re;
             stage_rows(g.nrows, g.nrb, rb, ra, re);
@@ -1356,12 +1487,18 @@ __device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring 
                 if (TRACE(p) && kp == 0 && rb == 0 && m == 0 && warp == 0 && lane == 0) s.misc->t_first = tw1;
                 const uint8_t *tile = s.ring + (size_t)sl * p.slot_bytes;
                 if constexpr (NB == 1) {
-                    gemv_stage1<I8>(tile, re - ra, RG, rgp, rowc, c0, c1, hv, s.res + (size_t)m * g.nrows + ra,
-                                    g.nmat * g.nrows, seg, kp == 0, lane);
+                    gemv_stage1<WF>(tile, re - ra, RG, rgp, rowc, c0, c1, hv, s.res + (size_t)m * g.nrows + ra,
+                                    g.nmat * g.nrows, seg, kp == 0, lane, s.sc + ((size_t)m * g.nrows + ra) * ng, ng,
+                                    k0, p.group);
                 } else {
                     float *res = s.res + ((size_t)m * g.nrows + ra) * p.Bmax;
-                    gemv_tile<I8, NB>(tile, re - ra, S, g.Kc, reinterpret_cast<const uint32_t *>(s.act), p.batch, res,
-                                      g.nmat * g.nrows, p.Bmax, kp == 0, warp, lane);
+                    const int wpitch = smem_pitch((int)wf_bytes(WF, g.Kc), NB), apitch = smem_pitch(g.Kc * 2, NB);
+                    if constexpr (I8)
+                        gemv_tile<I8, NB>(tile, re - ra, S, g.Kc, wpitch, s.act, apitch, p.batch, res, g.nmat * g.nrows,
+                                          p.Bmax, kp == 0, warp, lane);
+                    else
+                        gemv_tile_mma<NB>(tile, re - ra, g.Kc, wpitch, s.act, apitch, p.batch, res, g.nmat * g.nrows,
+                                          p.Bmax, kp == 0, warp, lane);
                 }
                 if (TRACE(p) && warp == 0 && lane == 0) {
                     s.misc->t_wait_full += tw1 - tw0;
@@ -1373,7 +1510,7 @@ __device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring 
         }
         if (cbar_or(s.misc->abort != 0)) return false;
     }
-    return gemv_epilogue<I8, NB>(p, s, t, ti, S, rp, ctid);
+    return gemv_epilogue<WF, NB>(p, s, t, ti, S, rp, ctid);
 }
 
 /* ----------------------------------------------------------- attention */
@@ -1401,22 +1538,37 @@ __device__ __forceinline__ AttSmem att_smem(const Params &p, Smem &s, int GP) {
 }
 
 /* Online-softmax state of one warp over all GP (= G rounded up to a power of
- * two) heads of a kv group.  Scoring: LP = d / 4 lanes share a position,
- * each holding four elements of K and the matching four q values of every
- * head.  P.V: every lane owns EL = d / 32 output elements of every head.  m
- * and l belong to head lane % GP (replicated over its lanes). */
-template <int LP, int GP>
+ * two) heads of a kv group.  Scoring: LP lanes share a position, each holding
+ * EK consecutive elements of K and the matching EK q values of every head.
+ * With one query head per kv head (multi-head attention) and D = 128, EK = 16,
+ * so a warp scores four positions at once with three shuffle steps each
+ * instead of one position with five; otherwise EK = 4.  Every wider form
+ * measured (EK = 16 at D = 64 too, EK = 8 for two heads per kv head) made the
+ * whole kernel spill more and slowed the grouped-query models by about 3%,
+ * although their own instantiation was unchanged.  P.V: every lane owns EL = D / 32
+ * output elements of every head.  m and l belong to head lane % GP
+ * (replicated over its lanes). */
+template <int D, int GP>
+struct AttShape {
+    static constexpr int EK = (GP == 1 && D == 128) ? 16 : 4;
+    static constexpr int LP = D / EK;
+    static constexpr int PW = 32 / LP;
+    static constexpr int EL = D / 32;
+};
+
+template <int D, int GP>
 struct AttState {
-    float q[GP][4];
-    float o[GP][LP / 8];
+    float q[GP][AttShape<D, GP>::EK];
+    float o[GP][AttShape<D, GP>::EL];
     float m, l;
 };
 
 /* positions j0 .. j0 + nb - 1 (nb <= ATT_BP) of a K/V tile in shared memory */
-template <int LP, int GP>
-__device__ __forceinline__ void att_block(AttState<LP, GP> &st, const uint16_t *Kt, const uint16_t *Vt, int j0,
-                                          int nb, int d, float *sb, int lane) {
-    constexpr int PW = 32 / LP, EL = LP / 8, LPH = 32 / GP;
+template <int D, int GP>
+__device__ __forceinline__ void att_block(AttState<D, GP> &st, const uint16_t *Kt, const uint16_t *Vt, int j0,
+                                          int nb, float *sb, int lane) {
+    constexpr int d = D, EK = AttShape<D, GP>::EK, LP = AttShape<D, GP>::LP, PW = AttShape<D, GP>::PW;
+    constexpr int EL = AttShape<D, GP>::EL, LPH = 32 / GP;
     /* a task runs this block once or a few times per layer, so its code is
      * usually not in the instruction cache: with many heads per kv head the
      * loops stay rolled (less code to fetch); with few, they unroll */
@@ -1428,11 +1580,18 @@ __device__ __forceinline__ void att_block(AttState<LP, GP> &st, const uint16_t *
         const int jj = it * PW + pg;
         float sc[GP];
         if (jj < nb) {
-            const uint2 kv = reinterpret_cast<const uint2 *>(Kt + (size_t)(j0 + jj) * d)[ch];
-            const float k0 = bf_lo(kv.x), k1 = bf_hi(kv.x), k2 = bf_lo(kv.y), k3 = bf_hi(kv.y);
+            const uint2 *kr = reinterpret_cast<const uint2 *>(Kt + (size_t)(j0 + jj) * d + ch * EK);
 #pragma unroll
-            for (int h = 0; h < GP; ++h)
-                sc[h] = fmaf(st.q[h][0], k0, st.q[h][1] * k1) + fmaf(st.q[h][2], k2, st.q[h][3] * k3);
+            for (int q4 = 0; q4 < EK / 4; ++q4) {
+                const uint2 kv = kr[q4];
+                const float k0 = bf_lo(kv.x), k1 = bf_hi(kv.x), k2 = bf_lo(kv.y), k3 = bf_hi(kv.y);
+#pragma unroll
+                for (int h = 0; h < GP; ++h) {
+                    const float part = fmaf(st.q[h][4 * q4], k0, st.q[h][4 * q4 + 1] * k1) +
+                                       fmaf(st.q[h][4 * q4 + 2], k2, st.q[h][4 * q4 + 3] * k3);
+                    sc[h] = q4 == 0 ? part : sc[h] + part;
+                }
+            }
         } else {
 #pragma unroll
             for (int h = 0; h < GP; ++h) sc[h] = 0.f;
@@ -1495,10 +1654,10 @@ __device__ __forceinline__ void att_block(AttState<LP, GP> &st, const uint16_t *
     __syncwarp();
 }
 
-template <int LP, int GP>
+template <int D, int GP>
 __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, Ring &rg, int ctid, int warp, int lane) {
-    constexpr int EL = LP / 8;
-    constexpr int d = 4 * LP; /* head_dim: LP = d / 4 lanes share a position */
+    constexpr int EL = AttShape<D, GP>::EL, EK = AttShape<D, GP>::EK, LP = AttShape<D, GP>::LP;
+    constexpr int d = D;
     const int G = p.G, NS = p.n_slots;
     const int l = t.layer, slot = l % p.depth, b = t.b, grp = t.g;
     const AttGeo ag = att_geo(p, t);
@@ -1570,7 +1729,7 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
         }
     }
 
-    AttState<LP, GP> st;
+    AttState<D, GP> st;
     st.m = -INFINITY;
     st.l = 0.f;
     {
@@ -1578,7 +1737,7 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
 #pragma unroll
         for (int h = 0; h < GP; ++h)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) st.q[h][e] = h < G ? as.q[h * d + ch * 4 + e] : 0.f;
+            for (int e = 0; e < EK; ++e) st.q[h][e] = h < G ? as.q[h * d + ch * EK + e] : 0.f;
 #pragma unroll
         for (int h = 0; h < GP; ++h)
 #pragma unroll
@@ -1603,7 +1762,7 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
          * covers it copies its K and V into that row first */
         const bool add_new = with_new && k == ag.ntile - 1 && nt < (int)t.rows_per_stage;
         const int ntot = nt + (add_new ? 1 : 0);
-        constexpr int PW = 32 / LP;
+        constexpr int PW = AttShape<D, GP>::PW;
         const int per = min(ATT_BP, ((ntot + NCW - 1) / NCW + PW - 1) / PW * PW);
         for (int j0 = warp * per; j0 < ntot; j0 += NCW * per) {
             const int nb = min(per, ntot - j0);
@@ -1614,7 +1773,7 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
                 }
                 __syncwarp();
             }
-            att_block<LP, GP>(st, Kt, Vt, j0, nb, d, sb, lane);
+            att_block<D, GP>(st, Kt, Vt, j0, nb, sb, lane);
         }
         if (add_new) new_done = true;
         if (TRACE(p) && warp == 0 && lane == 0) {
@@ -1625,7 +1784,7 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
         if (lane == 0) mbar_arrive(&s.empty[sl]);
     }
     /* otherwise the new position on its own, from shared memory, on the last warp */
-    if (with_new && !new_done && warp == NCW - 1) att_block<LP, GP>(st, as.knew, as.vnew, 0, 1, d, sb, lane);
+    if (with_new && !new_done && warp == NCW - 1) att_block<D, GP>(st, as.knew, as.vnew, 0, 1, sb, lane);
     if (TRACE(p) && ctid == 0) s.misc->t_stages = now_ns();
 
     /* the warp's state: o of every head, m and l of head lane (lane < GP) */
@@ -1679,13 +1838,13 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
     return !cbar_or(s.misc->abort != 0);
 }
 
-template <int LP>
+template <int D>
 __device__ bool att_task(const Params &p, Smem &s, const Task &t, int ti, Ring &rg, int ctid, int warp, int lane) {
     const int GP = att_gp(p.G);
-    if (GP == 1) return att_task_impl<LP, 1>(p, s, t, ti, rg, ctid, warp, lane);
-    if (GP == 2) return att_task_impl<LP, 2>(p, s, t, ti, rg, ctid, warp, lane);
-    if (GP == 4) return att_task_impl<LP, 4>(p, s, t, ti, rg, ctid, warp, lane);
-    return att_task_impl<LP, 8>(p, s, t, ti, rg, ctid, warp, lane);
+    if (GP == 1) return att_task_impl<D, 1>(p, s, t, ti, rg, ctid, warp, lane);
+    if (GP == 2) return att_task_impl<D, 2>(p, s, t, ti, rg, ctid, warp, lane);
+    if (GP == 4) return att_task_impl<D, 4>(p, s, t, ti, rg, ctid, warp, lane);
+    return att_task_impl<D, 8>(p, s, t, ti, rg, ctid, warp, lane);
 }
 
 /* Merge the C chunk partials of one query head of one sequence into its bf16
@@ -1776,7 +1935,7 @@ __device__ bool mrg_task(const Params &p, Smem &s, const Task &t, int ti, int ct
 
 /* ----------------------------------------------------------- the kernel */
 
-template <bool I8, int NB>
+template <int WF, int NB>
 __device__ __forceinline__ void run_tasks(const Params &p, Smem &s, int tbeg, int tend, int tid, int warp, int lane) {
     if (warp == NCW) {
         if (lane == 0) loader(p, s, tbeg, tend);
@@ -1788,11 +1947,13 @@ __device__ __forceinline__ void run_tasks(const Params &p, Smem &s, int tbeg, in
             Task t;
             load_task(p.tasks + ti, t);
             /* weights-only inputs are fetched before the task's inputs are ready */
-            if (I8 && t.op != OP_ATT && t.op != OP_MRG && t.op != OP_ARG) {
+            if (WF != WF_BF16 && t.op != OP_ATT && t.op != OP_MRG && t.op != OP_ARG) {
+                /* int8: one scale per row, [m][row]; int4: [m][row][group] */
                 const int n = t.r1 - t.r0, nm = t.op == OP_GUP ? 2 : 1;
-                for (int i = ctid; i < n * nm; i += NCW * 32) {
-                    const int m = i / n, rr = i % n;
-                    s.sc[i] = __ldg(op_scales(p, t, m) + t.r0 + rr);
+                const int per = WF == WF_I4 ? op_K(p, t.op) / p.group : 1;
+                for (int i = ctid; i < n * nm * per; i += NCW * 32) {
+                    const int m = i / (n * per), r = i % (n * per);
+                    s.sc[i] = __ldg(op_scales(p, t, m) + (size_t)t.r0 * per + r);
                 }
             }
 #if AMK_L2_PREFETCH_CODE
@@ -1811,14 +1972,14 @@ __device__ __forceinline__ void run_tasks(const Params &p, Smem &s, int tbeg, in
             }
             bool ok;
             if (t.op == OP_ATT)
-                ok = p.d == 64 ? att_task<16>(p, s, t, ti, rg, ctid, warp, lane)
-                               : att_task<32>(p, s, t, ti, rg, ctid, warp, lane);
+                ok = p.d == 64 ? att_task<64>(p, s, t, ti, rg, ctid, warp, lane)
+                               : att_task<128>(p, s, t, ti, rg, ctid, warp, lane);
             else if (t.op == OP_MRG)
                 ok = p.d == 64 ? mrg_task<64>(p, s, t, ti, ctid) : mrg_task<128>(p, s, t, ti, ctid);
             else if (t.op == OP_ARG)
                 ok = p.next_tokens ? arg_task(p, s, t, ti, ctid) : true;
             else
-                ok = gemv_task<I8, NB>(p, s, t, ti, rg, rp, ctid, warp, lane);
+                ok = gemv_task<WF, NB>(p, s, t, ti, rg, rp, ctid, warp, lane);
             if (!ok) break;
             if (tr && ctid == 0) {
                 tr[2] = s.misc->t_first;
@@ -1846,9 +2007,8 @@ __device__ __forceinline__ void run_tasks(const Params &p, Smem &s, int tbeg, in
     }
 }
 
-template <bool I8, int NB>
+template <int WF, int NB>
 __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p) {
-    extern __shared__ __align__(1024) uint8_t smem[];
     Smem s;
     s.full = reinterpret_cast<uint64_t *>(smem);
     s.empty = s.full + MAX_SLOTS;
@@ -1888,10 +2048,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p)
     uint32_t epoch = p.epoch;
     if (tid == 0) {
         if (p.epoch_word) epoch = ld_relaxed(p.epoch_word);
-        s_epoch_base = epoch * (uint32_t)(p.L + 1);
+        s.misc->epoch_base = epoch * (uint32_t)(p.L + 1);
     }
     const bool stale = __syncthreads_or(tid == 0 && (bad_input || ld_relaxed(p.err) != 0u));
-    if (!stale) run_tasks<I8, NB>(p, s, tbeg, tend, tid, warp, lane);
+    if (!stale) run_tasks<WF, NB>(p, s, tbeg, tend, tid, warp, lane);
     /* the last CTA to finish advances the device epoch for the next step (a
      * CTA reads it only at its start, so every CTA of this step has) */
     if (tid == 0 && p.epoch_word) {
@@ -1908,9 +2068,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) amk_decode_kernel(const Params p)
 bool kernel_has_trace() { return AMK_TRACE_CODE != 0; }
 bool kernel_has_l2_prefetch() { return AMK_L2_PREFETCH_CODE != 0; }
 
-KernelFn select_kernel(bool int8, int max_batch) {
-    if (int8) return max_batch == 1 ? amk_decode_kernel<true, 1> : amk_decode_kernel<true, MAXB>;
-    return max_batch == 1 ? amk_decode_kernel<false, 1> : amk_decode_kernel<false, MAXB>;
+KernelFn select_kernel(int weight_dtype, int max_batch) {
+    if (weight_dtype == 2) return amk_decode_kernel<WF_I4, 1>; /* 4-bit weights: batch 1 only */
+    if (weight_dtype == 1) return max_batch == 1 ? amk_decode_kernel<WF_I8, 1> : amk_decode_kernel<WF_I8, MAXB>;
+    return max_batch == 1 ? amk_decode_kernel<WF_BF16, 1> : amk_decode_kernel<WF_BF16, MAXB>;
 }
 
 cudaError_t prepare_kernel(KernelFn fn, int smem_bytes) {

@@ -9,8 +9,8 @@
 
 namespace amk {
 typedef void (*KernelFn)(const Params);
-/* kernel instance for the weight type and the largest batch */
-KernelFn select_kernel(bool int8, int max_batch);
+/* kernel instance for the weight type (amk_weight_dtype) and the largest batch */
+KernelFn select_kernel(int weight_dtype, int max_batch);
 cudaError_t prepare_kernel(KernelFn fn, int smem_bytes);
 cudaError_t occupancy(KernelFn fn, int smem_bytes, int *blocks_per_sm);
 /* whether this build's kernel carries the per-task timing code (trace

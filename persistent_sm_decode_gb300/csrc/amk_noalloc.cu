@@ -74,7 +74,7 @@ amk_status fail(cudaError_t e) {
 amk_status check_args(const amk_config *c, const amk_weights *w) {
     if (!c || !w || !w->embed || !w->final_norm || !w->layers) return AMK_ERR_INVALID_ARG;
     if (!aligned16(w->embed) || !aligned16(w->final_norm)) return AMK_ERR_INVALID_ARG;
-    const bool i8 = c->weight_dtype == AMK_WEIGHT_INT8;
+    const bool i8 = c->weight_dtype == AMK_WEIGHT_INT8 || c->weight_dtype == AMK_WEIGHT_INT4; /* scaled formats */
     if (!c->tied_embeddings && (!w->lm_head || !aligned16(w->lm_head) || (i8 && !w->s_lm))) return AMK_ERR_INVALID_ARG;
     if (c->n_layers < 1 || c->n_layers > 4096) return AMK_ERR_INVALID_ARG;
     for (int l = 0; l < c->n_layers; ++l) {
@@ -181,7 +181,7 @@ amk_status upload(DeviceState &ds, const amk_config *c, const amk_weights *w, in
         ds.plan = nullptr;
         return why;
     };
-    ds.fn = select_kernel(c->weight_dtype == AMK_WEIGHT_INT8, c->max_batch);
+    ds.fn = select_kernel(c->weight_dtype, c->max_batch);
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, (const void *)ds.fn) != cudaSuccess ||
         prepare_kernel(ds.fn, P.smem_bytes) != cudaSuccess) {
@@ -216,8 +216,9 @@ amk_status upload(DeviceState &ds, const amk_config *c, const amk_weights *w, in
     p.qkv_rows = g.qkv_rows;
     p.eps = c->rms_eps;
     p.qk_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
-    p.wint8 = g.i8;
-    p.lm_int8 = g.lm_i8;
+    p.wf = g.wf;
+    p.lm_wf = g.lm_wf;
+    p.group = g.group;
     p.tasks = (const Task *)(ds.base + o_tasks);
     p.task_start = (const int32_t *)(ds.base + o_start);
     p.C = P.k.C;

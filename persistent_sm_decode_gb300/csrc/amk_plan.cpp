@@ -170,7 +170,7 @@ int max_task_rows(const Geo &g, int op, int n_sm) {
 
 int rows_per_slot(const Geo &g, int op, int ks, int slot) {
     int kc = g.K(op) / ksplit_for(g, op, ks);
-    return std::max(1, std::min(256, slot / (kc * g.web(op))));
+    return std::max(1, std::min(256, slot / smem_pitch((int)g.wbytes(op, kc), g.B)));
 }
 
 /* Shared memory besides the ring.  One region serves whichever task runs:
@@ -186,12 +186,12 @@ SmemModel smem_model(const Geo &g, int ks, int slot, int C, int n_sm) {
         int kc = g.K(op) / ksplit_for(g, op, ks);
         /* the prologue writes the bf16 activations of the K slice (batch 1:
          * the warps then copy their segments into registers) */
-        gemv_act = std::max(gemv_act, g.B * kc * 2);
+        gemv_act = std::max(gemv_act, g.B * smem_pitch(kc * 2, g.B));
         int R = rows_per_slot(g, op, ks, slot);
-        int S = gemv_segments(g.B, kc, g.web(op) == 1, R);
+        int S = gemv_segments(g.B, kc, g.wf_of(op), R);
         int rows = max_task_rows(g, op, n_sm) + 1;  /* +1: a QKV matrix boundary can split a block */
         m.result = std::max(m.result, rows * g.nmat(op) * S * g.B * 4);
-        if (g.scaled(op)) m.scales = std::max(m.scales, rows * g.nmat(op) * 4);
+        if (g.row_scales(op, kc)) m.scales = std::max(m.scales, rows * g.nmat(op) * 4 * (int)g.row_scales(op, g.K(op)));
     }
     (void)C;
     m.act = align_up(gemv_act, 128);
@@ -329,7 +329,7 @@ struct Builder {
                 Task t = base(op, l);
                 t.ksplit = (uint8_t)ks;
                 t.rows_per_stage = (uint16_t)rows_per_stage(op, ks);
-                t.seg = (uint8_t)gemv_segments(g.B, g.K(op) / ks, g.web(op) == 1, t.rows_per_stage);
+                t.seg = (uint8_t)gemv_segments(g.B, g.K(op) / ks, g.wf_of(op), t.rows_per_stage);
                 std::vector<Access> ac;
                 if (op == OP_QKV) {
                     /* stay inside one matrix and touch at most MAX_SIG groups */
@@ -392,9 +392,13 @@ struct Builder {
     void att_level(int l) {
         int T = g.B * g.nkv * k.C;
         int qd = g.nq * g.d, kd = g.nkv * g.d;
+        /* order 1: attention chunks fill the CTAs from the top, merges from
+         * the bottom, so that a merge does not queue behind a chunk on its CTA
+         * when both fit */
         for (int t = 0; t < T; ++t) {
             int c = t % k.C, grp = (t / k.C) % g.nkv, b = t / (k.C * g.nkv);
             int sm = (int)((int64_t)t * n_sm / T);
+            if (k.order == 1) sm = T <= n_sm ? n_sm - 1 - t : n_sm - 1 - sm;
             Task x = base(OP_ATT, l);
             x.r0 = c;
             x.r1 = k.C;
@@ -422,6 +426,7 @@ struct Builder {
         for (int i = 0; i < M; ++i) {
             int b = i / g.nq, h = i % g.nq, grp = h / g.G;
             int sm = (int)((int64_t)i * n_sm / M);
+            if (k.order == 1 && M <= n_sm) sm = i;
             Task m = base(OP_MRG, l);
             m.r1 = k.C;
             m.b = (uint16_t)b;
@@ -476,6 +481,132 @@ struct Builder {
 
 namespace amk {
 
+/* Fitted to GB300 step times (TinyLlama bf16 and W8A16, SmolLM2, Llama-2-7B
+ * at batch 1 and 8, the TinyLlama short shape at batch 1..16). */
+const double COST_DEFAULT[COST_NCONST] = {
+    1.5e-6,  /* [0]  hand-off: producer's last store -> consumer sees every word */
+    0.5e-6,  /* [1]  RMSNorm prologue of one sequence (batch 1: one pass) */
+    0.4e-6,  /* [2]  copy prologue of one sequence (attention or SwiGLU output) */
+    0.6e-6,  /* [3]  GEMV epilogue (segment sums, residual, stores, barrier) */
+    7.5e10,  /* [4]  batch-1 consumer rate, bf16 weight bytes per second per CTA */
+    5.0e10,  /* [5]  batch-1 consumer rate, int8 weight bytes per second per CTA */
+    6.5e12,  /* [6]  HBM bytes per second, shared by the CTAs that stream */
+    0.5e-6,  /* [7]  attention prologue (q, k, v of the group; RoPE) */
+    2.0e-12, /* [8]  attention, per (position, head of the group, head element) */
+    0.8e-6,  /* [9]  attention epilogue (warp merge, partials) */
+    0.5e-6,  /* [10] merge task */
+    0.1e-6,  /* [11] per ring stage (slot wait, release) */
+    0.6e-6,  /* [12] extra prologue per further sequence at batch > 1 */
+    1.5e11,  /* [13] most bytes per second one CTA's loader can pull */
+};
+
+/* Task-level simulation of one step.  Every CTA's consumers run its tasks in
+ * order: a task starts when the CTA is free and every producer of what it
+ * waits on has finished, plus the hand-off.  Its tiles need their bytes from
+ * the CTA's loader, which streams the CTA's tasks in the same order at its
+ * share of HBM, never more than the ring ahead of what the consumers have
+ * released.  The step ends with the last task. */
+double plan_simulate(const amk_plan &P, const double *c) {
+    const Geo g = make_geo(P.cfg, P.batch);
+    const int n_sm = P.n_sm;
+    const double ring = (double)P.k.n_slots * P.k.slot_bytes;
+    const double rate = std::min(c[13], c[6] / n_sm);
+    /* producers' end time per dependency id, and how many have finished */
+    std::vector<double> dep_end(P.n_counters + 1, 0.0);
+    std::vector<int> dep_left(P.n_counters + 1, 0);
+    for (auto &v : P.sm_tasks)
+        for (auto &t : v)
+            for (int i = 0; i < t.nsig; ++i) dep_left[t.sig[i]]++;
+    struct Cta {
+        size_t next = 0;
+        double free = 0, loader = 0, fetched = 0; /* bytes fetched so far */
+        std::vector<std::pair<double, double>> done; /* (cumulative bytes consumed, time) */
+    };
+    std::vector<Cta> cs(n_sm);
+    auto task_bytes = [&](const Task &t) -> double {
+        if (t.op == OP_MRG || t.op == OP_ARG) return 0.0;
+        if (t.op == OP_ATT) {
+            const int n = g.Smax; /* a bound: positions of the chunk at full context */
+            return 4.0 * g.d * std::ceil((double)n / std::max(1, (int)t.r1));
+        }
+        return (double)(t.r1 - t.r0) * g.nmat(t.op) * g.row_bytes(t.op);
+    };
+    double end_all = 0;
+    size_t left = 0;
+    for (auto &v : P.sm_tasks) left += v.size();
+    bool progress = true;
+    while (left > 0 && progress) {
+        progress = false;
+        for (int sm = 0; sm < n_sm; ++sm) {
+            Cta &C = cs[sm];
+            while (C.next < P.sm_tasks[sm].size()) {
+                const Task &t = P.sm_tasks[sm][C.next];
+                if (t.op == OP_ARG) { /* runs only in greedy steps */
+                    ++C.next;
+                    --left;
+                    progress = true;
+                    continue;
+                }
+                if (t.wait_id != NO_WAIT && dep_left[t.wait_id] > 0) break;
+                const double ready = t.wait_id != NO_WAIT ? dep_end[t.wait_id] + c[0] : 0.0;
+                double start = std::max(C.free, ready);
+                /* prologue */
+                double pro;
+                const int B = g.B;
+                if (t.op == OP_ATT) pro = c[7];
+                else if (t.op == OP_MRG) pro = 0.0;
+                else if (t.op == OP_OPR || t.op == OP_DWN) pro = c[2] + (B - 1) * c[12];
+                else pro = c[1] + (B - 1) * c[12] * (B > 1 ? 2.0 : 1.0);
+                const int ks = t.op == OP_ATT || t.op == OP_MRG ? 1 : std::max(1, (int)t.ksplit);
+                pro *= ks;
+                /* bytes: the loader starts on them once the ring has room */
+                const double bytes = task_bytes(t);
+                const double need = C.fetched + bytes - ring; /* bytes the consumers must have released */
+                double room_t = 0.0;
+                if (need > 0) {
+                    room_t = -1.0;
+                    for (const auto &d : C.done)
+                        if (d.first >= need) {
+                            room_t = d.second;
+                            break;
+                        }
+                    if (room_t < 0) room_t = C.free; /* only this task's own tiles make room */
+                }
+                const double fstart = std::max(C.loader, room_t);
+                const double fend = fstart + bytes / rate;
+                C.loader = fend;
+                C.fetched += bytes;
+                /* tiles: consumer rate, and no earlier than the last byte */
+                double tiles;
+                if (t.op == OP_ATT) {
+                    const double pos = std::ceil((double)g.Smax / std::max(1, (int)t.r1));
+                    tiles = pos * att_gp(g.G) * g.d * c[8];
+                } else if (t.op == OP_MRG) {
+                    tiles = c[10];
+                } else {
+                    const double cr = g.wf_of(t.op) != WF_BF16 ? c[5] : c[4];
+                    const double stages = std::ceil(bytes / std::max(1, P.k.slot_bytes));
+                    tiles = bytes / cr + stages * c[11];
+                }
+                const double tend = std::max(start + pro + tiles, fend);
+                const double epi = t.op == OP_ATT ? c[9] : t.op == OP_MRG ? 0.0 : c[3];
+                const double end = tend + epi;
+                C.free = end;
+                C.done.push_back({C.fetched, end});
+                end_all = std::max(end_all, end);
+                for (int i = 0; i < t.nsig; ++i) {
+                    dep_end[t.sig[i]] = std::max(dep_end[t.sig[i]], end);
+                    dep_left[t.sig[i]]--;
+                }
+                ++C.next;
+                --left;
+                progress = true;
+            }
+        }
+    }
+    return end_all * 1e6;
+}
+
 Geo make_geo(const amk_config &c, int batch) {
     Geo g;
     g.L = c.n_layers;
@@ -489,14 +620,29 @@ Geo make_geo(const amk_config &c, int batch) {
     g.qkv_rows = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
     g.B = batch;
     g.Smax = c.max_seq;
-    g.i8 = c.weight_dtype == AMK_WEIGHT_INT8;
-    g.lm_i8 = g.i8 && !c.tied_embeddings;
+    g.wf = c.weight_dtype == AMK_WEIGHT_INT8 ? WF_I8 : c.weight_dtype == AMK_WEIGHT_INT4 ? WF_I4 : WF_BF16;
+    g.lm_wf = c.tied_embeddings ? WF_BF16 : g.wf;
+    g.group = c.group_size > 0 ? c.group_size : 128;
     return g;
 }
 
+/* The K split of one operator.  `ks` is the search's (or the caller's)
+ * split; at batch above 1 an operator whose activation slice would not fit
+ * ACT_BUDGET bytes of shared memory is split further.  A slice must be whole
+ * 16-byte units of weights, and for the tensor-core tile (bf16, batch above
+ * 1) whole k16 steps. */
+constexpr int ACT_BUDGET = 64 * 1024;
 int ksplit_for(const Geo &g, int op, int ks) {
+    auto ok = [&](int k) {
+        if (g.K(op) % k != 0 || g.wbytes(op, g.K(op) / k) % 16 != 0) return false;
+        if (g.wf_of(op) == WF_I4 && (g.K(op) / k) % g.group != 0) return false;
+        if (g.B > 1 && g.wf_of(op) == WF_BF16 && (g.K(op) / k) % 16 != 0) return false;
+        return true;
+    };
     int k = std::max(1, ks);
-    while (k > 1 && (g.K(op) % k != 0 || ((g.K(op) / k) * g.web(op)) % 16 != 0)) k /= 2;
+    if (g.B > 1)
+        while (k < 64 && ok(2 * k) && g.B * smem_pitch(g.K(op) / k * 2, g.B) > ACT_BUDGET) k *= 2;
+    while (k > 1 && !ok(k)) k /= 2;
     return k;
 }
 
@@ -524,14 +670,49 @@ static std::string check_config(const amk_config &c, int batch) {
     if (c.hidden % 16 || (c.n_heads * c.head_dim) % 16 || c.intermediate % 16)
         return "hidden, n_heads*head_dim and intermediate must be multiples of 16";
     if (c.hidden > 8192) return "hidden above 8192";
-    if (c.max_batch < 1 || c.max_batch > MAXB) return "max_batch must be 1..8";
+    if (c.max_batch < 1 || c.max_batch > MAXB) return "max_batch must be 1..16";
     if (batch < 1 || batch > c.max_batch) return "batch must be 1..max_batch";
-    if (c.weight_dtype != AMK_WEIGHT_BF16 && c.weight_dtype != AMK_WEIGHT_INT8) return "unknown weight dtype";
-    if (c.tied_embeddings && c.weight_dtype == AMK_WEIGHT_INT8) return "tied embeddings need bf16 weights";
+    if (c.weight_dtype != AMK_WEIGHT_BF16 && c.weight_dtype != AMK_WEIGHT_INT8 && c.weight_dtype != AMK_WEIGHT_INT4)
+        return "unknown weight dtype";
+    if (c.tied_embeddings && c.weight_dtype != AMK_WEIGHT_BF16) return "tied embeddings need bf16 weights";
+    if (c.weight_dtype == AMK_WEIGHT_INT4) {
+        const int gs = c.group_size > 0 ? c.group_size : 128;
+        if (c.max_batch != 1) return "4-bit weights run at batch 1 (max_batch must be 1)";
+        if (gs % 32 != 0 || c.hidden % gs || (c.n_heads * c.head_dim) % gs || c.intermediate % gs)
+            return "group_size must be a multiple of 32 that divides hidden, n_heads*head_dim and intermediate";
+    }
     if (!(c.rms_eps >= 0.0f) || !(c.rope_theta > 0.0f)) return "bad rms_eps or rope_theta";
     if (c.n_layers > 4096 || (int64_t)c.n_layers * (c.n_kv_heads * (c.max_batch + 1) + 4) >= NO_WAIT)
         return "too many layers";
     return "";
+}
+
+/* The static per-CTA task lists and shared-memory layout of one knob point. */
+static amk_plan *solidify(const amk_config *cfg, const Geo &g, const Knobs &k, int batch, int n_sm,
+                          int smem_per_cta) {
+    amk_plan *P = new amk_plan;
+    P->cfg = *cfg;
+    P->batch = batch;
+    P->n_sm = n_sm;
+    P->smem_per_cta = smem_per_cta;
+    P->k = k;
+    Builder bld{g, P->k, n_sm, P, 0};
+    bld.run();
+    SmemModel sm = smem_model(g, k.ksplit, k.slot_bytes, k.C, n_sm);
+    P->act_bytes = sm.act;
+    P->result_bytes = sm.result;
+    P->scale_bytes = sm.scales;
+    P->fac_bytes = sm.fac;
+    P->work_bytes = sm.work;
+    P->smem_bytes = sm.fixed + k.n_slots * k.slot_bytes;
+    int64_t wb = 0;
+    for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN})
+        wb += (int64_t)g.L * g.rows(op) * g.nmat(op) * g.row_bytes(op);
+    wb += (int64_t)g.rows(OP_LMH) * g.row_bytes(OP_LMH);
+    P->weight_bytes = wb;
+    ScratchSizes ss = scratch_sizes(*P);
+    P->scratch_bytes = 8 * (ss.x_in + ss.x_mid + ss.qkv + ss.part + ss.aout + ss.act + ss.argp);
+    return P;
 }
 
 amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_cta,
@@ -558,13 +739,21 @@ amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_c
     if (opt) o = *opt;
     Geo g = make_geo(*cfg, batch);
 
-    /* ---- search ---- */
+    /* ---- search ----
+     * 1. every feasible (K split, slot size, context chunks) point is scored
+     *    by the analytic per-level model (fast);
+     * 2. the best few are solidified under each task placement and scored by
+     *    the task-level simulation of the whole step (plan_simulate), which
+     *    sees placement, ring depth and the dependency structure;
+     * 3. the winner is validated. */
     const int slot_choices[] = {8192, 12288, 16384, 24576, 32768, 49152, 65536};
     const int ks_choices[] = {1, 2, 4};
-    Knobs best;
-    double best_cost = 1e300;
+    std::vector<std::pair<double, Knobs>> pts;
     int cands = 0;
-    int maxC = std::max(1, std::min(att_max_chunks(g.d), (2 * n_sm) / std::max(1, g.B * g.nkv)));
+    /* at batch 1 a few hundred attention tasks are plenty; larger batches
+     * have many (sequence, kv head) pairs and may need chunks to balance them */
+    int maxC = g.B == 1 ? std::max(1, std::min(att_max_chunks(g.d), (2 * n_sm) / std::max(1, g.nkv)))
+                        : att_max_chunks(g.d);
     for (int ks : ks_choices) {
         if (o.ksplit && ks != o.ksplit) continue;
         for (int slot : slot_choices) {
@@ -572,9 +761,8 @@ amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_c
             bool fits = true;
             for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN, OP_LMH}) {
                 const int kc = g.K(op) / ksplit_for(g, op, ks);
-                if ((int64_t)kc * g.web(op) > slot) fits = false;
-                if (g.B == 1 && gemv_lane_chunks(kc, gemv_segments(1, kc, g.web(op) == 1, NCW * RPG1),
-                                                 g.web(op) == 1) == 0)
+                if ((int64_t)smem_pitch((int)g.wbytes(op, kc), g.B) > slot) fits = false;
+                if (g.B == 1 && gemv_lane_chunks(kc, gemv_segments(1, kc, g.wf_of(op), NCW * RPG1), g.wf_of(op)) == 0)
                     fits = false;
             }
             if (g.d * 4 > slot) fits = false;
@@ -595,12 +783,8 @@ amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_c
                 k.att_tile = std::min(256, slot / (4 * g.d));
                 k.l2_prefetch_kb = o.l2_prefetch_kb < 0 ? 0 : o.l2_prefetch_kb > 0 ? o.l2_prefetch_kb : L2_PREFETCH_KB;
                 k.evict_first = o.l2_evict_first < 0 ? 0 : o.l2_evict_first > 0 ? 1 : EVICT_FIRST;
-                double c = model_cost_us(g, k, n_sm);
+                pts.push_back({model_cost_us(g, k, n_sm), k});
                 ++cands;
-                if (c < best_cost) {
-                    best_cost = c;
-                    best = k;
-                }
             }
         }
     }
@@ -608,32 +792,30 @@ amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_c
         *msg = "no schedule point fits the shared-memory model";
         return AMK_ERR_UNSUPPORTED;
     }
-
-    /* ---- solidify ---- */
-    amk_plan *P = new amk_plan;
-    P->cfg = *cfg;
-    P->batch = batch;
-    P->n_sm = n_sm;
-    P->smem_per_cta = smem_per_cta;
-    P->k = best;
-    Builder bld{g, best, n_sm, P, 0};
-    bld.run();
-    SmemModel sm = smem_model(g, best.ksplit, best.slot_bytes, best.C, n_sm);
-    P->act_bytes = sm.act;
-    P->result_bytes = sm.result;
-    P->scale_bytes = sm.scales;
-    P->fac_bytes = sm.fac;
-    P->work_bytes = sm.work;
-    P->smem_bytes = sm.fixed + best.n_slots * best.slot_bytes;
-    P->modeled_us = best_cost;
-    P->candidates = cands;
-    int64_t wb = 0;
-    for (int op : {OP_QKV, OP_OPR, OP_GUP, OP_DWN})
-        wb += (int64_t)g.L * g.rows(op) * g.nmat(op) * g.row_bytes(op);
-    wb += (int64_t)g.rows(OP_LMH) * g.row_bytes(OP_LMH);
-    P->weight_bytes = wb;
-    ScratchSizes ss = scratch_sizes(*P);
-    P->scratch_bytes = 8 * (ss.x_in + ss.x_mid + ss.qkv + ss.part + ss.aout + ss.act + ss.argp);
+    std::stable_sort(pts.begin(), pts.end(),
+                     [](const std::pair<double, Knobs> &a, const std::pair<double, Knobs> &b) { return a.first < b.first; });
+    constexpr int SIM_TOP = 6;
+    amk_plan *P = nullptr;
+    double best_sim = 1e300;
+    int simulated = 0;
+    for (int i = 0; i < (int)pts.size() && i < SIM_TOP; ++i)
+        for (int order = 0; order < 2; ++order) {
+            if (o.task_order && order != o.task_order - 1) continue;
+            Knobs k = pts[i].second;
+            k.order = order;
+            amk_plan *Q = solidify(cfg, g, k, batch, n_sm, smem_per_cta);
+            Q->modeled_us = pts[i].first;
+            Q->simulated_us = plan_simulate(*Q, COST_DEFAULT);
+            ++simulated;
+            if (Q->simulated_us < best_sim) {
+                best_sim = Q->simulated_us;
+                if (P) amk_plan_destroy(P);
+                P = Q;
+            } else {
+                amk_plan_destroy(Q);
+            }
+        }
+    P->candidates = cands + simulated;
 
     /* every GEMV task's partial sums must fit the result buffer */
     for (int sm_i = 0; sm_i < n_sm; ++sm_i)
@@ -929,6 +1111,8 @@ amk_status amk_plan_get_info(const amk_plan *p, amk_plan_info *info) {
     info->search_ms = p->search_ms;
     info->candidates = p->candidates;
     info->l2_evict_first = p->k.evict_first;
+    info->simulated_us = p->simulated_us;
+    info->task_order = p->k.order + 1;
     return AMK_OK;
 }
 
@@ -1047,6 +1231,13 @@ amk_status amk_plan_mutate(amk_plan *p, int32_t kind, uint64_t seed) {
     default:
         return AMK_ERR_INVALID_ARG;
     }
+}
+
+amk_status amk_plan_simulate(const amk_plan *p, const double *consts, int32_t n_consts, double *step_us) {
+    if (!p || !step_us) return AMK_ERR_INVALID_ARG;
+    if (consts && n_consts != COST_NCONST) return AMK_ERR_INVALID_ARG;
+    *step_us = plan_simulate(*p, consts ? consts : COST_DEFAULT);
+    return AMK_OK;
 }
 
 const char *amk_plan_last_message(void) { return g_plan_msg.c_str(); }

@@ -35,12 +35,18 @@ struct Knobs {
     int att_tile = 64;      /* positions per attention tile */
     int l2_prefetch_kb = 0;
     int evict_first = 1;    /* ring fills carry an L2 evict-first hint */
+    int order = 0;          /* task placement: 0 attention chunks and merges spread over all CTAs in step;
+                               1 merges on the CTAs that run no attention chunk (attention from the top) */
 };
+
+/* Constants of the task-level simulation (amk_plan_simulate); see amk_plan.h. */
+constexpr int COST_NCONST = 14;
+extern const double COST_DEFAULT[COST_NCONST];
 
 /* Model geometry seen by the planner. */
 struct Geo {
     int L, H, nq, nkv, d, I, V, G, qkv_rows, B, Smax;
-    bool i8, lm_i8;
+    int wf, lm_wf, group; /* weight formats (WF_*) and the int4 scale group */
     int K(int op) const {
         return op == OP_OPR ? nq * d : op == OP_DWN ? I : H;
     }
@@ -48,9 +54,14 @@ struct Geo {
         return op == OP_QKV ? qkv_rows : op == OP_GUP ? I : op == OP_LMH ? V : H;
     }
     int nmat(int op) const { return op == OP_GUP ? 2 : 1; }
-    int web(int op) const { return (op == OP_LMH ? lm_i8 : i8) ? 1 : 2; }
-    bool scaled(int op) const { return op == OP_LMH ? lm_i8 : i8; }
-    int64_t row_bytes(int op) const { return (int64_t)K(op) * web(op) + (scaled(op) ? 4 : 0); }
+    int wf_of(int op) const { return op == OP_LMH ? lm_wf : wf; }
+    /* bytes of k weights of `op` in its format */
+    int64_t wbytes(int op, int64_t k) const { return wf_bytes(wf_of(op), k); }
+    /* fp32 scales of one output row over k weights: int8 one, int4 one per group */
+    int64_t row_scales(int op, int64_t k) const {
+        return wf_of(op) == WF_I8 ? 1 : wf_of(op) == WF_I4 ? k / group : 0;
+    }
+    int64_t row_bytes(int op) const { return wbytes(op, K(op)) + 4 * row_scales(op, K(op)); }
 };
 
 Geo make_geo(const amk_config &c, int batch);
@@ -68,7 +79,7 @@ struct amk_plan {
     int n_lmh = 0; /* LM-head tasks (each publishes one partial argmax per sequence) */
     int act_bytes = 0, result_bytes = 0, scale_bytes = 0, fac_bytes = 0, work_bytes = 0, smem_bytes = 0;
     int64_t weight_bytes = 0, scratch_bytes = 0;
-    double modeled_us = 0, search_ms = 0;
+    double modeled_us = 0, search_ms = 0, simulated_us = 0;
     int candidates = 0;
 };
 
@@ -78,6 +89,8 @@ amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_c
                       const amk_schedule_options *opt, amk_plan **out, std::string *msg);
 /* Deadlock- and race-freedom check; true if the plan is safe. */
 bool plan_validate(const amk_plan &p, std::string *msg);
+/* Task-level simulation of one step of a solidified plan (µs). */
+double plan_simulate(const amk_plan &p, const double *c);
 /* Element counts of the scratch buffers described in Params. */
 struct ScratchSizes {
     int64_t x_in, x_mid, qkv, part, aout, act; /* 8-byte epoch-tagged words */

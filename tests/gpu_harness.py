@@ -39,7 +39,8 @@ def engine_config(wl, max_batch=None):
     import persistent_sm_decode_gb300 as amk
     return amk.make_config(wl.n_layers, wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.intermediate,
                            wl.vocab, wl.max_seq, max_batch or wl.batch, wl.rms_eps, wl.rope_theta,
-                           int8=wl.weight_dtype == "int8", tied=wl.tied)
+                           int8=wl.weight_dtype == "int8", tied=wl.tied,
+                          int4=wl.weight_dtype == "int4", group_size=wl.group_size)
 
 
 def make_engine(wl, dev, options=None, max_batch=None):
@@ -74,12 +75,12 @@ class Result:
 
     def summary(self) -> dict:
         rows = sorted({r[1] for r in self.records})
-        return {"steps": self.steps, "rows": rows, "worst": self.worst, "floor": self.floor,
-                "max_abs": self.max_abs, "strict_logits_ok": self.worst <= 1.0,
-                "argmax_checked": self.checked_argmax, "argmax_agree": self.argmax_agree,
-                "strict_argmax_ok": self.argmax_agree == self.checked_argmax,
-                "relaxed_misses": len(self.relaxed_misses()), "free_running": self.free_running,
-                "min_margin": min((r[2] for r in self.records), default=None)}
+        return {"steps": int(self.steps), "rows": [int(r) for r in rows], "worst": float(self.worst),
+                "floor": float(self.floor), "max_abs": float(self.max_abs), "strict_logits_ok": bool(self.worst <= 1.0),
+                "argmax_checked": int(self.checked_argmax), "argmax_agree": int(self.argmax_agree),
+                "strict_argmax_ok": bool(self.argmax_agree == self.checked_argmax),
+                "relaxed_misses": len(self.relaxed_misses()), "free_running": int(self.free_running),
+                "min_margin": float(min((r[2] for r in self.records), default=float("nan")))}
 
     def __repr__(self):
         return ("Result(worst=%.3g, floor=%.3g, max_abs=%.3g, argmax %d/%d, steps=%d, free-running %d)"
@@ -267,6 +268,7 @@ def layerwise(wl, steps=2, options=None, batch=None, positions0=None, check_rows
 
 
 def assert_layers_ok(res: LayerResult):
-    log_parity("per_layer", {"steps": res.steps, "layers_checked": res.layers_checked,
-                             "worst": dict(res.worst), "where": {k: list(v) for k, v in res.where.items()}})
+    log_parity("per_layer", {"steps": int(res.steps), "layers_checked": int(res.layers_checked),
+                             "worst": {k: float(v) for k, v in res.worst.items()},
+                             "where": {k: [int(x) for x in v] for k, v in res.where.items()}})
     assert all(v <= 1.0 for v in res.worst.values()), res

@@ -30,16 +30,17 @@ def amk():
 def _cfg(amk, wl, batch=None):
     return amk.make_config(wl.n_layers, wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.intermediate,
                            wl.vocab, wl.max_seq, batch or wl.batch, wl.rms_eps, wl.rope_theta,
-                           int8=wl.weight_dtype == "int8", tied=wl.tied)
+                           int8=wl.weight_dtype == "int8", tied=wl.tied,
+                          int4=wl.weight_dtype == "int4", group_size=wl.group_size)
 
 
 def test_library_exports_every_declared_symbol(amk):
     lib = amk.lib()
     names = set()
-    for h in ("amk.h", "amk_plan.h"):
+    for h in ("amk.h", "amk_plan.h", "amk_unfused.h"):
         src = open(os.path.join(ROOT, "include", h)).read()
         names |= set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(amk_\w+)\s*\(", src, re.M))
-    assert len(names) == 20 and {"amk_create", "amk_decode_step", "amk_decode_step_greedy", "amk_destroy",
+    assert len(names) == 24 and {"amk_create", "amk_decode_step", "amk_decode_step_greedy", "amk_destroy",
                                  "amk_plan_build"} <= names, names
     for n in sorted(names):
         assert hasattr(lib, n), "libamk.so does not export %s" % n
@@ -140,12 +141,12 @@ def _coverage(wl, plan, B):
 
 def test_rejects_bad_configs(amk):
     wl = synth.workload("tiny")
-    for bad in ({"head_dim": 96}, {"n_kv_heads": 3}, {"max_batch": 9}, {"hidden": 250}):
+    for bad in ({"head_dim": 96}, {"n_kv_heads": 3}, {"max_batch": 17}, {"hidden": 250}):
         c = _cfg(amk, wl)
         for k, v in bad.items():
             setattr(c, k, v)
         with pytest.raises(amk.AmkError):
-            amk.Plan(c, min(c.max_batch, 8), 16)
+            amk.Plan(c, min(c.max_batch, 16), 16)
 
 
 # ------------------------------------------------------- independent checker

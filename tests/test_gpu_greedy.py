@@ -83,10 +83,11 @@ def test_greedy_step_matches_argmax_and_oracle_tiny():
         if s + 1 < wl.steps and margin[0] > MARGIN:
             checked += 1
             agree += int(fed[s + 1][0] == ref_tok[0])
-    log_parity("greedy_device", {"steps": wl.steps, "rows": [0], "worst": worst, "floor": 0.0, "max_abs": 0.0,
-                                 "strict_logits_ok": worst <= 1.0, "argmax_checked": checked,
-                                 "argmax_agree": agree, "strict_argmax_ok": agree == checked,
-                                 "relaxed_misses": checked - agree, "free_running": wl.steps})
+    log_parity("greedy_device", {"steps": wl.steps, "rows": [0], "worst": float(worst), "floor": 0.0,
+                                 "max_abs": 0.0, "strict_logits_ok": bool(worst <= 1.0),
+                                 "argmax_checked": int(checked), "argmax_agree": int(agree),
+                                 "strict_argmax_ok": bool(agree == checked), "relaxed_misses": int(checked - agree),
+                                 "free_running": wl.steps})
     assert worst <= 1.0
     assert agree == checked and checked > 20
 

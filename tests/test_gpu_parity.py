@@ -150,3 +150,86 @@ def test_llama2_7b_batch8_end_to_end_all_rows():
     # the test's CPU time
     wl = synth.workload("llama2_7b_b8")
     assert_end_to_end(teacher_forced(wl, steps=16, check_cache=False, floor=True))
+
+
+# ---- batches above 1: the tensor-core GEMV (bf16) and the batch-size sweep shape ----
+
+def test_tiny_batch16_ragged_positions():
+    # M = 16: both halves of the tensor-core A fragment carry sequences
+    wl = synth.workload("tiny", batch=16)
+    assert_ok(teacher_forced(wl, steps=5, positions0=[16 - (b % 9) * 2 for b in range(16)]))
+
+
+def test_tiny_batch9_and_k_split():
+    # one sequence in the upper half of the fragment; a K split adds the
+    # second slice's sums to the first's
+    wl = synth.workload("tiny", batch=9)
+    assert_ok(teacher_forced(wl, steps=4))
+    assert_ok(teacher_forced(synth.workload("tiny", batch=8), steps=4, options={"ksplit": 2}))
+
+
+def test_tiny_w8a16_batch5():
+    # int8 weights at batch above 1 take the CUDA-core tile
+    wl = synth.workload("tiny", batch=5, weight_dtype="int8", scale_jitter=0.5)
+    assert_ok(teacher_forced(wl, steps=4))
+
+
+def test_tinyllama_short_batch16_per_layer_and_end_to_end():
+    wl = synth.workload("tinyllama_1b1_short", batch=16)
+    assert_layers_ok(layerwise(wl, steps=1, check_rows=[0, 7, 8, 15]))
+    assert_end_to_end(teacher_forced(wl, steps=4, check_rows=[0, 9, 15], check_cache=False, floor=True))
+
+
+# ---- the per-operator comparison path (one launch per operator) ----
+
+def _unfused_teacher_forced(wl, steps):
+    import torch
+    import oracle
+    from tests.gpu_harness import engine_config
+    import persistent_sm_decode_gb300 as amk
+    from synth.device import kv_to_device, model_to_device
+    model = synth.make_model(wl, seed=1)
+    kc, vc = synth.make_kv(wl, seed=2)
+    dev = model_to_device(model)
+    u = amk.UnfusedEngine(engine_config(wl), dev["embed"], dev["final_norm"], dev["layers"], dev["lm_head"],
+                          dev["s_lm"])
+    kv = kv_to_device(kc, vc)
+    orc = oracle.Oracle(model, kc, vc)
+    lg = torch.empty((wl.batch, wl.vocab), dtype=torch.float32, device="cuda")
+    tok = synth.initial_tokens(wl)
+    worst = 0.0
+    for s in range(steps):
+        pos = np.full(wl.batch, wl.ctx + s, dtype=np.int32)
+        u.step(torch.from_numpy(tok).cuda(), torch.from_numpy(pos).cuda(), kv, lg)
+        torch.cuda.synchronize()
+        ref = orc.step(tok, pos)
+        got = lg.cpu().numpy().astype(np.float64)
+        worst = max(worst, float(np.abs(got - ref).max() / (1e-2 * np.abs(ref).max() + 1e-3)))
+        tok, _ = oracle.greedy(ref)
+    u.close()
+    return worst
+
+
+def test_unfused_tiny_matches_oracle():
+    assert _unfused_teacher_forced(synth.workload("tiny"), 8) <= 1.0
+
+
+def test_unfused_tiny_w8a16_matches_oracle():
+    assert _unfused_teacher_forced(synth.workload("tiny", weight_dtype="int8", scale_jitter=0.5), 6) <= 1.0
+
+
+# ---- W4A16: 4-bit weight codes with per-group scales (batch 1) ----
+
+def test_tiny_w4a16_group32():
+    # the tiny shape with I = 704 (a whole number of 32-weight chunks) and a
+    # scale every 32 weights, jittered so that a wrong group index shows
+    wl = synth.workload("tiny", weight_dtype="int4", intermediate=704, group_size=32, scale_jitter=0.5)
+    assert_ok(teacher_forced(wl))
+
+
+def test_tinyllama_1b1_w4a16_per_layer():
+    assert_layers_ok(layerwise(synth.workload("tinyllama_1b1_w4a16", scale_jitter=0.5), steps=2))
+
+
+def test_tinyllama_1b1_w4a16_end_to_end_32_steps():
+    assert_end_to_end(teacher_forced(synth.workload("tinyllama_1b1_w4a16"), steps=32, floor=True))
