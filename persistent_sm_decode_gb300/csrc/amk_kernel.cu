@@ -1521,7 +1521,8 @@ struct AttSmem {
     uint16_t *knew;  /* [d] bf16(rope(k)) of position p */
     uint16_t *vnew;  /* [d] */
     float *wst;      /* [NCW][GP][d + PART_PAD]: per-warp (o, m, l) of each head */
-    float *sbuf;     /* [NCW][ATT_BP][GP]: per-warp scores, then probabilities, of a block */
+    float *sbuf;     /* [NCW][GP] merge factors, then [GP] head maxima */
+    uint4 *qf;       /* [d / 16][32]: the q fragment of every k16 step and lane */
 };
 
 __device__ __forceinline__ AttSmem att_smem(const Params &p, Smem &s, int GP) {
@@ -1534,131 +1535,192 @@ __device__ __forceinline__ AttSmem att_smem(const Params &p, Smem &s, int GP) {
     base += align_up(2 * p.d * 2, 16);
     a.wst = reinterpret_cast<float *>(base);
     a.sbuf = a.wst + NCW * GP * (p.d + PART_PAD);
+    /* 16-byte aligned: q, k/v and wst are whole multiples of 16 bytes
+     * (NCW GP (d + PART_PAD) floats with d + PART_PAD a multiple of 4), and so
+     * is the block-score area of NCW ATT_BP GP floats */
+    a.qf = reinterpret_cast<uint4 *>(a.sbuf + NCW * ATT_BP * GP);
     return a;
 }
 
-/* Online-softmax state of one warp over all GP (= G rounded up to a power of
- * two) heads of a kv group.  Scoring: LP lanes share a position, each holding
- * EK consecutive elements of K and the matching EK q values of every head.
- * With one query head per kv head (multi-head attention) and D = 128, EK = 16,
- * so a warp scores four positions at once with three shuffle steps each
- * instead of one position with five; otherwise EK = 4.  Every wider form
- * measured (EK = 16 at D = 64 too, EK = 8 for two heads per kv head) made the
- * whole kernel spill more and slowed the grouped-query models by about 3%,
- * although their own instantiation was unchanged.  P.V: every lane owns EL = D / 32
- * output elements of every head.  m and l belong to head lane % GP
- * (replicated over its lanes). */
-template <int D, int GP>
-struct AttShape {
-    static constexpr int EK = (GP == 1 && D == 128) ? 16 : 4;
-    static constexpr int LP = D / EK;
-    static constexpr int PW = 32 / LP;
-    static constexpr int EL = D / 32;
-};
-
-template <int D, int GP>
+/* Tensor-core attention.  A warp takes blocks of up to 16 positions of a K/V
+ * tile in shared memory and keeps the online-softmax state of every head of
+ * the kv group (at most 8) over the positions it has seen.
+ *
+ * Scores S = Q K^T: one m16n8k16 bf16 mma per 8 positions and 16 dims.  A is
+ * the group's rotated, pre-scaled q split in two: row h holds bf16(q) of head
+ * h and row h + 8 the bf16 rounding of what is left, so S = D[h] + D[h + 8]
+ * carries q to about 16 bits at no extra mma; B is K, exact in bf16.  The
+ * sum over dims may take any order, so one lane reads 16 consecutive bytes of
+ * a K row per load: in k16 step (c, e) the fragment's dims 2t, 2t + 1, 2t + 8,
+ * 2t + 9 are the row's dims 32c + 8t + 4e + 0, 1, 2, 3.
+ *
+ * P.V as O^T += V^T P^T: m16n8k8 tf32 mmas per 16 dims and 8 positions, M =
+ * dims, N = heads, K = positions.  bf16 V is exact in tf32; P goes in twice,
+ * as its tf32 rounding and the tf32 rounding of the remainder, so it carries
+ * about 22 bits (one tf32 pass alone, 2^-11 relative, measurably widened the
+ * deep-stack deviation from the oracle).  Step j
+ * takes positions 8j .. 8j + 7 of the block with fragment slot t at position
+ * 8j + 2t and slot t + 4 at 8j + 2t + 1: exactly where the score fragment left
+ * P of head g in lane (g, t), so P needs no shuffle.  Row g of m-tile i is dim
+ * 2 w and row g + 8 dim 2 w + 1, w = 32 (i / 4) + 4g + i % 4, so a lane's V
+ * loads are 16 consecutive bytes and each load fills whole wavefronts.
+ *
+ * The q fragments are the same in every warp: they are made once per task
+ * into shared memory.  Lane (g, t) holds the O^T accumulators of heads 2t and
+ * 2t + 1 at those dims; the running maximum m of head g (equal in the four
+ * lanes of a quad); and its own part of the sum l of head g. */
+template <int D>
 struct AttState {
-    float q[GP][AttShape<D, GP>::EK];
-    float o[GP][AttShape<D, GP>::EL];
+    static constexpr int KS = D / 16; /* k16 steps of the scores = m-tiles of P.V */
+    float o[KS][4];
     float m, l;
 };
 
-/* positions j0 .. j0 + nb - 1 (nb <= ATT_BP) of a K/V tile in shared memory */
-template <int D, int GP>
-__device__ __forceinline__ void att_block(AttState<D, GP> &st, const uint16_t *Kt, const uint16_t *Vt, int j0,
-                                          int nb, float *sb, int lane) {
-    constexpr int d = D, EK = AttShape<D, GP>::EK, LP = AttShape<D, GP>::LP, PW = AttShape<D, GP>::PW;
-    constexpr int EL = AttShape<D, GP>::EL, LPH = 32 / GP;
-    /* a task runs this block once or a few times per layer, so its code is
-     * usually not in the instruction cache: with many heads per kv head the
-     * loops stay rolled (less code to fetch); with few, they unroll */
-    constexpr int UR = GP >= 4 ? 1 : 4;
-    const int pg = lane / LP, ch = lane % LP, li = lane % LP;
-    /* scores of every head for PW positions at a time */
-#pragma unroll UR
-    for (int it = 0; it * PW < nb; ++it) {
-        const int jj = it * PW + pg;
-        float sc[GP];
-        if (jj < nb) {
-            const uint2 *kr = reinterpret_cast<const uint2 *>(Kt + (size_t)(j0 + jj) * d + ch * EK);
-#pragma unroll
-            for (int q4 = 0; q4 < EK / 4; ++q4) {
-                const uint2 kv = kr[q4];
-                const float k0 = bf_lo(kv.x), k1 = bf_hi(kv.x), k2 = bf_lo(kv.y), k3 = bf_hi(kv.y);
-#pragma unroll
-                for (int h = 0; h < GP; ++h) {
-                    const float part = fmaf(st.q[h][4 * q4], k0, st.q[h][4 * q4 + 1] * k1) +
-                                       fmaf(st.q[h][4 * q4 + 2], k2, st.q[h][4 * q4 + 3] * k3);
-                    sc[h] = q4 == 0 ? part : sc[h] + part;
-                }
-            }
-        } else {
-#pragma unroll
-            for (int h = 0; h < GP; ++h) sc[h] = 0.f;
-        }
-        const float t = xsum_g<GP, LP>(sc, lane);
-        if (li % (LP / GP) == 0 && jj < nb) sb[jj * GP + li / (LP / GP)] = t;
-    }
-    __syncwarp();
-    /* online softmax, head lane % GP over positions lane / GP + LPH k */
-    const int hh = lane % GP, k0 = lane / GP;
-    float mb = -INFINITY;
-#pragma unroll 1
-    for (int jj = k0; jj < nb; jj += LPH) mb = fmaxf(mb, sb[jj * GP + hh]);
-#pragma unroll
-    for (int o = GP; o < 32; o <<= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
-    const float mnew = fmaxf(st.m, mb);
-    const float alpha = exp2f(st.m - mnew);
-    float ps = 0.f;
-#pragma unroll 1
-    for (int jj = k0; jj < nb; jj += LPH) {
-        const float pv = exp2f(sb[jj * GP + hh] - mnew);
-        sb[jj * GP + hh] = pv;
-        ps += pv;
-    }
-#pragma unroll
-    for (int o = GP; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-    st.l = st.l * alpha + ps;
-    st.m = mnew;
-#pragma unroll
-    for (int h = 0; h < GP; ++h) {
-        const float ah = __shfl_sync(0xffffffffu, alpha, h);
-#pragma unroll
-        for (int e = 0; e < EL; ++e) st.o[h][e] *= ah;
-    }
-    __syncwarp();
-    /* P.V */
-    const uint16_t *vcol = Vt + (size_t)j0 * d + lane * EL;
-#pragma unroll UR
-    for (int i = 0; i < nb; ++i) {
-        float v[EL];
-        if constexpr (EL == 2) {
-            const uint32_t w = *reinterpret_cast<const uint32_t *>(vcol + (size_t)i * d);
-            v[0] = bf_lo(w);
-            v[1] = bf_hi(w);
-        } else {
-            const uint2 w = *reinterpret_cast<const uint2 *>(vcol + (size_t)i * d);
-            v[0] = bf_lo(w.x);
-            v[1] = bf_hi(w.x);
-            v[2] = bf_lo(w.y);
-            v[3] = bf_hi(w.y);
-        }
-        const float *pr = sb + i * GP;
-#pragma unroll
-        for (int h = 0; h < GP; ++h) {
-            const float ph = pr[h];
-#pragma unroll
-            for (int e = 0; e < EL; ++e) st.o[h][e] = fmaf(ph, v[e], st.o[h][e]);
-        }
-    }
-    __syncwarp();
+/* D += A.B on the tensor cores: m16n8k8, tf32 operands, fp32 accumulators */
+__device__ __forceinline__ void mma_tf32_1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int D, int GP>
-__device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, Ring &rg, int ctid, int warp, int lane) {
-    constexpr int EL = AttShape<D, GP>::EL, EK = AttShape<D, GP>::EK, LP = AttShape<D, GP>::LP;
+__device__ __forceinline__ uint32_t f2tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+/* q fragment of k16 step s for lane (g, t), from q ([G][D] fp32 in shared
+ * memory; heads g >= G are zero): rows g and g + 8 of A */
+template <int D>
+__device__ __forceinline__ uint4 att_qfrag(const float *q, int G, int s, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (g < G) v = *reinterpret_cast<const float4 *>(q + g * D + 32 * (s >> 1) + 8 * t + 4 * (s & 1));
+    const float h0 = round_bf(v.x), h1 = round_bf(v.y), h2 = round_bf(v.z), h3 = round_bf(v.w);
+    return make_uint4(pack_bf2(h0, h1), pack_bf2(v.x - h0, v.y - h1), pack_bf2(h2, h3), pack_bf2(v.z - h2, v.w - h3));
+}
+
+template <int D>
+__device__ __forceinline__ void att_init(AttState<D> &st) {
+#pragma unroll
+    for (int s = 0; s < AttState<D>::KS; ++s) st.o[s][0] = st.o[s][1] = st.o[s][2] = st.o[s][3] = 0.f;
+    st.m = -INFINITY;
+    st.l = 0.f;
+}
+
+/* positions j0 .. j0 + nb - 1 (1 <= nb <= 16) of a K/V tile in shared memory
+ * (rows of D bf16); rows past nb are not read */
+template <int D>
+__device__ __forceinline__ void att_block(AttState<D> &st, const uint4 *qf, const uint16_t *Kt, const uint16_t *Vt,
+                                          int j0, int nb, int lane) {
+    constexpr int KS = AttState<D>::KS;
+    const int g = lane >> 2, t = lane & 3;
+    float sc[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+    const bool ok0 = g < nb, ok1 = 8 + g < nb;
+    const uint4 *kr0 = reinterpret_cast<const uint4 *>(Kt + (size_t)(j0 + g) * D) + t;
+    const uint4 *kr1 = reinterpret_cast<const uint4 *>(Kt + (size_t)(j0 + 8 + g) * D) + t;
+#pragma unroll
+    for (int c = 0; c < KS / 2; ++c) {
+        const uint4 k0 = ok0 ? kr0[4 * c] : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 k1 = ok1 ? kr1[4 * c] : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 qa = qf[2 * c * 32 + lane], qb = qf[(2 * c + 1) * 32 + lane];
+        mma_bf16_16816(sc[0], qa.x, qa.y, qa.z, qa.w, k0.x, k0.y);
+        mma_bf16_16816(sc[1], qa.x, qa.y, qa.z, qa.w, k1.x, k1.y);
+        mma_bf16_16816(sc[0], qb.x, qb.y, qb.z, qb.w, k0.z, k0.w);
+        mma_bf16_16816(sc[1], qb.x, qb.y, qb.z, qb.w, k1.z, k1.w);
+    }
+    /* head g at positions 8j + 2t + e */
+    float sv[2][2];
+    float mb = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            sv[j][e] = 8 * j + 2 * t + e < nb ? sc[j][e] + sc[j][2 + e] : -INFINITY;
+            mb = fmaxf(mb, sv[j][e]);
+        }
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+    const float mnew = fmaxf(st.m, mb); /* finite: position 0 is in the block */
+    const float alpha = exp2f(st.m - mnew);
+    uint32_t pb[2][2], pl[2][2];
+    float ps = 0.f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float pv = exp2f(sv[j][e] - mnew);
+            ps += pv;
+            pb[j][e] = f2tf32(pv);
+            pl[j][e] = f2tf32(pv - __uint_as_float(pb[j][e]));
+        }
+    st.l = st.l * alpha + ps;
+    st.m = mnew;
+    const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);     /* head 2t */
+    const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4); /* head 2t + 1 */
+#pragma unroll
+    for (int i = 0; i < KS; ++i) {
+        st.o[i][0] *= a0;
+        st.o[i][1] *= a1;
+        st.o[i][2] *= a0;
+        st.o[i][3] *= a1;
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int r0 = 8 * j + 2 * t;
+        const uint4 *v0 = reinterpret_cast<const uint4 *>(Vt + (size_t)(j0 + r0) * D) + g;
+        const uint4 *v1 = reinterpret_cast<const uint4 *>(Vt + (size_t)(j0 + r0 + 1) * D) + g;
+#pragma unroll
+        for (int hq = 0; hq < KS / 4; ++hq) {
+            const uint4 x0 = r0 < nb ? v0[8 * hq] : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 x1 = r0 + 1 < nb ? v1[8 * hq] : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t w0[4] = {x0.x, x0.y, x0.z, x0.w}, w1[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+            for (int i4 = 0; i4 < 4; ++i4) {
+                const uint32_t a0 = w0[i4] << 16, a1 = w0[i4] & 0xffff0000u;
+                const uint32_t a2 = w1[i4] << 16, a3 = w1[i4] & 0xffff0000u;
+                mma_tf32_1688(st.o[4 * hq + i4], a0, a1, a2, a3, pb[j][0], pb[j][1]);
+                mma_tf32_1688(st.o[4 * hq + i4], a0, a1, a2, a3, pl[j][0], pl[j][1]);
+            }
+        }
+    }
+}
+
+/* the warp's state into w = [GP][D + PART_PAD]: o of every head, then m and
+ * the full l of head g (its quad's parts added) */
+template <int D>
+__device__ __forceinline__ void att_store(const AttState<D> &st, float *w, int GP, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    constexpr int RS = D + PART_PAD;
+#pragma unroll
+    for (int i = 0; i < AttState<D>::KS; ++i) {
+        const int dm = 2 * (32 * (i >> 2) + 4 * g + (i & 3));
+        if (2 * t < GP) {
+            w[2 * t * RS + dm] = st.o[i][0];
+            w[2 * t * RS + dm + 1] = st.o[i][2];
+        }
+        if (2 * t + 1 < GP) {
+            w[(2 * t + 1) * RS + dm] = st.o[i][1];
+            w[(2 * t + 1) * RS + dm + 1] = st.o[i][3];
+        }
+    }
+    float l = st.l + __shfl_xor_sync(0xffffffffu, st.l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (t == 0 && g < GP) {
+        w[g * RS + D] = st.m;
+        w[g * RS + D + 1] = l;
+    }
+}
+
+template <int D>
+__device__ bool att_task(const Params &p, Smem &s, const Task &t, int ti, Ring &rg, int ctid, int warp, int lane) {
     constexpr int d = D;
-    const int G = p.G, NS = p.n_slots;
+    const int G = p.G, GP = att_gp(G), NS = p.n_slots;
     const int l = t.layer, slot = l % p.depth, b = t.b, grp = t.g;
     const AttGeo ag = att_geo(p, t);
     const bool active_seq = b < p.batch;
@@ -1729,24 +1791,15 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
         }
     }
 
-    AttState<D, GP> st;
-    st.m = -INFINITY;
-    st.l = 0.f;
-    {
-        const int ch = lane % LP;
-#pragma unroll
-        for (int h = 0; h < GP; ++h)
-#pragma unroll
-            for (int e = 0; e < EK; ++e) st.q[h][e] = h < G ? as.q[h * d + ch * EK + e] : 0.f;
-#pragma unroll
-        for (int h = 0; h < GP; ++h)
-#pragma unroll
-            for (int e = 0; e < EL; ++e) st.o[h][e] = 0.f;
-    }
-    float *sb = as.sbuf + warp * ATT_BP * GP;
+    /* the q fragments, once for all warps */
+    if (ctid < AttState<D>::KS * 32) as.qf[ctid] = att_qfrag<D>(as.q, active_seq ? G : 0, ctid >> 5, ctid & 31);
+    cbar();
+    AttState<D> st;
+    att_init<D>(st);
 
     const bool with_new = active_seq && (t.flags & TF_NEW_TOKEN);
     bool new_done = false; /* warp-uniform */
+    int gb = 0;            /* blocks of 16 positions dealt so far, round-robin over the warps */
     for (int k = 0; k < ag.ntile; ++k, rg.advance(NS)) {
         const int sl = rg.slot;
         const unsigned long long tw0 = TRACE(p) ? now_ns() : 0;
@@ -1762,10 +1815,9 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
          * covers it copies its K and V into that row first */
         const bool add_new = with_new && k == ag.ntile - 1 && nt < (int)t.rows_per_stage;
         const int ntot = nt + (add_new ? 1 : 0);
-        constexpr int PW = AttShape<D, GP>::PW;
-        const int per = min(ATT_BP, ((ntot + NCW - 1) / NCW + PW - 1) / PW * PW);
-        for (int j0 = warp * per; j0 < ntot; j0 += NCW * per) {
-            const int nb = min(per, ntot - j0);
+        const int nblk = (ntot + ATT_BP - 1) / ATT_BP;
+        for (int bi = (warp - gb % NCW + NCW) % NCW; bi < nblk; bi += NCW) {
+            const int j0 = bi * ATT_BP, nb = min(ATT_BP, ntot - j0);
             if (add_new && j0 <= nt && nt < j0 + nb) {
                 for (int i = lane; i < d / 8; i += 32) {
                     reinterpret_cast<uint4 *>(Kt + (size_t)nt * d)[i] = reinterpret_cast<const uint4 *>(as.knew)[i];
@@ -1773,8 +1825,9 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
                 }
                 __syncwarp();
             }
-            att_block<D, GP>(st, Kt, Vt, j0, nb, sb, lane);
+            att_block<D>(st, as.qf, Kt, Vt, j0, nb, lane);
         }
+        gb += nblk;
         if (add_new) new_done = true;
         if (TRACE(p) && warp == 0 && lane == 0) {
             s.misc->t_wait_full += tw1 - tw0;
@@ -1783,22 +1836,12 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.empty[sl]);
     }
-    /* otherwise the new position on its own, from shared memory, on the last warp */
-    if (with_new && !new_done && warp == NCW - 1) att_block<D, GP>(st, as.knew, as.vnew, 0, 1, sb, lane);
+    /* otherwise the new position on its own, from shared memory, on the next warp in turn */
+    if (with_new && !new_done && warp == gb % NCW) att_block<D>(st, as.qf, as.knew, as.vnew, 0, 1, lane);
     if (TRACE(p) && ctid == 0) s.misc->t_stages = now_ns();
 
-    /* the warp's state: o of every head, m and l of head lane (lane < GP) */
-    {
-        float *w = as.wst + (size_t)warp * GP * (d + PART_PAD);
-#pragma unroll
-        for (int h = 0; h < GP; ++h)
-#pragma unroll
-            for (int e = 0; e < EL; ++e) w[(size_t)h * (d + PART_PAD) + lane * EL + e] = st.o[h][e];
-        if (lane < GP) {
-            w[(size_t)lane * (d + PART_PAD) + d] = st.m;
-            w[(size_t)lane * (d + PART_PAD) + d + 1] = st.l;
-        }
-    }
+    /* the warp's state: o of every head, m and l of each head */
+    att_store<D>(st, as.wst + (size_t)warp * GP * (d + PART_PAD), GP, lane);
     if (cbar_or(s.misc->abort != 0)) return false;
 
     /* merge the warps of each head.  First the per-(warp, head) factors
@@ -1838,14 +1881,6 @@ __device__ bool att_task_impl(const Params &p, Smem &s, const Task &t, int ti, R
     return !cbar_or(s.misc->abort != 0);
 }
 
-template <int D>
-__device__ bool att_task(const Params &p, Smem &s, const Task &t, int ti, Ring &rg, int ctid, int warp, int lane) {
-    const int GP = att_gp(p.G);
-    if (GP == 1) return att_task_impl<D, 1>(p, s, t, ti, rg, ctid, warp, lane);
-    if (GP == 2) return att_task_impl<D, 2>(p, s, t, ti, rg, ctid, warp, lane);
-    if (GP == 4) return att_task_impl<D, 4>(p, s, t, ti, rg, ctid, warp, lane);
-    return att_task_impl<D, 8>(p, s, t, ti, rg, ctid, warp, lane);
-}
 
 /* Merge the C chunk partials of one query head of one sequence into its bf16
  * attention output: o = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c (the

@@ -79,11 +79,12 @@ struct SmemModel {
 };
 
 /* attention task: q of the group, the new k and v, per-warp (o, m, l) of every
- * head, per-warp block scores */
+ * head, the merge's per-warp factors and head maxima, the q fragments of the
+ * tensor-core scores */
 int att_smem_need(const Geo &g) {
     const int GP = att_gp(g.G);
     return align_up(GP * g.d * 4, 16) + align_up(2 * g.d * 2, 16) + NCW * GP * (g.d + PART_PAD) * 4 +
-           NCW * ATT_BP * GP * 4 + 256;
+           NCW * ATT_BP * GP * 4 + 16 + (g.d / 16) * 32 * 16 + 256;
 }
 
 /* merge task: per-lane-group sums of o and l, and chunk maxima */
@@ -780,7 +781,9 @@ amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_c
                 k.n_slots = ns;
                 k.ksplit = ks;
                 k.depth = o.scratch_depth > 0 ? std::min(o.scratch_depth, cfg->n_layers + 1) : 2;
+                /* whole blocks of 16 positions per attention tile where the slot holds them */
                 k.att_tile = std::min(256, slot / (4 * g.d));
+                if (k.att_tile >= ATT_BP) k.att_tile -= k.att_tile % ATT_BP;
                 k.l2_prefetch_kb = o.l2_prefetch_kb < 0 ? 0 : o.l2_prefetch_kb > 0 ? o.l2_prefetch_kb : L2_PREFETCH_KB;
                 k.evict_first = o.l2_evict_first < 0 ? 0 : o.l2_evict_first > 0 ? 1 : EVICT_FIRST;
                 pts.push_back({model_cost_us(g, k, n_sm), k});
