@@ -674,6 +674,7 @@ __device__ __forceinline__ void load_x4s(const Params &p, Smem &s, const uint64_
  * per word.  r_b is computed once per task (need_r) from the whole of x[b].
  * Reading x waits for its producers, XU groups of four per thread at a time. */
 constexpr int XU = 4;
+template <int NB>
 __device__ void norm_prologue(const Params &p, Smem &s, const uint64_t *xbase, bool from_embed, const uint16_t *gain,
                               int k0, int k1, bool need_r, uint32_t f, int task, int which, int ctid, int warp,
                               int lane) {
@@ -717,6 +718,62 @@ __device__ void norm_prologue(const Params &p, Smem &s, const uint64_t *xbase, b
         }
         return;
     }
+    const int kc = k1 - k0, a4 = k0 / 4, n4 = kc / 4, apitch = smem_pitch(kc * 2, p.Bmax);
+    if (NB > 1 && !from_embed && H4 % 32 == 0) {
+        /* several sequences: the rows of x are contiguous, so both passes run
+         * over (sequence, group) pairs, XB groups per thread at a time, and
+         * one round trip serves several sequences.  A warp's 32 groups of a
+         * round belong to one sequence (H4 is a multiple of 32). */
+        constexpr int XB = 4;
+        if (need_r) {
+            if (lane < p.batch) s.misc->red[lane][warp] = 0.f;
+            __syncwarp();
+            const int T = p.batch * H4;
+            for (int i0 = ctid; i0 < T; i0 += XB * TS) {
+                float4 x[XB];
+                load_x4s<XB>(p, s, xbase, nullptr, [=](int u) { return i0 + u * TS < T ? i0 + u * TS : -1; }, x, f,
+                             task, which);
+#pragma unroll
+                for (int u = 0; u < XB; ++u) {
+                    const int i = i0 + u * TS;
+                    if (i - lane >= T) break; /* warp-uniform: the warp's groups are past the end */
+                    float v = i < T ? x[u].x * x[u].x + x[u].y * x[u].y + x[u].z * x[u].z + x[u].w * x[u].w : 0.f;
+                    v = warp_sum(v);
+                    if (lane == 0) s.misc->red[i / H4][warp] += v;
+                }
+            }
+            cbar();
+            if (ctid < p.batch) {
+                float ss = 0.f;
+#pragma unroll
+                for (int w = 0; w < NCW; ++w) ss += s.misc->red[ctid][w];
+                s.misc->rnorm[ctid] = rsqrtf(ss / (float)H + p.eps);
+            }
+            cbar();
+        }
+        const int T = p.batch * n4;
+        for (int i0 = ctid; i0 < T; i0 += XB * TS) {
+            float4 x[XB];
+            load_x4s<XB>(p, s, xbase, nullptr, [=](int u) {
+                const int i = i0 + u * TS;
+                return i < T ? (i / n4) * H4 + a4 + i % n4 : -1;
+            }, x, f, task, which);
+#pragma unroll
+            for (int u = 0; u < XB; ++u) {
+                const int i = i0 + u * TS;
+                if (i < T) {
+                    const int b = i / n4, j = i % n4;
+                    const float r = s.misc->rnorm[b];
+                    const float4 v = x[u];
+                    const uint2 gw = __ldg(reinterpret_cast<const uint2 *>(gain) + a4 + j);
+                    reinterpret_cast<uint2 *>(s.act + (size_t)b * apitch)[j] =
+                        make_uint2(pack_bf2(v.x * r * bf_lo(gw.x), v.y * r * bf_hi(gw.x)),
+                                   pack_bf2(v.z * r * bf_lo(gw.y), v.w * r * bf_hi(gw.y)));
+                }
+            }
+        }
+        return;
+    }
     if (need_r) {
         for (int b = 0; b < p.batch; ++b) {
             const uint64_t *xs = from_embed ? nullptr : xbase + (size_t)b * H;
@@ -741,7 +798,6 @@ __device__ void norm_prologue(const Params &p, Smem &s, const uint64_t *xbase, b
         }
         cbar();
     }
-    const int kc = k1 - k0, a4 = k0 / 4, n4 = kc / 4, apitch = smem_pitch(kc * 2, p.Bmax);
     for (int b = 0; b < p.batch; ++b) {
         const uint64_t *xs = from_embed ? nullptr : xbase + (size_t)b * H;
         const uint16_t *emb = from_embed ? p.embed + (size_t)__ldg(p.tokens + b) * H : nullptr;
@@ -909,53 +965,75 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
  * pairs A and B through one permutation: thread t of a fragment row supplies
  * the four consecutive elements 4t .. 4t + 3 (one 8-byte shared load) where
  * the fragment layout names elements 2t, 2t + 1, 2t + 8, 2t + 9.  Warp w
- * takes K segment w of 8 for every row block of the stage, up to RB row
- * blocks at once: one activation load serves them all and their
- * accumulators form independent chains.  res[(w * sstride + row) * Bmax + b]
- * receives the warp's partial sums (added over K-split passes). */
+ * takes K segment w of 8 for every row block of the stage.  A dependent
+ * chain of mmas waits out each one's latency, so the warp keeps four
+ * independent accumulators: NR row blocks times CH interleaved K chains
+ * (k16 step kb feeds chain kb % CH), summed at the end. */
+template <int NB, int NR, int CH>
+__device__ __forceinline__ void mma_chains(const uint8_t *tile, int rb0, int nrows, int wpitch, const uint8_t *x0,
+                                           const uint8_t *x1, bool lo, bool hi, int k0, int k1, int batch,
+                                           float *res, int sstride, int Bmax, bool first, int warp, int g, int t) {
+    float acc[NR * CH][4];
+    const uint8_t *wr[NR];
+    bool rok[NR];
+#pragma unroll
+    for (int a = 0; a < NR * CH; ++a) acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        rok[r] = rb0 + 8 * r + g < nrows;
+        wr[r] = tile + (size_t)(rb0 + 8 * r + g) * wpitch + 8 * t;
+    }
+    for (int kb = k0; kb < k1; kb += CH) {
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            if (kb + c >= k1) break; /* warp-uniform */
+            const int ko = 32 * (kb + c);
+            const uint2 a = lo ? *reinterpret_cast<const uint2 *>(x0 + ko) : make_uint2(0u, 0u);
+            const uint2 e = hi ? *reinterpret_cast<const uint2 *>(x1 + ko) : make_uint2(0u, 0u);
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                const uint2 w = rok[r] ? *reinterpret_cast<const uint2 *>(wr[r] + ko) : make_uint2(0u, 0u);
+                mma_bf16_16816(acc[r * CH + c], a.x, e.x, a.y, e.y, w.x, w.y);
+            }
+        }
+    }
+    /* acc 0, 1: sequence g, rows 2t, 2t + 1 of the block; 2, 3: sequence g + 8 */
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float v = acc[r * CH][q];
+#pragma unroll
+            for (int c = 1; c < CH; ++c) v += acc[r * CH + c][q];
+            const int b = g + (q >= 2 ? 8 : 0), rr = rb0 + 8 * r + 2 * t + (q & 1);
+            if (b < batch && rr < nrows) {
+                float *o = res + ((size_t)warp * sstride + rr) * Bmax + b;
+                *o = first ? v : *o + v;
+            }
+        }
+}
+
+/* res[(w * sstride + row) * Bmax + b] receives the warp's partial sums
+ * (added over K-split passes) */
 template <int NB>
 __device__ void gemv_tile_mma(const uint8_t *tile, int nrows, int Kc, int wpitch, const uint8_t *act, int apitch,
                               int batch, float *res, int sstride, int Bmax, bool first, int warp, int lane) {
-    constexpr int RB = 4;
     const int g = lane >> 2, t = lane & 3;
     const int nblk = Kc / 16, k0 = warp * nblk / NCW, k1 = (warp + 1) * nblk / NCW;
     const bool lo = g < batch, hi = NB > 8 && g + 8 < batch;
     const uint8_t *x0 = act + (size_t)g * apitch + 8 * t;
     const uint8_t *x1 = act + (size_t)(g + 8) * apitch + 8 * t;
-    for (int rb0 = 0; rb0 < nrows; rb0 += 8 * RB) {
-        float d[RB][4];
-        const uint8_t *wr[RB];
-        bool rok[RB];
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            d[r][0] = d[r][1] = d[r][2] = d[r][3] = 0.f;
-            rok[r] = rb0 + 8 * r + g < nrows;
-            wr[r] = tile + (size_t)(rb0 + 8 * r + g) * wpitch + 8 * t;
-        }
-        const int nrb = min(RB, (nrows - rb0 + 7) / 8); /* warp-uniform: row blocks with rows */
-#pragma unroll 2
-        for (int kb = k0; kb < k1; ++kb) {
-            const uint2 a = lo ? *reinterpret_cast<const uint2 *>(x0 + 32 * kb) : make_uint2(0u, 0u);
-            const uint2 c = hi ? *reinterpret_cast<const uint2 *>(x1 + 32 * kb) : make_uint2(0u, 0u);
-#pragma unroll
-            for (int r = 0; r < RB; ++r) {
-                if (r >= nrb) break;
-                const uint2 w = rok[r] ? *reinterpret_cast<const uint2 *>(wr[r] + 32 * kb) : make_uint2(0u, 0u);
-                mma_bf16_16816(d[r], a.x, c.x, a.y, c.y, w.x, w.y);
-            }
-        }
-        /* d0, d1: sequence g, rows 2t, 2t + 1 of the block; d2, d3: sequence g + 8 */
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int b = g + (q >= 2 ? 8 : 0), rr = rb0 + 8 * r + 2 * t + (q & 1);
-                if (b < batch && rr < nrows) {
-                    float *o = res + ((size_t)warp * sstride + rr) * Bmax + b;
-                    *o = first ? d[r][q] : *o + d[r][q];
-                }
-            }
-        }
+    for (int rb0 = 0; rb0 < nrows; rb0 += 32) {
+        const int nrb = min(4, (nrows - rb0 + 7) / 8); /* warp-uniform: row blocks with rows */
+        if (nrb == 1)
+            mma_chains<NB, 1, 4>(tile, rb0, nrows, wpitch, x0, x1, lo, hi, k0, k1, batch, res, sstride, Bmax, first,
+                                 warp, g, t);
+        else if (nrb == 2)
+            mma_chains<NB, 2, 2>(tile, rb0, nrows, wpitch, x0, x1, lo, hi, k0, k1, batch, res, sstride, Bmax, first,
+                                 warp, g, t);
+        else
+            mma_chains<NB, 4, 1>(tile, rb0, nrows, wpitch, x0, x1, lo, hi, k0, k1, batch, res, sstride, Bmax, first,
+                                 warp, g, t);
     }
 }
 
@@ -1469,7 +1547,7 @@ __device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring 
     for (int kp = 0; kp < g.ks; ++kp) {
         const int k0 = kp * g.Kc, k1 = k0 + g.Kc;
         if (norm)
-            norm_prologue(p, s, src, emb, gain, k0, k1, kp == 0, f, ti, which, ctid, warp, lane);
+            norm_prologue<NB>(p, s, src, emb, gain, k0, k1, kp == 0, f, ti, which, ctid, warp, lane);
         else
             copy_prologue(p, s, src, len, k0, k1, f, ti, which, ctid);
         if (cbar_or(s.misc->abort != 0)) return false;
