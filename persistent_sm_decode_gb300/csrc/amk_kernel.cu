@@ -959,82 +959,110 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 }
 
 /* Batched tensor-core tile (bf16 weights, batch 2..16).  One m16n8k16 takes
- * the activations as A (M = the sequences, rows 8..15 zero up to batch 8)
- * and 8 weight rows as B (N = 8 output rows), so D holds 8 outputs of every
- * sequence.  The sum over K is the same for any order of K, so each k16 step
- * pairs A and B through one permutation: thread t of a fragment row supplies
- * the four consecutive elements 4t .. 4t + 3 (one 8-byte shared load) where
- * the fragment layout names elements 2t, 2t + 1, 2t + 8, 2t + 9.  Warp w
- * takes K segment w of 8 for every row block of the stage.  A dependent
- * chain of mmas waits out each one's latency, so the warp keeps four
- * independent accumulators: NR row blocks times CH interleaved K chains
- * (k16 step kb feeds chain kb % CH), summed at the end. */
-template <int NB, int NR, int CH>
-__device__ __forceinline__ void mma_chains(const uint8_t *tile, int rb0, int nrows, int wpitch, const uint8_t *x0,
-                                           const uint8_t *x1, bool lo, bool hi, int k0, int k1, int batch,
-                                           float *res, int sstride, int Bmax, bool first, int warp, int g, int t) {
-    float acc[NR * CH][4];
-    const uint8_t *wr[NR];
-    bool rok[NR];
+ * 16 weight rows as A (M = output rows) and the activations of 8 sequences as
+ * B (N = sequences; a second n-tile above batch 8), so every weight element
+ * loaded feeds all sequences.  The sum over K is the same for any order of
+ * K, so each k16 step pairs A and B through one permutation: thread t of a
+ * fragment row supplies the four consecutive elements 4t .. 4t + 3 (one
+ * 8-byte shared load) where the fragment layout names elements 2t, 2t + 1,
+ * 2t + 8, 2t + 9.  Warp w takes K segment w of 8 for every row block of the
+ * stage.  A dependent chain of mmas waits out each one's latency, so the
+ * warp keeps several independent accumulator sets (four with one n-tile, two
+ * with two): NR row blocks times CH interleaved K chains (k16 step kb feeds
+ * chain kb % CH), summed at the end.
+ * res[(w * sstride + row) * Bmax + b] receives the warp's partial sums
+ * (added over K-split passes). */
+template <int NT, int NR, int CH>
+__device__ __forceinline__ void mma_chains(const uint8_t *tile, int rb0, int nrows, int wpitch, const uint8_t *act,
+                                           int apitch, int batch, int k0, int k1, float *res, int sstride, int Bmax,
+                                           bool first, int warp, int g, int t) {
+    float acc[NR * CH][NT][4];
+    int wr[NR][2]; /* byte offsets into the tile and the activations */
+    bool rok[NR][2];
+    int xs[NT];
+    bool xok[NT];
 #pragma unroll
-    for (int a = 0; a < NR * CH; ++a) acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
+    for (int a = 0; a < NR * CH; ++a)
 #pragma unroll
-    for (int r = 0; r < NR; ++r) {
-        rok[r] = rb0 + 8 * r + g < nrows;
-        wr[r] = tile + (size_t)(rb0 + 8 * r + g) * wpitch + 8 * t;
+        for (int n = 0; n < NT; ++n) acc[a][n][0] = acc[a][n][1] = acc[a][n][2] = acc[a][n][3] = 0.f;
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = rb0 + 16 * r + 8 * h + g;
+            rok[r][h] = row < nrows;
+            wr[r][h] = row * wpitch + 8 * t;
+        }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        xok[n] = 8 * n + g < batch;
+        xs[n] = (8 * n + g) * apitch + 8 * t;
     }
     for (int kb = k0; kb < k1; kb += CH) {
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
             if (kb + c >= k1) break; /* warp-uniform */
             const int ko = 32 * (kb + c);
-            const uint2 a = lo ? *reinterpret_cast<const uint2 *>(x0 + ko) : make_uint2(0u, 0u);
-            const uint2 e = hi ? *reinterpret_cast<const uint2 *>(x1 + ko) : make_uint2(0u, 0u);
+            uint2 bx[NT];
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+                bx[n] = xok[n] ? *reinterpret_cast<const uint2 *>(act + xs[n] + ko) : make_uint2(0u, 0u);
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
-                const uint2 w = rok[r] ? *reinterpret_cast<const uint2 *>(wr[r] + ko) : make_uint2(0u, 0u);
-                mma_bf16_16816(acc[r * CH + c], a.x, e.x, a.y, e.y, w.x, w.y);
+                const uint2 w0 = rok[r][0] ? *reinterpret_cast<const uint2 *>(tile + wr[r][0] + ko) : make_uint2(0u, 0u);
+                const uint2 w1 = rok[r][1] ? *reinterpret_cast<const uint2 *>(tile + wr[r][1] + ko) : make_uint2(0u, 0u);
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+                    mma_bf16_16816(acc[r * CH + c][n], w0.x, w1.x, w0.y, w1.y, bx[n].x, bx[n].y);
             }
         }
     }
-    /* acc 0, 1: sequence g, rows 2t, 2t + 1 of the block; 2, 3: sequence g + 8 */
+    /* acc 0, 1: row g, sequences 2t, 2t + 1 of the n-tile; 2, 3: row g + 8 */
 #pragma unroll
     for (int r = 0; r < NR; ++r)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            float v = acc[r * CH][q];
+        for (int n = 0; n < NT; ++n)
 #pragma unroll
-            for (int c = 1; c < CH; ++c) v += acc[r * CH + c][q];
-            const int b = g + (q >= 2 ? 8 : 0), rr = rb0 + 8 * r + 2 * t + (q & 1);
-            if (b < batch && rr < nrows) {
-                float *o = res + ((size_t)warp * sstride + rr) * Bmax + b;
-                *o = first ? v : *o + v;
+            for (int q = 0; q < 4; ++q) {
+                float v = acc[r * CH][n][q];
+#pragma unroll
+                for (int c = 1; c < CH; ++c) v += acc[r * CH + c][n][q];
+                const int rr = rb0 + 16 * r + g + (q >= 2 ? 8 : 0), b = 8 * n + 2 * t + (q & 1);
+                if (b < batch && rr < nrows) {
+                    float *o = res + ((size_t)warp * sstride + rr) * Bmax + b;
+                    *o = first ? v : *o + v;
+                }
             }
-        }
 }
 
-/* res[(w * sstride + row) * Bmax + b] receives the warp's partial sums
- * (added over K-split passes) */
+template <int NT>
+__device__ void gemv_tile_mma_nt(const uint8_t *tile, int nrows, int Kc, int wpitch, const uint8_t *act, int apitch,
+                                 int batch, float *res, int sstride, int Bmax, bool first, int warp, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    const int nblk = Kc / 16, k0 = warp * nblk / NCW, k1 = (warp + 1) * nblk / NCW;
+    /* accumulator sets: four with one n-tile, two with two (registers) */
+    constexpr int AS = NT == 1 ? 4 : 2;
+    for (int rb0 = 0; rb0 < nrows; rb0 += 16 * AS) {
+        const int nrb = min(AS, (nrows - rb0 + 15) / 16); /* warp-uniform: row blocks with rows */
+        if (nrb == 1)
+            mma_chains<NT, 1, AS>(tile, rb0, nrows, wpitch, act, apitch, batch, k0, k1, res, sstride, Bmax, first,
+                                  warp, g, t);
+        else if (AS == 4 && nrb == 2)
+            mma_chains<NT, 2, AS / 2>(tile, rb0, nrows, wpitch, act, apitch, batch, k0, k1, res, sstride, Bmax,
+                                      first, warp, g, t);
+        else
+            mma_chains<NT, AS, 1>(tile, rb0, nrows, wpitch, act, apitch, batch, k0, k1, res, sstride, Bmax, first,
+                                  warp, g, t);
+    }
+}
+
 template <int NB>
 __device__ void gemv_tile_mma(const uint8_t *tile, int nrows, int Kc, int wpitch, const uint8_t *act, int apitch,
                               int batch, float *res, int sstride, int Bmax, bool first, int warp, int lane) {
-    const int g = lane >> 2, t = lane & 3;
-    const int nblk = Kc / 16, k0 = warp * nblk / NCW, k1 = (warp + 1) * nblk / NCW;
-    const bool lo = g < batch, hi = NB > 8 && g + 8 < batch;
-    const uint8_t *x0 = act + (size_t)g * apitch + 8 * t;
-    const uint8_t *x1 = act + (size_t)(g + 8) * apitch + 8 * t;
-    for (int rb0 = 0; rb0 < nrows; rb0 += 32) {
-        const int nrb = min(4, (nrows - rb0 + 7) / 8); /* warp-uniform: row blocks with rows */
-        if (nrb == 1)
-            mma_chains<NB, 1, 4>(tile, rb0, nrows, wpitch, x0, x1, lo, hi, k0, k1, batch, res, sstride, Bmax, first,
-                                 warp, g, t);
-        else if (nrb == 2)
-            mma_chains<NB, 2, 2>(tile, rb0, nrows, wpitch, x0, x1, lo, hi, k0, k1, batch, res, sstride, Bmax, first,
-                                 warp, g, t);
-        else
-            mma_chains<NB, 4, 1>(tile, rb0, nrows, wpitch, x0, x1, lo, hi, k0, k1, batch, res, sstride, Bmax, first,
-                                 warp, g, t);
-    }
+    if (NB <= 8 || batch <= 8)
+        gemv_tile_mma_nt<1>(tile, nrows, Kc, wpitch, act, apitch, batch, res, sstride, Bmax, first, warp, lane);
+    else
+        gemv_tile_mma_nt<2>(tile, nrows, Kc, wpitch, act, apitch, batch, res, sstride, Bmax, first, warp, lane);
 }
 
 /* ------------------------------------------- batch-1 GEMV, activations in registers */
