@@ -77,13 +77,15 @@ amk_status amk_plan_mutate(amk_plan *plan, int32_t kind, uint64_t seed);
  * has finished, plus the hand-off latency; its tiles cannot finish before
  * the CTA's loader has streamed their bytes, in task order, at the CTA's
  * share of HBM and at most one ring ahead of what the consumers released.
- * consts: NULL for the built-in constants (fitted to GB300), or n_consts = 14
+ * consts: NULL for the built-in constants (fitted to GB300), or n_consts = 15
  * values in this order: [0] hand-off s, [1] RMSNorm prologue s, [2] copy
- * prologue s, [3] GEMV epilogue s, [4] bf16 consumer bytes/s per CTA, [5]
- * int8 consumer bytes/s per CTA, [6] HBM bytes/s, [7] attention prologue s,
- * [8] attention s per (position, head, element), [9] attention epilogue s,
- * [10] merge s, [11] s per ring stage, [12] s of prologue per further
- * sequence at batch > 1, [13] most bytes/s one CTA's loader pulls.
+ * prologue s, [3] GEMV epilogue s, [4] batch-1 bf16 consumer bytes/s per
+ * CTA, [5] int8 consumer bytes/s per CTA, [6] HBM bytes/s, [7] attention
+ * prologue s, [8] attention s per (position, head, element), [9] attention
+ * epilogue s, [10] merge s, [11] s per ring stage, [12] s of prologue per
+ * further sequence at batch > 1, [13] most bytes/s one CTA's loader pulls,
+ * [14] bf16 consumer bytes/s per CTA at batch > 1 (the tensor-core tile;
+ * half of it above batch 8).  Any other n_consts is AMK_ERR_INVALID_ARG.
  * Writes the step time in microseconds to *step_us. */
 amk_status amk_plan_simulate(const amk_plan *plan, const double *consts, int32_t n_consts, double *step_us);
 

@@ -193,7 +193,7 @@ class Plan:
 
     def simulate(self, consts: Optional[Sequence[float]] = None) -> float:
         """The task-level simulation's step time (µs) under the built-in cost
-        constants, or under `consts` (14 values; see amk_plan_simulate)."""
+        constants, or under `consts` (15 values; see amk_plan_simulate)."""
         out = f64()
         arr = None if consts is None else (f64 * len(consts))(*consts)
         _check(lib().amk_plan_simulate(self._p, arr, 0 if consts is None else len(consts), ctypes.byref(out)),

@@ -40,7 +40,7 @@ struct Knobs {
 };
 
 /* Constants of the task-level simulation (amk_plan_simulate); see amk_plan.h. */
-constexpr int COST_NCONST = 14;
+constexpr int COST_NCONST = 15;
 extern const double COST_DEFAULT[COST_NCONST];
 
 /* Model geometry seen by the planner. */

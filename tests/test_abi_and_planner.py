@@ -105,6 +105,31 @@ def test_headline_schedule_is_the_measured_best_point(amk):
     assert info["l2_evict_first"] == 1 and info["smem_bytes"] <= 232448
 
 
+def test_schedule_simulation_entry_point(amk):
+    # amk_plan_simulate takes exactly fifteen constants (or none, for the
+    # built-in fit) and its step time moves the way the model says: a slower
+    # hand-off, a slower HBM or a slower consumer never makes a step faster
+    wl = synth.workload("tinyllama_1b1")
+    plan = amk.Plan(_cfg(amk, wl), 1, 152)
+    base = [1.8e-6, 0.17e-6, 0.13e-6, 0.48e-6, 6.75e10, 2.63e10, 6.5e12, 1.5e-6, 6e-12, 0.27e-6, 1.5e-6,
+            0.23e-6, 0.38e-6, 1.67e11, 1.77e10]
+    t0 = plan.simulate(base)
+    assert t0 > 0 and abs(plan.simulate(base) - t0) == 0.0
+    assert abs(plan.simulate() - plan.info()["simulated_us"]) < 1e-6
+    with pytest.raises(Exception):
+        plan.simulate(base[:14])
+    for i, f in ((0, 2.0), (6, 0.5), (4, 0.5), (10, 2.0)):
+        c = list(base)
+        c[i] *= f
+        assert plan.simulate(c) > t0, i
+    # the batched consumer rate only matters above batch 1
+    c = list(base)
+    c[14] *= 0.5
+    assert plan.simulate(c) == t0
+    plan8 = amk.Plan(_cfg(amk, synth.workload("llama2_7b_b8")), 8, 152)
+    assert plan8.simulate(c) > plan8.simulate(base)
+
+
 def _coverage(wl, plan, B):
     d, nq, nkv = wl.head_dim, wl.n_heads, wl.n_kv_heads
     rows = {"QKV": (nq + 2 * nkv) * d, "OPR": wl.hidden, "GUP": wl.intermediate, "DWN": wl.hidden, "LMH": wl.vocab}
