@@ -200,10 +200,10 @@ constexpr int SMEM_MISC = 2048;
 
 /* At batch above 1, every weight row of a ring slot and every activation row
  * of the K slice sits in shared memory at a pitch of its bytes rounded up to
- * 128 plus 32: the rows that one tensor-core fragment load reads (four rows,
- * 32 bytes apart in K) then fall on distinct banks. */
+ * 128 plus 64: a tensor-core fragment load gives each row 64 consecutive
+ * bytes, and a quarter-warp's two rows then fall on distinct banks. */
 AMK_HD inline int smem_pitch(int row_bytes, int batch_max) {
-    return batch_max > 1 ? (row_bytes + 127) / 128 * 128 + 32 : row_bytes;
+    return batch_max > 1 ? (row_bytes + 127) / 128 * 128 + 64 : row_bytes;
 }
 
 AMK_HD inline int align_up(int x, int a) { return (x + a - 1) / a * a; }

@@ -963,24 +963,33 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
  * B (N = sequences; a second n-tile above batch 8), so every weight element
  * loaded feeds all sequences.  The sum over K is the same for any order of
  * K, so each k16 step pairs A and B through one permutation: thread t of a
- * fragment row supplies the four consecutive elements 4t .. 4t + 3 (one
- * 8-byte shared load) where the fragment layout names elements 2t, 2t + 1,
- * 2t + 8, 2t + 9.  Warp w takes K segment w of 8 for every row block of the
+ * fragment row supplies four consecutive elements where the fragment layout
+ * names 2t, 2t + 1, 2t + 8, 2t + 9, and one 16-byte shared load (elements
+ * 8t .. 8t + 7 of 32) serves two steps.  Warp w takes K segment w of 8 for every row block of the
  * stage.  A dependent chain of mmas waits out each one's latency, so the
  * warp keeps several independent accumulator sets (four with one n-tile, two
  * with two): NR row blocks times CH interleaved K chains (k16 step kb feeds
  * chain kb % CH), summed at the end.
  * res[(w * sstride + row) * Bmax + b] receives the warp's partial sums
  * (added over K-split passes). */
+__device__ __forceinline__ uint4 ld_shared16(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 ld_shared8(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+
 template <int NT, int NR, int CH>
-__device__ __forceinline__ void mma_chains(const uint8_t *tile, int rb0, int nrows, int wpitch, const uint8_t *act,
-                                           int apitch, int batch, int k0, int k1, float *res, int sstride, int Bmax,
-                                           bool first, int warp, int g, int t) {
+__device__ __forceinline__ void mma_chains(uint32_t tile, int rb0, int nrows, int wpitch, uint32_t act, int apitch,
+                                           int batch, int k0, int k1, float *res, int sstride, int Bmax, bool first,
+                                           int warp, int g, int t) {
     float acc[NR * CH][NT][4];
-    int wr[NR][2]; /* byte offsets into the tile and the activations */
-    bool rok[NR][2];
-    int xs[NT];
-    bool xok[NT];
+    uint32_t wr[NR][2], xs[NT]; /* shared addresses of this lane's row, at K step 0 */
+    bool rok[NR][2], xok[NT];
 #pragma unroll
     for (int a = 0; a < NR * CH; ++a)
 #pragma unroll
@@ -991,29 +1000,53 @@ __device__ __forceinline__ void mma_chains(const uint8_t *tile, int rb0, int nro
         for (int h = 0; h < 2; ++h) {
             const int row = rb0 + 16 * r + 8 * h + g;
             rok[r][h] = row < nrows;
-            wr[r][h] = row * wpitch + 8 * t;
+            wr[r][h] = tile + (uint32_t)(row * wpitch + 32 * k0 + 16 * t);
         }
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
         xok[n] = 8 * n + g < batch;
-        xs[n] = (8 * n + g) * apitch + 8 * t;
+        xs[n] = act + (uint32_t)((8 * n + g) * apitch + 32 * k0 + 16 * t);
     }
-    for (int kb = k0; kb < k1; kb += CH) {
+    /* pairs of k16 steps: a lane's 16 bytes are elements 8t .. 8t + 7 of 32,
+     * the first four for the first step, the last four for the second; CH
+     * pairs feed CH independent chains, all loads before the first mma */
+    const int np = (k1 - k0) / 2;
+    for (int p0 = 0; p0 < np; p0 += CH) {
+        uint4 bx[CH][NT], w0[CH][NR], w1[CH][NR];
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
-            if (kb + c >= k1) break; /* warp-uniform */
-            const int ko = 32 * (kb + c);
-            uint2 bx[NT];
+            const bool in = p0 + c < np;
+            const uint32_t o = 64u * (uint32_t)(p0 + c);
 #pragma unroll
-            for (int n = 0; n < NT; ++n)
-                bx[n] = xok[n] ? *reinterpret_cast<const uint2 *>(act + xs[n] + ko) : make_uint2(0u, 0u);
+            for (int n = 0; n < NT; ++n) bx[c][n] = in && xok[n] ? ld_shared16(xs[n] + o) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
-                const uint2 w0 = rok[r][0] ? *reinterpret_cast<const uint2 *>(tile + wr[r][0] + ko) : make_uint2(0u, 0u);
-                const uint2 w1 = rok[r][1] ? *reinterpret_cast<const uint2 *>(tile + wr[r][1] + ko) : make_uint2(0u, 0u);
+                w0[c][r] = in && rok[r][0] ? ld_shared16(wr[r][0] + o) : make_uint4(0u, 0u, 0u, 0u);
+                w1[c][r] = in && rok[r][1] ? ld_shared16(wr[r][1] + o) : make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
 #pragma unroll
-                for (int n = 0; n < NT; ++n)
-                    mma_bf16_16816(acc[r * CH + c][n], w0.x, w1.x, w0.y, w1.y, bx[n].x, bx[n].y);
+        for (int c = 0; c < CH; ++c)
+#pragma unroll
+            for (int r = 0; r < NR; ++r)
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    mma_bf16_16816(acc[r * CH + c][n], w0[c][r].x, w1[c][r].x, w0[c][r].y, w1[c][r].y, bx[c][n].x,
+                                   bx[c][n].y);
+                    mma_bf16_16816(acc[r * CH + c][n], w0[c][r].z, w1[c][r].z, w0[c][r].w, w1[c][r].w, bx[c][n].z,
+                                   bx[c][n].w);
+                }
+    }
+    if ((k1 - k0) & 1) { /* the last step alone: 8 bytes per lane, elements 4t .. 4t + 3 */
+        const uint32_t o = 64u * (uint32_t)np;
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            const uint2 a0 = rok[r][0] ? ld_shared8(wr[r][0] + o - 8u * t) : make_uint2(0u, 0u);
+            const uint2 a1 = rok[r][1] ? ld_shared8(wr[r][1] + o - 8u * t) : make_uint2(0u, 0u);
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const uint2 b = xok[n] ? ld_shared8(xs[n] + o - 8u * t) : make_uint2(0u, 0u);
+                mma_bf16_16816(acc[r * CH][n], a0.x, a1.x, a0.y, a1.y, b.x, b.y);
             }
         }
     }
@@ -1036,9 +1069,11 @@ __device__ __forceinline__ void mma_chains(const uint8_t *tile, int rb0, int nro
 }
 
 template <int NT>
-__device__ void gemv_tile_mma_nt(const uint8_t *tile, int nrows, int Kc, int wpitch, const uint8_t *act, int apitch,
-                                 int batch, float *res, int sstride, int Bmax, bool first, int warp, int lane) {
+__device__ void gemv_tile_mma_nt(const uint8_t *tile_p, int nrows, int Kc, int wpitch, const uint8_t *act_p,
+                                 int apitch, int batch, float *res, int sstride, int Bmax, bool first, int warp,
+                                 int lane) {
     const int g = lane >> 2, t = lane & 3;
+    const uint32_t tile = smem_addr(tile_p), act = smem_addr(act_p);
     const int nblk = Kc / 16, k0 = warp * nblk / NCW, k1 = (warp + 1) * nblk / NCW;
     /* accumulator sets: four with one n-tile, two with two (registers) */
     constexpr int AS = NT == 1 ? 4 : 2;
