@@ -28,8 +28,11 @@ POINTS = [
     ("llama2_7b", 1, {}), ("llama2_7b", 1, {"task_order": 1}), ("llama2_7b", 1, {"att_chunks": 8}),
     ("llama2_7b_b8", 8, {"att_chunks": 4}), ("llama2_7b_b8", 8, {"att_chunks": 7}),
     ("llama2_7b_b8", 8, {"att_chunks": 8}),
-    ("tinyllama_1b1_short", 1, {}), ("tinyllama_1b1_short", 2, {}), ("tinyllama_1b1_short", 4, {}),
-    ("tinyllama_1b1_short", 8, {}), ("tinyllama_1b1_short", 16, {}),
+    ("tinyllama_1b1_short", 1, {}), ("tinyllama_1b1_short", 2, {"slot_bytes": 49152, "n_slots": 3}),
+    ("tinyllama_1b1_short", 2, {"slot_bytes": 61440, "n_slots": 3}), ("tinyllama_1b1_short", 4, {}),
+    ("tinyllama_1b1_short", 8, {"slot_bytes": 49152, "n_slots": 2}),
+    ("tinyllama_1b1_short", 8, {"slot_bytes": 61440, "n_slots": 2}), ("tinyllama_1b1_short", 16, {}),
+    ("smollm2_135m", 1, {"slot_bytes": 40960, "n_slots": 5}),
 ]
 
 FIRST_GUESS = [1.5e-6, 0.5e-6, 0.4e-6, 0.6e-6, 7.5e10, 5.0e10, 6.5e12, 0.5e-6, 2.0e-12, 0.8e-6, 0.5e-6, 0.1e-6,

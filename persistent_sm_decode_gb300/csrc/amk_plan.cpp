@@ -483,29 +483,30 @@ struct Builder {
 namespace amk {
 
 /* Fitted to GB300 step times by least squares on the log of the ratio, each
- * constant held within a factor of three of a physical first guess: 23
+ * constant held within a factor of three of a physical first guess: 25
  * measured schedules (TinyLlama bf16 under seven schedule options, W8A16,
- * SmolLM2 under two ring shapes, Llama-2-7B at batch 1 and at batch 8 under
- * three chunk counts, the TinyLlama short shape at batch 1..16).  Every
- * fitted point lands within 11 % of its measurement; fitted without its own
- * workload, a point lands within 15 %, except SmolLM2 (+22 %), W8A16 (-28 %)
- * and batch 16 (+34 %). */
+ * SmolLM2 under three ring shapes, Llama-2-7B at batch 1 and at batch 8
+ * under three chunk counts, the TinyLlama short shape at batch 1..16 under
+ * two ring shapes).  Batch-1 points land within 2 % of their measurement,
+ * batched ones within 13 %; fitted without its own workload, a point lands
+ * within 20 %, except W8A16 (-32 %), short batch 2 (+28 %) and batch 16
+ * (+41 %), whose constants only they inform. */
 const double COST_DEFAULT[COST_NCONST] = {
-    1.83e-6,  /* [0]  hand-off: producer's last store -> consumer sees every word */
-    0.17e-6,  /* [1]  RMSNorm prologue of one sequence (batch 1: one pass) */
-    0.13e-6,  /* [2]  copy prologue of one sequence (attention or SwiGLU output) */
-    0.48e-6,  /* [3]  GEMV epilogue (segment sums, residual, stores, barrier) */
-    6.75e10,  /* [4]  batch-1 consumer rate, bf16 weight bytes per second per CTA */
-    2.63e10,  /* [5]  consumer rate, int8 weight bytes per second per CTA */
+    1.73e-6,  /* [0]  hand-off: producer's last store -> consumer sees every word */
+    0.166e-6, /* [1]  RMSNorm prologue of one sequence (batch 1: one pass) */
+    0.133e-6, /* [2]  copy prologue of one sequence (attention or SwiGLU output) */
+    0.211e-6, /* [3]  GEMV epilogue (segment sums, residual, stores, barrier) */
+    6.87e10,  /* [4]  batch-1 consumer rate, bf16 weight bytes per second per CTA */
+    2.67e10,  /* [5]  consumer rate, int8 weight bytes per second per CTA */
     6.5e12,   /* [6]  HBM bytes per second, shared by the CTAs that stream (measured copy rate, not fitted) */
     1.5e-6,   /* [7]  attention prologue (q, k, v of the group; RoPE) */
-    6.0e-12,  /* [8]  attention, per (position, head of the group, head element) */
-    0.27e-6,  /* [9]  attention epilogue (warp merge, partials) */
+    6.01e-12, /* [8]  attention, per (position, head of the group, head element) */
+    1.93e-6,  /* [9]  attention epilogue (warp merge, partials) */
     1.5e-6,   /* [10] merge task */
-    0.23e-6,  /* [11] per ring stage (slot wait, release) */
-    0.38e-6,  /* [12] extra prologue per further sequence at batch > 1 */
-    1.67e11,  /* [13] most bytes per second one CTA's loader can pull */
-    1.77e10,  /* [14] batch > 1 tensor-core consumer rate, bf16 weight bytes per second per CTA (halved above batch 8) */
+    0.247e-6, /* [11] per ring stage (slot wait, release) */
+    0.49e-6,  /* [12] extra prologue per further sequence at batch > 1 */
+    3.55e11,  /* [13] most bytes per second one CTA's loader can pull */
+    2.34e10,  /* [14] batch > 1 tensor-core consumer rate, bf16 weight bytes per second per CTA (halved above batch 8) */
 };
 
 /* Task-level simulation of one step.  Every CTA's consumers run its tasks in
@@ -754,7 +755,7 @@ amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_c
      *    the task-level simulation of the whole step (plan_simulate), which
      *    sees placement, ring depth and the dependency structure;
      * 3. the winner is validated. */
-    const int slot_choices[] = {8192, 12288, 16384, 24576, 32768, 49152, 65536};
+    const int slot_choices[] = {8192, 12288, 16384, 24576, 32768, 40960, 49152, 57344, 61440, 65536};
     const int ks_choices[] = {1, 2, 4};
     std::vector<std::pair<double, Knobs>> pts;
     int cands = 0;
