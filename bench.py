@@ -527,7 +527,9 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
     import synth
-    wl = synth.workload(args.workload)
+    # 'name@B' runs the workload at batch B (the batch sweep's shapes)
+    name, _, bs = args.workload.partition("@")
+    wl = synth.workload(name, **({"batch": int(bs)} if bs else {}))
 
     if args.impl == "reference":
         return reference_arm(args, wl, rank, world)
