@@ -805,7 +805,7 @@ amk_status plan_build(const amk_config *cfg, int batch, int n_sm, int smem_per_c
     }
     std::stable_sort(pts.begin(), pts.end(),
                      [](const std::pair<double, Knobs> &a, const std::pair<double, Knobs> &b) { return a.first < b.first; });
-    constexpr int SIM_TOP = 6;
+    constexpr int SIM_TOP = 12;
     amk_plan *P = nullptr;
     double best_sim = 1e300;
     int simulated = 0;
