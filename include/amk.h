@@ -142,8 +142,8 @@ typedef struct amk_handle amk_handle;
 
 /* Builds, validates and uploads the schedule; copies the weight pointers.
  * options may be NULL.  On success *out owns device memory for the task
- * table, dependency counters, RoPE table and activation scratch (released
- * by amk_destroy).  Errors: INVALID_ARG (NULL/misaligned/inconsistent),
+ * table, the epoch and error words, the RoPE table and the activation
+ * scratch (released by amk_destroy).  Errors: INVALID_ARG (NULL/misaligned/inconsistent),
  * UNSUPPORTED (shape or device), SCHEDULE (validator), COOPERATIVE, CUDA, OOM. */
 amk_status amk_create(const amk_config *config, const amk_weights *weights,
                       const amk_schedule_options *options, amk_handle **out);
@@ -217,7 +217,9 @@ amk_status amk_decode_step_noalloc(const amk_config *config, const amk_weights *
 
 /* Synchronises the stream of the last step and reads the device error word.
  * Returns AMK_ERR_TIMEOUT if any wait of any step since the last call gave up
- * (then the handle's counters are reset, so the next step runs normally). */
+ * (then the error word is cleared, so the next step runs normally: the
+ * failed step still advanced the device epoch, so none of its words can pass
+ * for the next step's). */
 amk_status amk_sync_status(amk_handle *h);
 
 /* Frees everything the handle owns (synchronises first).  NULL is accepted. */
@@ -243,7 +245,10 @@ amk_status amk_last_error(const amk_handle *h, amk_error_info *info);
 
 /* Summary of the solidified schedule of a handle or a plan. */
 typedef struct amk_plan_info {
-    int32_t n_sm, n_tasks, n_counters, n_levels;
+    int32_t n_sm, n_tasks;
+    int32_t n_counters;       /* dependency ids of the schedule graph (what the validator checks; the
+                                 kernel keeps no counters: it polls epoch-tagged words) */
+    int32_t n_levels;
     int32_t att_chunks, slot_bytes, n_slots, ksplit, scratch_depth, att_tile;
     int32_t smem_bytes;       /* dynamic shared memory per CTA */
     int32_t max_tasks_per_sm;
