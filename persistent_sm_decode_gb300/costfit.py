@@ -82,23 +82,32 @@ def _constants(x: Sequence[float]) -> List[float]:
     return c
 
 
-def fit(path: str, bound: float = 1.1) -> List[float]:
-    import numpy as np
-    from scipy.optimize import least_squares
+def _plans(recs, n_sm: int = 152):
     import synth
     import persistent_sm_decode_gb300 as amk
-    recs = [json.loads(ln) for ln in open(path) if ln.strip()]
     plans = []
     for r in recs:
         wl = synth.workload(r["workload"], batch=r["batch"])
         opts = {k: r["plan"][k] for k in KNOBS}
-        plans.append((amk.Plan(_config(amk, wl, r["batch"]), r["batch"], 152, options=opts), r["us"], r))
+        plans.append((amk.Plan(_config(amk, wl, r["batch"]), r["batch"], n_sm, options=opts), r["us"], r))
+    return plans
 
-    def solve(sel):
-        res = lambda x: [np.log(plans[i][0].simulate(_constants(x)) / plans[i][1]) for i in sel]
-        return least_squares(res, np.zeros(len(FITTED)), bounds=(-bound, bound), diff_step=0.05).x
 
-    c = _constants(solve(range(len(plans))))
+def fit_constants(plans, sel, bound: float = 1.1) -> List[float]:
+    """The fitted constants for the points `sel` of `plans` [(plan, measured
+    µs, record)]."""
+    import numpy as np
+    from scipy.optimize import least_squares
+    res = lambda x: [np.log(plans[i][0].simulate(_constants(x)) / plans[i][1]) for i in sel]
+    return _constants(least_squares(res, np.zeros(len(FITTED)), bounds=(-bound, bound), diff_step=0.05).x)
+
+
+def fit(path: str, bound: float = 1.1) -> List[float]:
+    recs = [json.loads(ln) for ln in open(path) if ln.strip()]
+    plans = _plans(recs)
+    solve = lambda sel: fit_constants(plans, sel, bound)
+
+    c = solve(range(len(plans)))
     print("constants:", ", ".join("%.3g" % v for v in c))
     print("| workload | batch | options | measured µs | simulated µs | error |")
     print("|---|---|---|---|---|---|")
@@ -112,7 +121,7 @@ def fit(path: str, bound: float = 1.1) -> List[float]:
     for key in sorted({(r["workload"], r["batch"]) for _, _, r in plans}):
         train = [i for i, (_, _, r) in enumerate(plans) if (r["workload"], r["batch"]) != key]
         test = [i for i, (_, _, r) in enumerate(plans) if (r["workload"], r["batch"]) == key]
-        cx = _constants(solve(train))
+        cx = solve(train)
         print("| %s | %d | %s |" % (key[0], key[1], " ".join("%+.1f %%" % (100 * (plans[i][0].simulate(cx) /
                                                                                  plans[i][1] - 1)) for i in test)))
     return c

@@ -1,0 +1,42 @@
+"""The measure-and-fit loop of the schedule simulation, pinned on the host:
+step times made by the simulation itself under known constants must be
+reproduced by the constants the fit recovers from them (the fit's residual
+is the log ratio of simulated to measured time, so a wrong sign, a dropped
+point or a mixed-up constant index shows up as a residual far from zero)."""
+import math
+
+import pytest
+
+import synth
+
+
+@pytest.fixture(scope="module")
+def amk():
+    import persistent_sm_decode_gb300 as m
+    m.build()
+    return m
+
+
+def test_fit_recovers_step_times_made_by_known_constants(amk):
+    from persistent_sm_decode_gb300 import costfit
+    # a point of the search space per record: two tiny shapes, three schedules each, on few CTAs
+    truth = list(costfit.FIRST_GUESS)
+    truth[0] *= 1.6   # hand-off
+    truth[4] *= 0.7   # batch-1 consumer rate
+    truth[10] *= 1.4  # merge
+    recs = []
+    for B, opts in ((1, {"att_chunks": 2, "slot_bytes": 8192, "n_slots": 8, "ksplit": 1, "task_order": 1}),
+                    (1, {"att_chunks": 4, "slot_bytes": 16384, "n_slots": 4, "ksplit": 1, "task_order": 1}),
+                    (1, {"att_chunks": 1, "slot_bytes": 12288, "n_slots": 6, "ksplit": 1, "task_order": 2}),
+                    (2, {"att_chunks": 2, "slot_bytes": 16384, "n_slots": 4, "ksplit": 1, "task_order": 1})):
+        wl = synth.workload("tiny", batch=B)
+        plan = amk.Plan(costfit._config(amk, wl, B), B, 16, options=opts)
+        info = plan.info()
+        knobs = {k: info[k] for k in costfit.KNOBS}
+        recs.append({"workload": "tiny", "batch": B, "opts": opts, "us": plan.simulate(truth), "plan": knobs})
+    plans = costfit._plans(recs, n_sm=16)
+    fitted = costfit.fit_constants(plans, range(len(plans)), bound=1.1)
+    for p, us, _ in plans:
+        assert abs(math.log(p.simulate(fitted) / us)) < 0.02
+    # and the untouched guess does not reproduce them: the test can fail
+    assert max(abs(math.log(p.simulate(costfit.FIRST_GUESS) / us)) for p, us, _ in plans) > 0.05
