@@ -7,9 +7,13 @@
  * to kernel launches and puts inter-operator HBM round trips among the costs
  * the MegaKernel removes; the AutoMegaKernel abstract compares its fused
  * kernel against CUDA-graphed per-operator library kernels.  This file is
- * that per-operator form, written plainly: every operator of the step is its
- * own launch and hands its output to the next one through global memory.
- * Callers capture a step in a CUDA graph to take the host's launch cost out.
+ * that per-operator form: every operator of the step is its own launch and
+ * hands its output to the next one through global memory.  Each launch is
+ * written to keep HBM busy on its own (GEMV rows with several loads in
+ * flight per lane, attention split over the context into about two blocks
+ * per SM and merged by a second launch), so the comparison measures the
+ * launches and round trips rather than slow kernels.  Callers capture a step
+ * in a CUDA graph to take the host's launch cost out.
  *
  * Arithmetic follows the same definition as the MegaKernel (bf16 weights or
  * int8 weights with row scales, bf16 activations at the GEMV inputs and in
@@ -65,15 +69,29 @@ __global__ void k_embed(float *x, const uint16_t *embed, const int32_t *tokens, 
     for (int i = threadIdx.x; i < H; i += blockDim.x) x[(size_t)b * H + i] = bf2f(e[i]);
 }
 
-/* h[b] = bf16(x[b] * gain / sqrt(mean(x[b]^2) + eps)) */
+/* h[b] = bf16(x[b] * gain / sqrt(mean(x[b]^2) + eps)); groups of four, the
+ * loop unrolled so that a thread's loads are in flight together */
 __global__ void k_rmsnorm(uint16_t *h, const float *x, const uint16_t *gain, int H, float eps) {
     __shared__ float sh[32];
-    const int b = blockIdx.x;
-    const float *xb = x + (size_t)b * H;
+    const int b = blockIdx.x, H4 = H / 4;
+    const float4 *xb = reinterpret_cast<const float4 *>(x + (size_t)b * H);
     float ss = 0.f;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) ss += xb[i] * xb[i];
+#pragma unroll 4
+    for (int i = threadIdx.x; i < H4; i += blockDim.x) {
+        const float4 v = xb[i];
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
     const float r = rsqrtf(block_sum(ss, sh) / (float)H + eps);
-    for (int i = threadIdx.x; i < H; i += blockDim.x) h[(size_t)b * H + i] = f2bf(xb[i] * r * bf2f(gain[i]));
+#pragma unroll 4
+    for (int i = threadIdx.x; i < H4; i += blockDim.x) {
+        const float4 v = xb[i];
+        const uint2 gw = reinterpret_cast<const uint2 *>(gain)[i];
+        const float g0 = bf2f((uint16_t)gw.x), g1 = bf2f((uint16_t)(gw.x >> 16));
+        const float g2 = bf2f((uint16_t)gw.y), g3 = bf2f((uint16_t)(gw.y >> 16));
+        reinterpret_cast<uint2 *>(h + (size_t)b * H)[i] =
+            make_uint2((uint32_t)f2bf(v.x * r * g0) | ((uint32_t)f2bf(v.y * r * g1) << 16),
+                       (uint32_t)f2bf(v.z * r * g2) | ((uint32_t)f2bf(v.w * r * g3) << 16));
+    }
 }
 
 /* y[b][row0 + r] = (s[r]) * sum_k W[r][k] h[b][k] for up to three matrices
@@ -101,6 +119,7 @@ __global__ void k_gemv(float *y, int ystride, Mats m, const uint16_t *h, int K, 
     for (int b = 0; b < MB; ++b) acc[b] = 0.f;
     if (I8) {
         const int8_t *w = (const int8_t *)m.w[mi] + (size_t)r * K;
+#pragma unroll 4
         for (int k = lane * 4; k < K; k += 128) {
             const char4 q = *reinterpret_cast<const char4 *>(w + k);
             for (int b = 0; b < B && b < MB; ++b) {
@@ -110,16 +129,29 @@ __global__ void k_gemv(float *y, int ystride, Mats m, const uint16_t *h, int K, 
             }
         }
     } else {
+        /* eight 16-byte weight loads per lane in flight before any product */
+        constexpr int U = 8;
         const uint16_t *w = (const uint16_t *)m.w[mi] + (size_t)r * K;
-        for (int k = lane * 8; k < K; k += 256) {
-            const uint4 wv = *reinterpret_cast<const uint4 *>(w + k);
-            const uint16_t *wp = reinterpret_cast<const uint16_t *>(&wv);
-            for (int b = 0; b < B && b < MB; ++b) {
-                const uint4 hv = *reinterpret_cast<const uint4 *>(h + (size_t)b * K + k);
-                const uint16_t *hp = reinterpret_cast<const uint16_t *>(&hv);
-                float a = 0.f;
-                for (int e = 0; e < 8; ++e) a = fmaf(bf2f(wp[e]), bf2f(hp[e]), a);
-                acc[b] += a;
+        for (int k0 = lane * 8; k0 < K; k0 += 256 * U) {
+            uint4 wv[U];
+#pragma unroll
+            for (int u2 = 0; u2 < U; ++u2) {
+                const int k = k0 + 256 * u2;
+                wv[u2] = k < K ? *reinterpret_cast<const uint4 *>(w + k) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u2 = 0; u2 < U; ++u2) {
+                const int k = k0 + 256 * u2;
+                if (k >= K) break;
+                const uint16_t *wp = reinterpret_cast<const uint16_t *>(&wv[u2]);
+                for (int b = 0; b < B && b < MB; ++b) {
+                    const uint4 hv = *reinterpret_cast<const uint4 *>(h + (size_t)b * K + k);
+                    const uint16_t *hp = reinterpret_cast<const uint16_t *>(&hv);
+                    float a = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) a = fmaf(bf2f(wp[e]), bf2f(hp[e]), a);
+                    acc[b] += a;
+                }
             }
         }
     }
@@ -153,56 +185,103 @@ __global__ void k_rope_kv(float *qkv, int qkv_rows, uint16_t *kc, uint16_t *vc, 
     }
 }
 
-/* softmax(q K^T / sqrt(d)) V over positions 0..p of one (sequence, query
- * head); the scores sit in shared memory.  Scores: 8 lanes per position, each
- * a 16-byte piece of the K row; P.V: (256 / d) thread groups split the
- * positions, each thread one output element, the groups' sums added in order. */
-__global__ void k_attention(uint16_t *out, const float *qkv, int qkv_rows, const uint16_t *kc, const uint16_t *vc,
-                            const int32_t *positions, int l, int Bmax, int nq, int nkv, int d, int Smax) {
+/* Split-context attention of one (query head, split, sequence): over
+ * positions [m0, m1) of 0..p (split sp of S), the softmax partial m = max
+ * score, l = sum exp(s - m), o = sum exp(s - m) v (unnormalised) into
+ * part[((b nq + j) S + sp) (d + 2)].  Scores: 8 lanes per position, each a
+ * 16-byte piece of the K row, kept in shared memory; P.V: (256 / d) thread
+ * groups split the positions, each thread one output element, the groups'
+ * sums added in order. */
+__global__ void k_attn_split(float *part, const float *qkv, int qkv_rows, const uint16_t *kc, const uint16_t *vc,
+                             const int32_t *positions, int l, int Bmax, int nq, int nkv, int d, int Smax, int S) {
     extern __shared__ float sc[];
     __shared__ float sh[32];
-    __shared__ float part[TB];
-    const int j = blockIdx.x, b = blockIdx.y, g = j / (nq / nkv), p = positions[b];
+    __shared__ float pp[TB];
+    const int j = blockIdx.x, sp = blockIdx.y, b = blockIdx.z, g = j / (nq / nkv), n = positions[b] + 1;
+    const int m0 = (int)((long long)sp * n / S), m1 = (int)((long long)(sp + 1) * n / S);
+    float *out = part + ((size_t)(b * nq + j) * S + sp) * (d + 2);
     const float *q = qkv + (size_t)b * qkv_rows + (size_t)j * d;
     const size_t base = (((size_t)l * Bmax + b) * nkv + g) * Smax * d;
     const float scale = rsqrtf((float)d);
     const int lane = threadIdx.x & 31, sub = lane & 7, grp = threadIdx.x >> 3, ngrp = blockDim.x >> 3;
     float mx = -INFINITY;
-    for (int m0 = 0; m0 <= p; m0 += ngrp) {
-        const int m = m0 + grp;
+    for (int a0 = m0; a0 < m1; a0 += ngrp) {
+        const int m = a0 + grp;
         float s = 0.f;
-        if (m <= p)
+        if (m < m1)
             for (int e0 = sub * 8; e0 < d; e0 += 64) {
                 const uint4 kv = *reinterpret_cast<const uint4 *>(kc + base + (size_t)m * d + e0);
                 const uint16_t *kp = reinterpret_cast<const uint16_t *>(&kv);
                 for (int e = 0; e < 8; ++e) s = fmaf(q[e0 + e], bf2f(kp[e]), s);
             }
         for (int o = 4; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (m <= p) {
+        if (m < m1) {
             s *= scale;
-            if (sub == 0) sc[m] = s;
+            if (sub == 0) sc[m - m0] = s;
             mx = fmaxf(mx, s);
         }
     }
     mx = block_max(mx, sh);
     float sum = 0.f;
-    for (int m = threadIdx.x; m <= p; m += blockDim.x) {
-        const float e = __expf(sc[m] - mx);
-        sc[m] = e;
+    for (int m = m0 + threadIdx.x; m < m1; m += blockDim.x) {
+        const float e = __expf(sc[m - m0] - mx);
+        sc[m - m0] = e;
         sum += e;
     }
     sum = block_sum(sum, sh);
     __syncthreads();
     const int e = threadIdx.x % d, gi = threadIdx.x / d, ng = blockDim.x / d;
     float o = 0.f;
-    for (int m = gi; m <= p; m += ng) o = fmaf(sc[m], bf2f(vc[base + (size_t)m * d + e]), o);
-    part[threadIdx.x] = o;
+    for (int m = m0 + gi; m < m1; m += ng) o = fmaf(sc[m - m0], bf2f(vc[base + (size_t)m * d + e]), o);
+    pp[threadIdx.x] = o;
     __syncthreads();
     if (threadIdx.x < d) {
         float t = 0.f;
-        for (int i2 = 0; i2 < ng; ++i2) t += part[i2 * d + threadIdx.x];
-        out[(size_t)b * nq * d + (size_t)j * d + threadIdx.x] = f2bf(t / sum);
+        for (int i2 = 0; i2 < ng; ++i2) t += pp[i2 * d + threadIdx.x];
+        out[threadIdx.x] = t;
     }
+    if (threadIdx.x == 0) {
+        out[d] = mx;
+        out[d + 1] = sum;
+    }
+}
+
+/* out[b][j] = bf16(sum_s 2^... ) : the S partials of one (query head,
+ * sequence) combined by their log-sum-exp weights: o = sum_s e^(m_s - M) o_s /
+ * sum_s e^(m_s - M) l_s; one thread per output element */
+__global__ void k_attn_merge(uint16_t *out, const float *part, int nq, int d, int S) {
+    const int j = blockIdx.x, b = blockIdx.y, e = threadIdx.x;
+    if (e >= d) return;
+    const float *pj = part + (size_t)(b * nq + j) * S * (d + 2);
+    float M = -INFINITY, L = 0.f, O = 0.f;
+    /* rounds of eight splits, every load of a round in flight together */
+    for (int s0 = 0; s0 < S; s0 += 8) {
+        float mv[8], lv[8], ov[8];
+#pragma unroll
+        for (int u2 = 0; u2 < 8; ++u2) {
+            const bool in = s0 + u2 < S;
+            const float *q = pj + (size_t)(s0 + u2) * (d + 2);
+            mv[u2] = in ? q[d] : -INFINITY;
+            lv[u2] = in ? q[d + 1] : 0.f;
+            ov[u2] = in ? q[e] : 0.f;
+        }
+        float Mn = M;
+#pragma unroll
+        for (int u2 = 0; u2 < 8; ++u2) Mn = fmaxf(Mn, mv[u2]);
+        if (Mn == -INFINITY) continue;
+        const float c = M == -INFINITY ? 0.f : __expf(M - Mn);
+        L *= c;
+        O *= c;
+#pragma unroll
+        for (int u2 = 0; u2 < 8; ++u2) {
+            if (mv[u2] == -INFINITY) continue;
+            const float f = __expf(mv[u2] - Mn);
+            L = fmaf(f, lv[u2], L);
+            O = fmaf(f, ov[u2], O);
+        }
+        M = Mn;
+    }
+    out[(size_t)b * nq * d + (size_t)j * d + e] = f2bf(O / L);
 }
 
 __global__ void k_residual(float *x, const float *y, int n) {
@@ -228,7 +307,8 @@ struct amk_unfused {
     std::vector<amk_layer_weights> layers;
     const void *embed, *final_norm, *lm;
     const float *s_lm;
-    float *x = nullptr, *y = nullptr, *qkv = nullptr, *gu = nullptr, *rope = nullptr;
+    float *x = nullptr, *y = nullptr, *qkv = nullptr, *gu = nullptr, *rope = nullptr, *part = nullptr;
+    int splits = 1; /* context splits of the attention: about two blocks per SM at batch 1 */
     uint16_t *h = nullptr; /* the bf16 input of the next GEMV: norm, attention or SwiGLU output */
 };
 
@@ -267,6 +347,11 @@ amk_status amk_unfused_create(const amk_config *c, const amk_weights *w, amk_unf
     chk(cudaMalloc(&u->gu, sizeof(float) * B * 2 * I));
     chk(cudaMalloc(&u->rope, sizeof(float) * rope.size()));
     chk(cudaMalloc(&u->h, sizeof(uint16_t) * B * KM));
+    int dev = 0, n_sm = 0;
+    chk(cudaGetDevice(&dev));
+    chk(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
+    u->splits = std::max(1, std::min(32, ceil_div(2 * std::max(1, n_sm), c->n_heads)));
+    chk(cudaMalloc(&u->part, sizeof(float) * B * c->n_heads * u->splits * (d + 2)));
     if (e == cudaSuccess) chk(cudaMemcpy(u->rope, rope.data(), sizeof(float) * rope.size(), cudaMemcpyHostToDevice));
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -303,8 +388,10 @@ amk_status amk_unfused_decode_step(amk_unfused *u, int32_t batch, const int32_t 
         gemv(u->qkv, qkv_rows, Mats{{L.wq, L.wk, L.wv}, {L.s_q, L.s_k, L.s_v}, {nq * d, nkv * d, nkv * d}, 3}, H, i8);
         k_rope_kv<<<B, TB, 0, s>>>(u->qkv, qkv_rows, kc, vc, positions, u->rope, l, c.max_batch, nq, nkv, d,
                                    c.max_seq);
-        k_attention<<<dim3(nq, B), TB, sizeof(float) * c.max_seq, s>>>(u->h, u->qkv, qkv_rows, kc, vc, positions,
-                                                                      l, c.max_batch, nq, nkv, d, c.max_seq);
+        const int S = u->splits;
+        k_attn_split<<<dim3(nq, S, B), TB, sizeof(float) * (c.max_seq / S + 2), s>>>(
+            u->part, u->qkv, qkv_rows, kc, vc, positions, l, c.max_batch, nq, nkv, d, c.max_seq, S);
+        k_attn_merge<<<dim3(nq, B), d, 0, s>>>(u->h, u->part, nq, d, S);
         gemv(u->y, H, Mats{{L.wo}, {L.s_o}, {H}, 1}, nq * d, i8);
         k_residual<<<ceil_div(B * H, TB), TB, 0, s>>>(u->x, u->y, B * H);
         k_rmsnorm<<<B, TB, 0, s>>>(u->h, u->x, (const uint16_t *)L.mlp_norm, H, c.rms_eps);
@@ -327,6 +414,7 @@ amk_status amk_unfused_destroy(amk_unfused *u) {
     cudaFree(u->gu);
     cudaFree(u->rope);
     cudaFree(u->h);
+    cudaFree(u->part);
     delete u;
     return AMK_OK;
 }
