@@ -419,7 +419,7 @@ SUB_WORKLOADS = ("tinyllama_1b1_w8a16", "tinyllama_1b1_w4a16", "llama2_7b", "lla
                  "tinyllama_1b1_short@1", "tinyllama_1b1_short@2", "tinyllama_1b1_short@4",
                  "tinyllama_1b1_short@8", "tinyllama_1b1_short@16",
                  # the same step as one launch per operator, CUDA-graphed
-                 "unfused:tinyllama_1b1")
+                 "unfused:tinyllama_1b1", "unfused:llama2_7b")
 
 
 def unfused_record(amk, wl, steps, local):
