@@ -27,11 +27,17 @@
  *    {payload, epoch}, written with one 8-byte store, and a consumer polls
  *    the words it needs until they carry the current step's epoch.  One
  *    cross-SM round trip per dependency, no fences, no counters;
- *  - batch-1 GEMV: CUDA cores, each consumer warp keeps the activations of a
- *    fixed K segment in registers and streams 16-byte weight chunks from the
- *    ring with short independent FMA chains; fp32 accumulation;
- *  - attention: split-context flash decoding per (sequence, kv head) chunk
- *    with an online softmax in log2 units; MRG tasks merge the chunks;
+ *  - batch-1 GEMV (about 1 flop per weight byte): CUDA cores, each consumer
+ *    warp keeps the activations of a fixed K segment in registers and
+ *    streams 16-byte weight chunks (bf16, int8 or int4 codes) from the ring
+ *    into mixed-precision FMAs; fp32 accumulation;
+ *  - GEMV at batch 2..16: tensor cores (mma.sync m16n8k16, 16 weight rows as
+ *    A, the sequences as N), several independent accumulator chains per warp;
+ *  - attention: split-context flash decoding per (sequence, kv head) chunk on
+ *    the tensor cores (bf16 scores with q split in two, tf32 P.V with P split
+ *    in two), online softmax in log2 units; MRG tasks merge the chunks;
+ *  - greedy steps: every LM-head task keeps its rows' best logit, one ARG
+ *    task reduces them to the next token and position;
  *  - every wait is bounded: on timeout the CTA records the error, stops,
  *    waits for its own bulk copies in flight and returns; later launches see
  *    the error word and do nothing until the host clears it.
