@@ -462,7 +462,7 @@ def unfused_record(amk, wl, steps, local):
         torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     u.close()
-    n_launch = 3 + 12 * wl.n_layers
+    n_launch = 3 + 13 * wl.n_layers
     return {"ms_per_step": ms, "us_per_token": 1e3 * ms / wl.batch, "tokens_per_s": wl.batch / (ms / 1e3),
             "steps": steps, "launches_per_step": n_launch, "clocks": clocks.summary(), "config": config_block(wl),
             "data": "synthetic, weights and KV filled on the device by torch's seeded generator",
