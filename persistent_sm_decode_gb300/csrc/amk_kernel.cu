@@ -1183,18 +1183,46 @@ __device__ __forceinline__ void acc_chunk(float &s0, float &s1, const uint4 &w, 
     fma_bf16_lo(s0, w.w, h.w[3]);
     fma_bf16_hi(s1, w.w, h.w[3]);
 }
-__device__ __forceinline__ void acc_chunk_i8(float &s0, float &s1, const uint4 &w, const float (&hf)[16]) {
+/* fp16 pairs and the mixed-precision FMA with fp16 operands */
+__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ void fma_f16_lo(float &a, uint32_t w, uint32_t h) {
+    asm("{\n\t.reg .b16 w0, w1, h0, h1;\n\tmov.b32 {w0, w1}, %1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, w0, h0, %0;\n\t}"
+        : "+f"(a)
+        : "r"(w), "r"(h));
+}
+__device__ __forceinline__ void fma_f16_hi(float &a, uint32_t w, uint32_t h) {
+    asm("{\n\t.reg .b16 w0, w1, h0, h1;\n\tmov.b32 {w0, w1}, %1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, w1, h1, %0;\n\t}"
+        : "+f"(a)
+        : "r"(w), "r"(h));
+}
+/* bf16 pair -> fp16 pair (the activations of an int8 task, once per task):
+ * exact for magnitudes in [2^-14, 65504]; below that the fp16 subnormals keep
+ * multiples of 2^-24 */
+__device__ __forceinline__ uint32_t bf2_to_f16x2(uint32_t v) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(bf_hi(v)), "f"(bf_lo(v)));
+    return r;
+}
+/* int8 x fp16 activations: four codes b of one word become two fp16 pairs
+ * exactly, the byte b ^ 0x80 = b + 128 under the exponent of 1024 (fp16
+ * 1024 + b + 128) minus 1152; the products are exact in fp32 (11-bit by
+ * 11-bit significands) and accumulate in fp32 */
+__device__ __forceinline__ void acc_chunk_i8(float &s0, float &s1, const uint4 &w, const ActChunk<WF_I8> &h) {
     const uint32_t x[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        float f0 = __uint_as_float(__byte_perm(x[q], 0x4B000000u, 0x7540u));
-        float f1 = __uint_as_float(__byte_perm(x[q], 0x4B000000u, 0x7541u));
-        float f2 = __uint_as_float(__byte_perm(x[q], 0x4B000000u, 0x7542u));
-        float f3 = __uint_as_float(__byte_perm(x[q], 0x4B000000u, 0x7543u));
-        add_f32x2(f0, f1, -8388736.0f, -8388736.0f);
-        add_f32x2(f2, f3, -8388736.0f, -8388736.0f);
-        fma_f32x2(s0, s1, f0, f1, hf[4 * q], hf[4 * q + 1]);
-        fma_f32x2(s0, s1, f2, f3, hf[4 * q + 2], hf[4 * q + 3]);
+        const uint32_t p01 = sub_f16x2(__byte_perm(x[q], 0x64646464u, 0x4140u), 0x64806480u);
+        const uint32_t p23 = sub_f16x2(__byte_perm(x[q], 0x64646464u, 0x4342u), 0x64806480u);
+        fma_f16_lo(s0, p01, h.w[2 * q]);
+        fma_f16_hi(s1, p01, h.w[2 * q]);
+        fma_f16_lo(s0, p23, h.w[2 * q + 1]);
+        fma_f16_hi(s1, p23, h.w[2 * q + 1]);
     }
 }
 
@@ -1253,6 +1281,11 @@ __device__ __forceinline__ void act_regs(const uint8_t *act, int c0, int c1, Act
                 hv[j].w[4 * q + 1] = __byte_perm(v.z, v.w, 0x5410u); /* (h4, h6) */
                 hv[j].w[4 * q + 2] = __byte_perm(v.x, v.y, 0x7632u); /* (h1, h3) */
                 hv[j].w[4 * q + 3] = __byte_perm(v.z, v.w, 0x7632u); /* (h5, h7) */
+            } else if constexpr (WF == WF_I8) { /* fp16 pairs for acc_chunk_i8 */
+                hv[j].w[4 * q] = bf2_to_f16x2(v.x);
+                hv[j].w[4 * q + 1] = bf2_to_f16x2(v.y);
+                hv[j].w[4 * q + 2] = bf2_to_f16x2(v.z);
+                hv[j].w[4 * q + 3] = bf2_to_f16x2(v.w);
             } else {
                 hv[j].w[4 * q] = v.x;
                 hv[j].w[4 * q + 1] = v.y;
@@ -1295,14 +1328,8 @@ __device__ __forceinline__ void gemv_stage1(const uint8_t *tile, int nrows, int 
             for (int i = 0; i < RPG; ++i)
                 wv[i] = (r0 + i < nrows && c < c1) ? W[(size_t)(r0 + i) * rowc + c] : make_uint4(0u, 0u, 0u, 0u);
             if constexpr (WF == WF_I8) {
-                float hf[16];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    hf[2 * q] = bf_lo(hv[j].w[q]);
-                    hf[2 * q + 1] = bf_hi(hv[j].w[q]);
-                }
-#pragma unroll
-                for (int i = 0; i < RPG; ++i) acc_chunk_i8(a0[i], a1[i], wv[i], hf);
+                for (int i = 0; i < RPG; ++i) acc_chunk_i8(a0[i], a1[i], wv[i], hv[j]);
             } else if constexpr (WF == WF_I4) {
                 const int gi = (kbase + 32 * c) / group;
 #pragma unroll
