@@ -735,6 +735,9 @@ __device__ void norm_prologue(const Params &p, Smem &s, const uint64_t *xbase, b
             if (lane < p.batch) s.misc->red[lane][warp] = 0.f;
             __syncwarp();
             const int T = p.batch * H4;
+            /* group i = b * H4 + g: a thread's groups step by TS, so its
+             * sequence b advances without a division per group */
+            int b = ctid / H4, g = ctid - b * H4;
             for (int i0 = ctid; i0 < T; i0 += XB * TS) {
                 float4 x[XB];
                 load_x4s<XB>(p, s, xbase, nullptr, [=](int u) { return i0 + u * TS < T ? i0 + u * TS : -1; }, x, f,
@@ -745,7 +748,8 @@ __device__ void norm_prologue(const Params &p, Smem &s, const uint64_t *xbase, b
                     if (i - lane >= T) break; /* warp-uniform: the warp's groups are past the end */
                     float v = i < T ? x[u].x * x[u].x + x[u].y * x[u].y + x[u].z * x[u].z + x[u].w * x[u].w : 0.f;
                     v = warp_sum(v);
-                    if (lane == 0) s.misc->red[i / H4][warp] += v;
+                    if (lane == 0) s.misc->red[b][warp] += v;
+                    for (g += TS; g >= H4; g -= H4) ++b;
                 }
             }
             cbar();
@@ -757,25 +761,32 @@ __device__ void norm_prologue(const Params &p, Smem &s, const uint64_t *xbase, b
             }
             cbar();
         }
-        const int T = p.batch * n4;
+        /* item i = b * n4 + j: group j of sequence b's slice, (b, j) walked
+         * as in the first pass; gi holds the round's group indices in x */
+        const int T = p.batch * n4, ap2 = apitch / 8;
+        int b = ctid / n4, j = ctid - b * n4;
         for (int i0 = ctid; i0 < T; i0 += XB * TS) {
-            float4 x[XB];
-            load_x4s<XB>(p, s, xbase, nullptr, [=](int u) {
-                const int i = i0 + u * TS;
-                return i < T ? (i / n4) * H4 + a4 + i % n4 : -1;
-            }, x, f, task, which);
+            const int rb = b, rj = j;
+            int gi[XB];
 #pragma unroll
             for (int u = 0; u < XB; ++u) {
-                const int i = i0 + u * TS;
-                if (i < T) {
-                    const int b = i / n4, j = i % n4;
-                    const float r = s.misc->rnorm[b];
+                gi[u] = i0 + u * TS < T ? b * H4 + a4 + j : -1;
+                for (j += TS; j >= n4; j -= n4) ++b;
+            }
+            float4 x[XB];
+            load_x4s<XB>(p, s, xbase, nullptr, [=](int u) { return gi[u]; }, x, f, task, which);
+            int sb = rb, sj = rj;
+#pragma unroll
+            for (int u = 0; u < XB; ++u) {
+                if (gi[u] >= 0) {
+                    const float r = s.misc->rnorm[sb];
                     const float4 v = x[u];
-                    const uint2 gw = __ldg(reinterpret_cast<const uint2 *>(gain) + a4 + j);
-                    reinterpret_cast<uint2 *>(s.act + (size_t)b * apitch)[j] =
+                    const uint2 gw = __ldg(reinterpret_cast<const uint2 *>(gain) + a4 + sj);
+                    reinterpret_cast<uint2 *>(s.act)[sb * ap2 + sj] =
                         make_uint2(pack_bf2(v.x * r * bf_lo(gw.x), v.y * r * bf_hi(gw.x)),
                                    pack_bf2(v.z * r * bf_lo(gw.y), v.w * r * bf_hi(gw.y)));
                 }
+                for (sj += TS; sj >= n4; sj -= n4) ++sb;
             }
         }
         return;
@@ -830,32 +841,70 @@ __device__ void norm_prologue(const Params &p, Smem &s, const uint64_t *xbase, b
 /* O-projection and down-projection prologues: bf16 activations [k0, k1) of
  * rows of `len` elements (attention output, SwiGLU output), held two per
  * epoch-tagged word, copied as they are (two per word); waits for their
- * producers, CU word pairs per thread at a time over all sequences */
+ * producers, CU word pairs per thread at a time.  Up to 8 sequences, one
+ * sequence's slice per run of rounds; above 8, the items (sequence, word
+ * pair) of all of them run as one sequence of rounds, so that a round trip
+ * serves several sequences (measured on the 1.1B shape at context 64: 17 %
+ * faster at 16 sequences, 5 % slower at 2 and 8). */
 constexpr int CU = 8;
+template <int NB>
 __device__ void copy_prologue(const Params &p, Smem &s, const uint64_t *src0, int len, int k0, int k1, uint32_t f,
                               int task, int which, int ctid) {
     constexpr int TS = NCW * 32;
     const int kc = k1 - k0, n4 = kc / 4, apitch = smem_pitch(kc * 2, p.Bmax);
-    for (int b = 0; b < p.batch; ++b) {
-        /* word pair i of the slice holds elements k0 + 4 i .. k0 + 4 i + 3 */
-        const uint64_t *sb = src0 + ((size_t)b * len + k0) / 2;
-        uint2 *dst = reinterpret_cast<uint2 *>(s.act + (size_t)b * apitch);
-        for (int i0 = ctid; i0 < n4; i0 += CU * TS) {
+    if (NB > 1 && p.batch > 8) {
+        /* item i = b * n4 + j: word pair j of sequence b's slice, elements
+         * k0 + 4 j .. k0 + 4 j + 3.  A thread's items step by TS, so (b, j)
+         * advance without a division per item. */
+        const int T = p.batch * n4, ap2 = apitch / 8;
+        uint2 *act = reinterpret_cast<uint2 *>(s.act);
+        int b = ctid / n4, j = ctid - b * n4;
+        for (int i0 = ctid; i0 < T; i0 += CU * TS) {
+            const int rb = b, rj = j; /* the round's first item */
             ulonglong2 v[CU];
             uint32_t pend = 0u;
 #pragma unroll
             for (int u = 0; u < CU; ++u) {
-                const int i = i0 + u * TS;
-                v[u] = i < n4 ? ld_ll2(sb + 2 * (size_t)i) : ulonglong2{0ull, 0ull};
+                const bool in = i0 + u * TS < T;
+                v[u] = in ? ld_ll2(src0 + (b * len + k0) / 2 + 2 * j) : ulonglong2{0ull, 0ull};
+                if (in && !ll_ok(f, v[u])) pend |= 1u << u;
+                for (j += TS; j >= n4; j -= n4) ++b;
             }
-#pragma unroll
-            for (int u = 0; u < CU; ++u)
-                if (i0 + u * TS < n4 && !ll_ok(f, v[u])) pend |= 1u << u;
-            settle_all(p, s, v, pend, [=](int u) { return sb + 2 * (size_t)(i0 + u * TS); }, f, task, which);
+            /* (re-polls only: the item's place found again from the round's start) */
+            settle_all(p, s, v, pend, [=](int u) {
+                int bb = rb, jj = rj + u * TS;
+                for (; jj >= n4; jj -= n4) ++bb;
+                return src0 + (bb * len + k0) / 2 + 2 * jj;
+            }, f, task, which);
+            int sb = rb, sj = rj;
 #pragma unroll
             for (int u = 0; u < CU; ++u) {
-                const int i = i0 + u * TS;
-                if (i < n4) dst[i] = make_uint2((uint32_t)v[u].x, (uint32_t)v[u].y);
+                if (i0 + u * TS < T) act[sb * ap2 + sj] = make_uint2((uint32_t)v[u].x, (uint32_t)v[u].y);
+                for (sj += TS; sj >= n4; sj -= n4) ++sb;
+            }
+        }
+    } else {
+        for (int b = 0; b < p.batch; ++b) {
+            /* word pair i of the slice holds elements k0 + 4 i .. k0 + 4 i + 3 */
+            const uint64_t *sb = src0 + ((size_t)b * len + k0) / 2;
+            uint2 *dst = reinterpret_cast<uint2 *>(s.act + (size_t)b * apitch);
+            for (int i0 = ctid; i0 < n4; i0 += CU * TS) {
+                ulonglong2 v[CU];
+                uint32_t pend = 0u;
+#pragma unroll
+                for (int u = 0; u < CU; ++u) {
+                    const int i = i0 + u * TS;
+                    v[u] = i < n4 ? ld_ll2(sb + 2 * (size_t)i) : ulonglong2{0ull, 0ull};
+                }
+#pragma unroll
+                for (int u = 0; u < CU; ++u)
+                    if (i0 + u * TS < n4 && !ll_ok(f, v[u])) pend |= 1u << u;
+                settle_all(p, s, v, pend, [=](int u) { return sb + 2 * (size_t)(i0 + u * TS); }, f, task, which);
+#pragma unroll
+                for (int u = 0; u < CU; ++u) {
+                    const int i = i0 + u * TS;
+                    if (i < n4) dst[i] = make_uint2((uint32_t)v[u].x, (uint32_t)v[u].y);
+                }
             }
         }
     }
@@ -1645,7 +1694,7 @@ __device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring 
         if (norm)
             norm_prologue<NB>(p, s, src, emb, gain, k0, k1, kp == 0, f, ti, which, ctid, warp, lane);
         else
-            copy_prologue(p, s, src, len, k0, k1, f, ti, which, ctid);
+            copy_prologue<NB>(p, s, src, len, k0, k1, f, ti, which, ctid);
         if (cbar_or(s.misc->abort != 0)) return false;
         if (TRACE(p) && kp == 0 && ctid == 0) s.misc->t_pro = now_ns();
         ActChunk<WF> hv[wf_jmax(WF)];
