@@ -408,6 +408,55 @@ def level_times(trace, plan: "Plan") -> List[dict]:
     return out
 
 
+_PRODUCER = {"ATT": "QKV", "MRG": "ATT", "OPR": "MRG", "GUP": "OPR", "DWN": "GUP"}
+
+
+def prologue_lag(trace, plan: "Plan", layer: int) -> List[dict]:
+    """For every operator of one layer of a traced step, when its tasks got
+    their inputs: the end of each task's inputs-and-prologue phase minus
+    the end of the last task of the level it reads (the previous layer's
+    down projection for QKV, the merge level for the O projection, or the
+    attention level where a step has no merge tasks), as min / median / max
+    over the operator's tasks, in µs; and the median durations of its
+    prologue, tiles and epilogue phases.  A lag near the prologue's own
+    duration means the inputs were ready when the task began; a long lag
+    after every producer has finished is the prologue's own cost.
+    Arguments as for chrome_trace; ``layer`` >= 1."""
+    rows = iter(trace)
+    ends: Dict[tuple, int] = {}
+    tasks: Dict[str, List[tuple]] = {}
+    for sm in range(plan.n_sm):
+        for t in plan.tasks(sm):
+            r = [int(v) for v in next(rows)]
+            if r[0] == 0:
+                continue
+            key = (t["layer"], t["op"])
+            ends[key] = max(ends.get(key, 0), r[3])
+            if t["layer"] == layer:
+                tasks.setdefault(t["op"], []).append(r)
+
+    def med(v: List[float]) -> float:
+        v = sorted(v)
+        return (v[(len(v) - 1) // 2] + v[len(v) // 2]) / 2 if v else float("nan")
+
+    out = []
+    for op in ("QKV", "ATT", "MRG", "OPR", "GUP", "DWN"):
+        if op not in tasks:
+            continue
+        src = (layer - 1, "DWN") if op == "QKV" else (layer, _PRODUCER[op])
+        if src not in ends and op == "OPR":
+            src = (layer, "ATT")
+        if src not in ends:
+            continue
+        lag = [(r[6] - ends[src]) / 1e3 for r in tasks[op] if r[6] >= r[0] > 0]
+        out.append({"op": op, "after": src[1], "tasks": len(tasks[op]),
+                    "lag_min_us": min(lag), "lag_median_us": med(lag), "lag_max_us": max(lag),
+                    "prologue_us": med([(r[6] - r[0]) / 1e3 for r in tasks[op]]),
+                    "tiles_us": med([(r[7] - r[6]) / 1e3 for r in tasks[op]]),
+                    "epilogue_us": med([(r[8] - r[7]) / 1e3 for r in tasks[op]])})
+    return out
+
+
 class UnfusedEngine:
     """The same decode step as one kernel launch per operator
     (include/amk_unfused.h), for comparison with DecodeEngine on the same
