@@ -431,6 +431,30 @@ __device__ __forceinline__ AttGeo att_geo(const Params &p, const Task &t) {
     return a;
 }
 
+/* The stages of a GEMV task in order: stage rb holds the task's rows
+ * [rb·n/nst, (rb+1)·n/nst) (stage_rows), walked by additions, with one
+ * division per task instead of two 64-bit ones per stage. */
+struct StageWalk {
+    int q, r, nst, carry, end;
+    __device__ __forceinline__ StageWalk(int n, int nst_) : q(0), r(n), nst(nst_), carry(0), end(0) {
+        if (nst > 0) {
+            q = n / nst;
+            r = n - q * nst;
+        }
+    }
+    /* rows [a, e) of the next stage */
+    __device__ __forceinline__ void next(int &a, int &e) {
+        a = end;
+        end += q;
+        carry += r;
+        if (carry >= nst) {
+            carry -= nst;
+            ++end;
+        }
+        e = end;
+    }
+};
+
 __device__ __forceinline__ void load_task(const Task *src, Task &t) {
     const uint4 *s = reinterpret_cast<const uint4 *>(src);
     uint4 *d = reinterpret_cast<uint4 *>(&t);
@@ -606,9 +630,10 @@ __device__ void loader(const Params &p, Smem &s, int tbeg, int tend) {
         /* batch 1: rows back to back; larger batches: rows at the padded pitch */
         const size_t pitch = (size_t)smem_pitch((int)segb, p.Bmax);
         for (int kp = 0; kp < g.ks; ++kp) {
+            StageWalk sw(g.nrows, g.nrb);
             for (int rb = 0; rb < g.nrb; ++rb) {
                 int ra, re;
-                stage_rows(g.nrows, g.nrb, rb, ra, re);
+                sw.next(ra, re);
                 ra += t.r0;
                 re += t.r0;
                 const uint32_t bytes = (uint32_t)((re - ra) * segb);
@@ -1699,9 +1724,10 @@ __device__ bool gemv_task(const Params &p, Smem &s, const Task &t, int ti, Ring 
         if (TRACE(p) && kp == 0 && ctid == 0) s.misc->t_pro = now_ns();
         ActChunk<WF> hv[wf_jmax(WF)];
         if constexpr (NB == 1) act_regs<WF>(s.act, c0, c1, hv, lane);
+        StageWalk sw(g.nrows, g.nrb);
         for (int rb = 0; rb < g.nrb; ++rb) {
             int ra, re;
-            stage_rows(g.nrows, g.nrb, rb, ra, re);
+            sw.next(ra, re);
             for (int m = 0; m < g.nmat; ++m, rg.advance(NS)) {
                 const int sl = rg.slot;
                 const unsigned long long tw0 = TRACE(p) ? now_ns() : 0;
