@@ -4,6 +4,7 @@ candidate execution traces; the scores are only as good as the constants).
 
     python -m persistent_sm_decode_gb300.costfit measure campaign.jsonl   # GPU
     python -m persistent_sm_decode_gb300.costfit fit campaign.jsonl       # CPU
+    python -m persistent_sm_decode_gb300.costfit refit bench.json 12,14   # CPU
 
 `measure` times every point of POINTS (a workload, a batch and schedule
 options) with the device-filled inputs of bench.py and appends one JSON line
@@ -12,9 +13,14 @@ the simulation constants (amk_plan_simulate's fifteen) that minimise the
 squared log ratio of simulated to measured step time, each constant held
 within a factor e^bound of its physical first guess in FIRST_GUESS, prints
 the fitted table and, for every workload, the errors of a fit made without
-it.  The HBM rate stays at the measured copy rate.
+it.  The HBM rate stays at the measured copy rate.  `refit` takes the JSON
+line of a `bench.py` run instead, whose records are the default schedules,
+and refits only the listed constants, the others held at BUILT_IN (the
+library's built-in table): it brings a few constants up to date after a
+kernel change that leaves the schedules alone.
 """
 import json
+import math
 import sys
 from typing import List, Sequence
 
@@ -38,6 +44,11 @@ POINTS = [
 FIRST_GUESS = [1.5e-6, 0.5e-6, 0.4e-6, 0.6e-6, 7.5e10, 5.0e10, 6.5e12, 0.5e-6, 2.0e-12, 0.8e-6, 0.5e-6, 0.1e-6,
                0.6e-6, 1.5e11, 2.5e10]
 FITTED = [0, 1, 2, 3, 4, 5, 7, 8, 9, 10, 11, 12, 13, 14]  # [6], the HBM rate, is measured, not fitted
+
+# The library's built-in constants (COST_DEFAULT in amk_plan.cpp), in the
+# same order; a test checks that the two agree.
+BUILT_IN = [1.73e-6, 0.166e-6, 0.133e-6, 0.211e-6, 6.87e10, 2.67e10, 6.5e12, 1.5e-6, 6.01e-12, 1.93e-6, 1.5e-6,
+            0.247e-6, 0.339e-6, 3.55e11, 2.69e10]
 
 KNOBS = ("att_chunks", "slot_bytes", "n_slots", "ksplit", "task_order")
 
@@ -75,7 +86,6 @@ def measure(path: str, points=POINTS) -> None:
 
 
 def _constants(x: Sequence[float]) -> List[float]:
-    import math
     c = list(FIRST_GUESS)
     for i, v in zip(FITTED, x):
         c[i] = FIRST_GUESS[i] * math.exp(v)
@@ -127,10 +137,64 @@ def fit(path: str, bound: float = 1.1) -> List[float]:
     return c
 
 
+def bench_points(path: str):
+    """[(plan, measured µs, name)] of a bench.py JSON line (the last line of
+    the file): the headline and every sub-record that carries a schedule,
+    each planned on the host with the default search.  A record whose host
+    plan differs from the schedule it ran is left out, with a note."""
+    import synth
+    import persistent_sm_decode_gb300 as amk
+    d = json.loads([ln for ln in open(path) if ln.strip()][-1])
+    n_sm = d["schedule"]["n_sm"]
+    recs = [(d["config"]["workload"], d)] + [(k, v) for k, v in (d.get("workloads") or {}).items()
+                                             if "schedule" in v]
+    out = []
+    for key, r in recs:
+        name, B = r["config"]["workload"], int(r["config"]["batch"])
+        wl = synth.workload(name, batch=B)
+        plan = amk.Plan(_config(amk, wl, B), B, n_sm)
+        info = plan.info()
+        ran = r["schedule"]
+        if any(info[k] != ran[k] for k in ("att_chunks", "slot_bytes", "n_slots", "ksplit")):
+            print("left out %s: the host plan differs from the schedule it ran" % key)
+            continue
+        out.append((plan, r["ms_per_step"] * 1e3, "%s@%d" % (name, B)))
+    return out
+
+
+def refit(path: str, idx: Sequence[int], bound: float = 1.1) -> List[float]:
+    """Refit the constants `idx` to a bench.py line, the others held at
+    BUILT_IN; each fitted constant within a factor e^bound of its built-in
+    value.  Prints the errors before and after."""
+    import numpy as np
+    from scipy.optimize import least_squares
+    pts = bench_points(path)
+    idx = list(idx)
+
+    def consts(x):
+        c = list(BUILT_IN)
+        for i, v in zip(idx, x):
+            c[i] = BUILT_IN[i] * math.exp(v)
+        return c
+
+    res = lambda x: [math.log(p.simulate(consts(x)) / us) for p, us, _ in pts]
+    c = consts(least_squares(res, np.zeros(len(idx)), bounds=(-bound, bound), diff_step=0.05).x)
+    print("refitted:", ", ".join("[%d] %.3g -> %.3g" % (i, BUILT_IN[i], c[i]) for i in idx))
+    print("| workload | measured µs | built-in | refitted |")
+    print("|---|---|---|---|")
+    for p, us, name in pts:
+        a, b = p.simulate(BUILT_IN), p.simulate(c)
+        print("| %s | %.1f | %.1f (%+.1f %%) | %.1f (%+.1f %%) |" % (name, us, a, 100 * (a / us - 1), b,
+                                                                   100 * (b / us - 1)))
+    return c
+
+
 if __name__ == "__main__":
-    if len(sys.argv) < 3 or sys.argv[1] not in ("measure", "fit"):
+    if len(sys.argv) < 3 or sys.argv[1] not in ("measure", "fit", "refit"):
         sys.exit(__doc__)
     if sys.argv[1] == "measure":
         measure(sys.argv[2])
+    elif sys.argv[1] == "refit":
+        refit(sys.argv[2], [int(v) for v in sys.argv[3].split(",")] if len(sys.argv) > 3 else [12, 14])
     else:
         fit(sys.argv[2], float(sys.argv[3]) if len(sys.argv) > 3 else 1.1)

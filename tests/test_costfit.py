@@ -40,3 +40,23 @@ def test_fit_recovers_step_times_made_by_known_constants(amk):
         assert abs(math.log(p.simulate(fitted) / us)) < 0.02
     # and the untouched guess does not reproduce them: the test can fail
     assert max(abs(math.log(p.simulate(costfit.FIRST_GUESS) / us)) for p, us, _ in plans) > 0.05
+
+
+def test_built_in_table_matches_the_library(amk):
+    """costfit.BUILT_IN mirrors the library's COST_DEFAULT: a plan simulated
+    under it and under the built-in constants takes the same time, on a shape
+    where every constant enters (batch > 1, int8 at batch 1)."""
+    from persistent_sm_decode_gb300 import costfit
+    for name, B in (("tiny", 1), ("tiny", 4), ("tiny", 16)):
+        for wd in ("bf16", "int8"):
+            wl = synth.workload(name, batch=B, **({"weight_dtype": "int8"} if wd == "int8" else {}))
+            plan = amk.Plan(costfit._config(amk, wl, B), B, 16)
+            assert plan.simulate(costfit.BUILT_IN) == pytest.approx(plan.simulate(None), rel=1e-12)
+    # and a change of any one constant moves some simulated step
+    wl = synth.workload("tiny", batch=4)
+    plan = amk.Plan(costfit._config(amk, wl, 4), 4, 16)
+    base = plan.simulate(costfit.BUILT_IN)
+    for i in (0, 1, 2, 3, 7, 9, 10, 11, 12, 14):
+        c = list(costfit.BUILT_IN)
+        c[i] *= 2
+        assert plan.simulate(c) != pytest.approx(base, rel=1e-9), i
