@@ -60,3 +60,39 @@ def test_built_in_table_matches_the_library(amk):
         c = list(costfit.BUILT_IN)
         c[i] *= 2
         assert plan.simulate(c) != pytest.approx(base, rel=1e-9), i
+
+
+def test_refit_recovers_two_constants_from_a_bench_line(amk, tmp_path):
+    """costfit.refit on a bench.py-shaped JSON line whose step times the
+    simulation made under known values of [12] and [14]: the refit lands on
+    those values, and a record whose schedule differs from the host plan is
+    left out."""
+    import json
+    from persistent_sm_decode_gb300 import costfit
+    truth = list(costfit.BUILT_IN)
+    truth[12] *= 1.5
+    truth[14] *= 0.8
+    n_sm = 16
+
+    def record(B):
+        wl = synth.workload("tiny", batch=B)
+        plan = amk.Plan(costfit._config(amk, wl, B), B, n_sm)
+        info = plan.info()
+        return {"config": {"workload": "tiny", "batch": B}, "ms_per_step": plan.simulate(truth) / 1e3,
+                "schedule": {k: info[k] for k in ("att_chunks", "slot_bytes", "n_slots", "ksplit")}}
+
+    line = record(1)
+    line["schedule"]["n_sm"] = n_sm
+    subs = {"tiny@%d" % B: record(B) for B in (2, 4, 8, 16)}
+    stray = record(3)
+    stray["schedule"]["slot_bytes"] += 4096  # not what the host plans: left out
+    subs["tiny@3"] = stray
+    line["workloads"] = subs
+    path = tmp_path / "bench.json"
+    path.write_text("not json, a log line\n" + json.dumps(line) + "\n")
+    assert len(costfit.bench_points(str(path))) == 5
+    got = costfit.refit(str(path), [12, 14])
+    assert got[12] == pytest.approx(truth[12], rel=0.03)
+    assert got[14] == pytest.approx(truth[14], rel=0.03)
+    assert [got[i] for i in range(15) if i not in (12, 14)] == [costfit.BUILT_IN[i] for i in range(15)
+                                                                if i not in (12, 14)]
